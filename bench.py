@@ -1,0 +1,444 @@
+"""Benchmark of one paged-KV decode step on GB300.
+
+A step is the whole hot path for one layer of one decode batch:
+slot mapping -> KV store -> paged decode attention (partition + LSE merge)
+-> fused sampler, replayed as one CUDA graph.  Inputs are seeded synthetic
+tensors with the named workload's shapes, resident in HBM when timing
+starts; L2 is flushed (a 512 MB write) before every timed step, outside the
+timed events.
+
+Reported (one JSON line on rank 0):
+  value        algorithmic HBM GB/s of the step (bytes the method must move
+               / step time), unit GB/s; tokens_per_s = batch / step time
+  roofline     the attention call timed alone with CUDA events, against the
+               measured HBM copy peak
+  e2e          the same metric through the public API with host buffers:
+               pinned host -> device copy of the step's inputs, the step, and
+               device -> host copy of its outputs, all inside the timing
+  cpu_baseline the float64 oracle on a bounded sample, on the host cores
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config qwen3]
+    python bench.py --impl reference ...   (the oracle as the reference arm)
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+from workloads import configs  # noqa: E402
+
+METRIC = "decode-attention HBM GB/s (% of ~8 TB/s) and decode tokens/s per batch×ctx"
+DEFAULT_CONFIG = "qwen3"
+FLUSH_BYTES = 512 << 20
+KERNELS_PER_STEP = 5            # slot mapping, kv store, partition, merge, sampler
+
+
+# ----------------------------------------------------------------- bytes
+def algorithmic_bytes(cfg, layout):
+    """Bytes the method must move per step (each unique byte once)."""
+    s = cfg.itemsize
+    B, Hq, Hkv, D, bs = layout.num_seqs, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size
+    ctx = layout.context_lens.astype(np.int64)
+    nblk = -(-ctx // bs)
+    if cfg.table_kind == "shared_prefix":
+        prefix = cfg.ctx_args[0]
+        kv_tokens = prefix + int(np.sum(ctx - prefix))
+    else:
+        kv_tokens = int(ctx.sum())
+    attn = kv_tokens * 2 * Hkv * D * s + 2 * B * Hq * D * s + int(nblk.sum()) * 4 + 4 * B
+    store = 4 * B * Hkv * D * s + 8 * B
+    slots = B * (4 + 4 + 8)
+    sample = B * cfg.vocab * cfg.logits_itemsize + B * (4 + 4 + 4 + 8 + 8 + 4)
+    return {"attention": attn, "kv_store": store, "slot_mapping": slots, "sampler": sample,
+            "step": attn + store + slots + sample}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "paged_kv_decode_store_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.startswith("attention"):
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config_name):
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    was taken on the current attention sources."""
+    path = os.path.join(ROOT, "profiles", "attention_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    for ln in open(path):
+        parts = ln.split()
+        if len(parts) >= 3 and not ln.startswith("#") and parts[0] == want and parts[1] == config_name:
+            return int(parts[2])
+    return None
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = tempfile.mktemp(suffix=".csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in open(self.path):
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [x for x in sm if x >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- setup
+def build_step(cfg, device, path):
+    import paged_kv_decode_store_gb300 as pk
+    w = workloads.make_workload(cfg, device=device)
+    lay = w.layout
+    kc, vc = w.cache[0, lay.layer], w.cache[1, lay.layer]
+    step = pk.DecodeStep(kc, vc, lay.num_seqs, cfg.num_q_heads, lay.max_blocks_per_seq, lay.max_context_len,
+                         cfg.vocab, w.logits.dtype, w.scale, path=path)
+    host = {
+        "q": w.q, "k_new": w.k_new, "v_new": w.v_new,
+        "block_tables": torch.from_numpy(lay.block_tables).to(device),
+        "context_lens": torch.from_numpy(lay.context_lens).to(device),
+        "logits": w.logits,
+        "temperature": torch.from_numpy(w.temperature).to(device),
+        "top_k": torch.from_numpy(w.top_k).to(device),
+        "top_p": torch.from_numpy(w.top_p).to(device),
+        "seeds": torch.from_numpy(w.seeds.view(np.int64)).to(device),
+        "offsets": torch.from_numpy(w.offsets.view(np.int64)).to(device),
+    }
+    for k, v in host.items():
+        getattr(step, k).copy_(v)
+    return w, step, host
+
+
+def time_steps(step, flush, steps, stream):
+    """Per-step CUDA-event durations (ms) of graph replays, L2 flushed before each."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.add_(1)
+        starts[i].record(stream)
+        step.replay()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def time_attention(step, flush, steps, stream):
+    import paged_kv_decode_store_gb300 as pk
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.add_(1)
+        starts[i].record(stream)
+        pk.paged_decode_attention(step.q, step.k_cache, step.v_cache, step.block_tables, step.context_lens,
+                                  step.max_context_len, step.scale, out=step.out, workspace=step.workspace,
+                                  err=step.err, path=step.path)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def time_e2e(step, host_pinned, flush, steps, stream):
+    """Public-API step with host buffers: H2D inputs, replay, D2H outputs."""
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
+    tok_host = torch.empty(step.token_ids.shape, dtype=torch.int32, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_pinned.values())
+    d2h = out_host.numel() * out_host.element_size() + tok_host.numel() * 4
+    times = []
+    for i in range(steps):
+        flush.add_(1)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for k, t in host_pinned.items():
+            getattr(step, k).copy_(t, non_blocking=True)
+        step.replay()
+        out_host.copy_(step.out, non_blocking=True)
+        tok_host.copy_(step.token_ids, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        times.append((time.perf_counter() - t0) * 1e3)
+    return times, h2d, d2h
+
+
+# ----------------------------------------------------------------- oracle arm
+ORACLE_SCRIPT = r"""
+import json, sys, time
+sys.path.insert(0, sys.argv[1])
+import numpy as np
+import oracle
+d = np.load(sys.argv[2])
+budget = float(sys.argv[3])
+rows = int(d["q"].shape[0])
+t0 = time.perf_counter()
+done = 0
+for i in range(rows):
+    kc, vc = d["k%d" % i], d["v%d" % i]
+    tab = d["t%d" % i][None, :]
+    ctx = d["ctx"][i:i + 1]
+    slots = oracle.paging.decode_slot_mapping(tab, ctx, int(d["bs"]))
+    oracle.store.kv_store(d["knew"][i:i + 1], d["vnew"][i:i + 1], slots, kc, vc)
+    oracle.attention.decode_attention(d["q"][i:i + 1], kc, vc, tab, ctx, float(d["scale"]))
+    oracle.sampler.sample_row(d["logits"][i], float(d["temp"][i]), int(d["topk"][i]), float(d["topp"][i]),
+                              int(d["seeds"][i]), 0)
+    done += 1
+    if time.perf_counter() - t0 > budget:
+        break
+print(json.dumps({"rows": done, "seconds": time.perf_counter() - t0}))
+"""
+
+
+def oracle_sample(cfg, w, budget_s=15.0, max_rows=None):
+    """Run the float64 oracle on whole rows of the workload in a single-threaded
+    subprocess until ~budget_s; return (rows done, seconds, bytes of those rows)."""
+    lay = w.layout
+    B = lay.num_seqs if max_rows is None else min(max_rows, lay.num_seqs)
+    order = np.argsort(lay.context_lens[:B])[::-1]
+    order = np.concatenate([order[len(order) // 2:], order[:len(order) // 2]])  # mid-length rows first
+    arrays = {"bs": np.array(cfg.block_size), "scale": np.array(w.scale)}
+    sel = order[:B]
+    arrays["q"] = w.q[torch.from_numpy(sel.copy()).to(w.q.device)].double().cpu().numpy()
+    arrays["knew"] = w.k_new[torch.from_numpy(sel.copy()).to(w.q.device)].double().cpu().numpy()
+    arrays["vnew"] = w.v_new[torch.from_numpy(sel.copy()).to(w.q.device)].double().cpu().numpy()
+    arrays["logits"] = w.logits[torch.from_numpy(sel.copy()).to(w.q.device)].double().cpu().numpy()
+    arrays["ctx"] = lay.context_lens[sel]
+    arrays["temp"], arrays["topk"], arrays["topp"] = w.temperature[sel], w.top_k[sel], w.top_p[sel]
+    arrays["seeds"] = w.seeds[sel]
+    bs = cfg.block_size
+    for j, i in enumerate(sel):
+        n = -(-int(lay.context_lens[i]) // bs)
+        idx = torch.from_numpy(lay.block_tables[i, :n].astype(np.int64)).to(w.cache.device)
+        arrays["k%d" % j] = w.cache[0, lay.layer].index_select(0, idx).double().cpu().numpy()
+        arrays["v%d" % j] = w.cache[1, lay.layer].index_select(0, idx).double().cpu().numpy()
+        arrays["t%d" % j] = np.arange(n, dtype=np.int64)
+    fd, path = tempfile.mkstemp(suffix=".npz")
+    os.close(fd)
+    np.savez(path, **arrays)
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-c", ORACLE_SCRIPT, ROOT, path, str(budget_s)], capture_output=True,
+                       text=True, env=env)
+    os.unlink(path)
+    if r.returncode:
+        raise RuntimeError(r.stderr[-2000:])
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    done = res["rows"]
+    rows = sel[:done]
+    sub = workloads.Layout(lay.context_lens[rows], lay.block_tables[rows], lay.num_blocks, lay.layer,
+                           lay.max_context_len)
+    nbytes = algorithmic_bytes(cfg, sub)["step"]
+    return done, res["seconds"], nbytes
+
+
+# ----------------------------------------------------------------- main
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return ws, rank, local
+
+
+def max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_reference(args, cfg, ws, rank, local):
+    """The oracle, as it stands, as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    w = workloads.make_workload(cfg, device=f"cuda:{local}" if torch.cuda.is_available() else "cpu")
+    per_step = []
+    for _ in range(args.warmup):
+        oracle_sample(cfg, w, budget_s=min(5.0, args.cpu_seconds), max_rows=8)
+    rows_tot = secs_tot = bytes_tot = 0
+    for _ in range(args.steps):
+        done, secs, nbytes = oracle_sample(cfg, w, budget_s=args.cpu_seconds)
+        per_step.append(secs)
+        rows_tot += done
+        secs_tot += secs
+        bytes_tot += nbytes
+    value = bytes_tot / secs_tot / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs_tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_block(cfg, w.layout),
+            "tokens_per_s": rows_tot / secs_tot,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{rows_tot} whole rows (store + attention + sampler) over {args.steps} "
+                                       f"steps, ~{args.cpu_seconds:.0f} s each"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def config_block(cfg, lay):
+    ctx = lay.context_lens
+    return {"workload": cfg.description, "name": cfg.name, "batch": int(lay.num_seqs),
+            "ctx_mean": float(ctx.mean()), "ctx_max": int(ctx.max()), "q_heads": cfg.num_q_heads,
+            "kv_heads": cfg.num_kv_heads, "head_dim": cfg.head_dim, "block_size": cfg.block_size,
+            "vocab": cfg.vocab, "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MB write)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--path", default="auto", choices=["auto", "fma", "mma"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    cfg = configs.get(args.config)
+    ws, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        run_reference(args, cfg, ws, rank, local)
+        return
+
+    import paged_kv_decode_store_gb300 as pk
+    path = {"auto": pk.PATH_AUTO, "fma": pk.PATH_FMA, "mma": pk.PATH_MMA}[args.path]
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    w, step, host = build_step(cfg, dev, path)
+    lay = w.layout
+    nbytes = algorithmic_bytes(cfg, lay)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    step.capture()
+    for _ in range(args.warmup):
+        flush.add_(1)
+        step.replay()
+    time_attention(step, flush, 3, stream)
+    torch.cuda.synchronize()
+
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        step_ms = time_steps(step, flush, args.steps, stream)
+        attn_ms = time_attention(step, flush, args.steps, stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    total_ms = max_over_ranks(sum(step_ms), ws, dev)
+    attn_mean = max_over_ranks(statistics.mean(attn_ms), ws, dev)
+    clocks = clk.summary()
+
+    pinned = {k: (v.cpu().pin_memory()) for k, v in host.items()}
+    for _ in range(2):
+        time_e2e(step, pinned, flush, 1, stream)
+    e2e_ms, h2d, d2h = time_e2e(step, pinned, flush, args.steps, stream)
+    e2e_total = max_over_ranks(sum(e2e_ms), ws, dev)
+    err = int(step.err.item())
+
+    if rank != 0:
+        return
+    ms_per_step = total_ms / args.steps
+    value = ws * nbytes["step"] / (ms_per_step * 1e-3) / 1e9
+    peaks = {}
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        peaks = json.load(open(pk_path))
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or 6800.0
+    attn_gbs = nbytes["attention"] / (attn_mean * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic", "config": config_block(cfg, lay),
+        "tokens_per_s": ws * lay.num_seqs / (ms_per_step * 1e-3),
+        "step_bytes": nbytes["step"], "attention_bytes": nbytes["attention"],
+        "attention_ms": attn_mean, "attention_path": args.path,
+        "roofline": {"kernel": "paged_decode_attention (partition + LSE merge)", "bound": "hbm",
+                     "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
+                     "peak_source": peak_src, "traffic": recorded_traffic(cfg.name)},
+        "e2e": {"value": ws * nbytes["step"] / (e2e_total / args.steps * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_total / args.steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": KERNELS_PER_STEP * args.steps + 2 * args.steps,
+        "clocks": clocks, "device_err_flag": err,
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        done, secs, cbytes = oracle_sample(cfg, w, budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": cbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{done} whole rows of this workload (store + attention + sampler), "
+                                          f"{secs:.1f} s, single thread"}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

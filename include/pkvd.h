@@ -1,0 +1,213 @@
+/*
+ * pkvd.h -- C ABI of the paged KV-cache decode step for GB300 (sm_103a).
+ *
+ * One decode step of a paged-KV inference engine, as the pages describe it:
+ *
+ *   slot mapping   nano-vllm "Model Runner" notes, sections "prefill and
+ *                  decode" and "allocated kv cache" (slot = block_table
+ *                  [pos / block_size] * block_size + pos % block_size, with
+ *                  pos = context_len - 1 for the token decoded now).
+ *   kv_store       same notes, "prepare Prefill" / "allocated kv cache": the
+ *                  new token's K and V are written into its slot of the
+ *                  per-layer cache, in place (Grok-1 "第 8 章 runners.py
+ *                  推理引擎", section 8.4 donated buffers, section 8.5 cache
+ *                  shapes and updates).
+ *   attention      single-query grouped-query attention of the new token
+ *                  over the sequence's block table up to context_len (same
+ *                  notes, "prefill and decode"; Grok-1 section 8.5 GQA 48:8;
+ *                  Grok-1 section 8.2.3: an inactive row, context 0, gives a
+ *                  zero output).
+ *   sample         temperature, top-k, nucleus cut, Gumbel-max draw (Grok-1
+ *                  sections 8.3 and 8.3.1 sample_token / top_p_filter;
+ *                  nanochat "04 · Engine" section 3 top-k; nano-vllm "run
+ *                  model" Gumbel-max sampler).
+ *
+ * Conventions for every entry point:
+ *   - All tensor arguments are DEVICE pointers unless stated; sizes are
+ *     element counts; strides are in elements.  `stream` is a cudaStream_t
+ *     (NULL = legacy default stream).  Every call only enqueues work on
+ *     `stream` and returns; nothing synchronises, nothing allocates, no
+ *     state is kept between calls.  The caller owns every buffer, including
+ *     workspaces, and may capture the calls in a CUDA graph.
+ *   - Argument checks run on the host before anything is enqueued and return
+ *     a status code; the library never aborts, exits or traps.
+ *   - `err_flag`, where present, is an optional device int32.  Kernels OR
+ *     PKVD_ERR_* bits into it when they meet a bad index in device data
+ *     (e.g. a block id outside the pool) and skip the offending access.
+ *     The caller zeroes it and reads it back when it wants to know.
+ *   - dtype codes: PKVD_F32, PKVD_F16, PKVD_BF16.  q, the new K/V, the cache
+ *     and the attention output share one dtype.
+ */
+#ifndef PKVD_H
+#define PKVD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKVD_OK = 0,
+  PKVD_INVALID_ARG = 1,          /* null pointer, negative size, bad scale ... */
+  PKVD_UNSUPPORTED_DTYPE = 2,
+  PKVD_UNSUPPORTED_SHAPE = 3,    /* head_dim, group size, block size, alignment */
+  PKVD_WORKSPACE_TOO_SMALL = 4,
+  PKVD_CUDA_ERROR = 5            /* a CUDA runtime call failed (launch, query) */
+} pkvd_status;
+
+typedef enum { PKVD_F32 = 0, PKVD_F16 = 1, PKVD_BF16 = 2 } pkvd_dtype;
+
+/* Bits kernels OR into *err_flag. */
+#define PKVD_ERR_BLOCK_ID    1   /* block-table entry outside [0, num_blocks) */
+#define PKVD_ERR_SLOT        2   /* slot >= num_blocks * block_size           */
+#define PKVD_ERR_CONTEXT     4   /* context_len < 0 or > the stated bound     */
+#define PKVD_ERR_TIMEOUT     8   /* a pipeline wait gave up (never expected)  */
+
+/* Attention path selector for pkvd_paged_decode_attention_ex. */
+typedef enum {
+  PKVD_PATH_AUTO = 0,   /* the library's choice for the shape              */
+  PKVD_PATH_FMA = 1,    /* fp32 CUDA-core dot products                     */
+  PKVD_PATH_MMA = 2     /* tensor-core m16n8k16 over the query group       */
+} pkvd_attn_path;
+
+/*
+ * One layer's K and V cache, described without a copy.
+ *
+ * Element (block b, row r, kv head h, dim d) of K sits at
+ *   k_base + b*block_stride + r*token_stride + h*head_stride + d
+ * (same for V at v_base).  For nano-vllm's tensor
+ *   kv_cache[2, num_layers, num_blocks, block_size, num_kv_heads, head_dim]
+ * ("allocated kv cache") layer l is k_base = &kv_cache[0, l, 0, 0, 0, 0],
+ * v_base = &kv_cache[1, l, 0, 0, 0, 0], block_stride = block_size*H*D,
+ * token_stride = H*D, head_stride = D.
+ * Requirements: head_dim in {64, 128}; block_size a power of two >= 16;
+ * head_dim elements contiguous; base pointers and every stride times the
+ * element size multiples of 16 bytes.
+ */
+typedef struct {
+  void* k_base;
+  void* v_base;
+  int32_t dtype;          /* pkvd_dtype */
+  int32_t block_size;
+  int64_t num_blocks;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int64_t block_stride;
+  int64_t token_stride;
+  int64_t head_stride;
+} pkvd_cache;
+
+/* Human-readable text of a status code (static storage). */
+const char* pkvd_status_string(pkvd_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t pkvd_version(void);
+
+/*
+ * pkvd_slot_mapping -- slot of each row's new token.
+ *   slot_mapping[i] = block_tables[i*max_blocks_per_seq + (ctx_i-1)/block_size]
+ *                     * block_size + (ctx_i-1) % block_size,  ctx_i = context_lens[i]
+ *   and -1 where ctx_i == 0 (an inactive row).
+ * Inputs: block_tables int32 [num_seqs, max_blocks_per_seq] row-major;
+ *         context_lens int32 [num_seqs] (includes the new token).
+ * Output: slot_mapping int64 [num_seqs].
+ * Device errors: a block id outside [0, num_blocks) or a context longer than
+ * max_blocks_per_seq*block_size sets the matching bit and writes -1.
+ */
+pkvd_status pkvd_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,
+                              int32_t max_blocks_per_seq, const int32_t* context_lens,
+                              int32_t num_seqs, int32_t block_size, int64_t num_blocks,
+                              void* stream, int32_t* err_flag);
+
+/*
+ * pkvd_kv_store -- write each token's new K and V rows into its cache slot.
+ *   K[slot / bs, slot % bs, :, :] = k[i, :, :];  V[...] = v[i, :, :]
+ * an exact bit copy; rows with slot < 0 are skipped.
+ * Inputs: k, v [num_tokens, num_kv_heads, head_dim] contiguous, cache dtype;
+ *         slot_mapping int64 [num_tokens]; slots must be distinct.
+ * Device errors: slot >= num_blocks*block_size sets PKVD_ERR_SLOT, row skipped.
+ */
+pkvd_status pkvd_kv_store(const void* k, const void* v, const int64_t* slot_mapping,
+                          int32_t num_tokens, const pkvd_cache* cache, void* stream,
+                          int32_t* err_flag);
+
+/*
+ * Workspace bytes pkvd_paged_decode_attention needs for these sizes on a
+ * GPU with `sm_count` SMs (sm_count <= 0: query the current device).
+ * Host only; returns PKVD_CUDA_ERROR if the device query fails.
+ */
+pkvd_status pkvd_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                        int32_t head_dim, int32_t max_context_len,
+                                        int32_t sm_count, size_t* bytes);
+
+/*
+ * pkvd_paged_decode_attention -- one query token per sequence attends to
+ * its cached context.  For row i, query head h, kv head hk = h / G
+ * (G = num_q_heads / num_kv_heads, contiguous groups):
+ *   s_j = scale * <q[i,h,:], K_j>,  j < context_lens[i],
+ *   K_j = K[block_tables[i][j / bs], j % bs, hk, :]   (V_j likewise)
+ *   out[i,h,:] = sum_j softmax(s)_j V_j ;  zeros when context_lens[i] == 0.
+ * Inputs: q [num_seqs, num_q_heads, head_dim] contiguous, cache dtype;
+ *         block_tables int32 [num_seqs, max_blocks_per_seq]; context_lens
+ *         int32 [num_seqs], each <= max_context_len (a host-side bound used
+ *         for the launch shape; larger values set PKVD_ERR_CONTEXT and are
+ *         clamped).  Entries past a row's last block and cache rows past its
+ *         context are never read.
+ * Output: out [num_seqs, num_q_heads, head_dim], cache dtype, fp32 softmax
+ *         and accumulation.
+ * workspace: device scratch of at least pkvd_decode_workspace_bytes(...)
+ *         bytes (16-byte aligned), used for split-context partial results;
+ *         its contents need no initialisation.
+ * Requirements: num_q_heads % num_kv_heads == 0, group size <= 8,
+ *         num_kv_heads <= 8 or == 16.
+ */
+pkvd_status pkvd_paged_decode_attention(void* out, const void* q, const pkvd_cache* cache,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* context_lens, int32_t max_context_len,
+                                        int32_t num_seqs, int32_t num_q_heads, float scale,
+                                        void* workspace, size_t workspace_bytes,
+                                        void* stream, int32_t* err_flag);
+
+/* Same as pkvd_paged_decode_attention with an explicit compute path
+ * (pkvd_attn_path); PKVD_UNSUPPORTED_SHAPE if the path cannot run the shape. */
+pkvd_status pkvd_paged_decode_attention_ex(void* out, const void* q, const pkvd_cache* cache,
+                                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                           const int32_t* context_lens, int32_t max_context_len,
+                                           int32_t num_seqs, int32_t num_q_heads, float scale,
+                                           void* workspace, size_t workspace_bytes,
+                                           void* stream, int32_t* err_flag, int32_t path);
+
+/* Workspace bytes pkvd_sample needs (host only; currently always 0). */
+pkvd_status pkvd_sample_workspace_bytes(int32_t num_rows, int32_t vocab, size_t* bytes);
+
+/*
+ * pkvd_sample -- one token id per row of logits.
+ * Row r (x = logits[r*row_stride : r*row_stride + vocab]):
+ *   T = temperature[r] == 0  ->  argmax x (lowest index on ties).
+ *   otherwise x' = x / T; keep the top_k[r] largest (exactly k, lowest index
+ *   first among equal values; k <= 0 or k >= vocab keeps all); if top_p[r] < 1
+ *   keep the smallest descending prefix of the kept set whose renormalised
+ *   probability mass exceeds top_p[r], plus every id equal to its last value;
+ *   token = argmax over kept j of x'_j + g_j, g_j = -log(-log u_j), with
+ *   u_j = ((w_j >> 9) + 0.5) * 2^-23 and w_j word (j % 4) of Philox4x32-10
+ *   (Salmon et al., SC'11) at key (lo32(seeds[r]), hi32(seeds[r])) and
+ *   counter (j / 4, lo32(offsets[r]), hi32(offsets[r]), 0).
+ * Inputs: logits (dtype) rows of `vocab` elements `row_stride` apart;
+ *         temperature f32 [num_rows] (>= 0), top_k int32, top_p f32,
+ *         seeds u64, offsets u64, all [num_rows] device arrays.
+ * Output: token_ids int32 [num_rows].
+ * Requirements: 1 <= vocab <= 2^23.  NaN logits give unspecified ids.
+ */
+pkvd_status pkvd_sample(int32_t* token_ids, const void* logits, int32_t dtype,
+                        int32_t num_rows, int32_t vocab, int64_t row_stride,
+                        const float* temperature, const int32_t* top_k, const float* top_p,
+                        const uint64_t* seeds, const uint64_t* offsets,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKVD_H */

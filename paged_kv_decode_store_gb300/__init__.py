@@ -1,0 +1,97 @@
+"""GB300 paged-KV decode step: Python binding of the libpkvd C ABI.
+
+The functions below only marshal torch tensors into the C calls declared in
+``include/pkvd.h``; every step of the decode path runs in the library's CUDA
+kernels.  If ``libpkvd.so`` has not been built, every call raises.
+
+    slot_mapping(block_tables, context_lens, block_size, num_blocks)
+    kv_store(k, v, slot_mapping, k_cache, v_cache)
+    paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens,
+                           max_context_len, scale)
+    sample(logits, temperature, top_k, top_p, seeds, offsets)
+    DecodeStep(...)   -- the four calls captured in one CUDA graph
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from ._capi import (LIB_PATH, PATH_AUTO, PATH_FMA, PATH_MMA, ERR_BLOCK_ID, ERR_SLOT,  # noqa: F401
+                    ERR_CONTEXT, ERR_TIMEOUT, PkvdCache, PkvdError, lib, check, dtype_code,
+                    stream_handle, cache_desc, ptr)
+from .step import DecodeStep  # noqa: F401
+
+__all__ = ["slot_mapping", "kv_store", "paged_decode_attention", "decode_workspace_bytes",
+           "sample", "DecodeStep", "PkvdError", "lib"]
+
+
+def _err_ptr(err):
+    return ptr(err) if err is not None else None
+
+
+def slot_mapping(block_tables: torch.Tensor, context_lens: torch.Tensor, block_size: int,
+                 num_blocks: int, out: torch.Tensor | None = None, err: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """int64 slot of each row's new token (-1 for an empty row)."""
+    B = context_lens.shape[0]
+    if out is None:
+        out = torch.empty(B, dtype=torch.int64, device=context_lens.device)
+    check(lib().pkvd_slot_mapping(ptr(out), ptr(block_tables), block_tables.shape[1],
+                                  ptr(context_lens), B, block_size, num_blocks,
+                                  stream_handle(stream, out), _err_ptr(err)))
+    return out
+
+
+def kv_store(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+             k_cache: torch.Tensor, v_cache: torch.Tensor, err: torch.Tensor | None = None,
+             stream=None) -> None:
+    """Write k[i], v[i] ([N, Hkv, D], contiguous) into slot_mapping[i] of the caches
+    ([num_blocks, block_size, Hkv, D] views, modified in place)."""
+    c = cache_desc(k_cache, v_cache)
+    check(lib().pkvd_kv_store(ptr(k), ptr(v), ptr(slot_mapping), k.shape[0], ctypes.byref(c),
+                              stream_handle(stream, k), _err_ptr(err)))
+
+
+def decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int, max_context_len: int,
+                           sm_count: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    check(lib().pkvd_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len,
+                                            sm_count, ctypes.byref(n)))
+    return int(n.value)
+
+
+def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor,
+                           max_context_len: int, scale: float, out: torch.Tensor | None = None,
+                           workspace: torch.Tensor | None = None, err: torch.Tensor | None = None,
+                           stream=None, path: int = PATH_AUTO) -> torch.Tensor:
+    """out[i, h] = softmax(scale * q[i, h] . K_i^T) V_i over row i's paged context."""
+    B, Hq, D = q.shape
+    c = cache_desc(k_cache, v_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = decode_workspace_bytes(B, Hq, D, max_context_len)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    check(lib().pkvd_paged_decode_attention_ex(
+        ptr(out), ptr(q), ctypes.byref(c), ptr(block_tables), block_tables.shape[1],
+        ptr(context_lens), max_context_len, B, Hq, ctypes.c_float(scale), ptr(workspace),
+        workspace.numel() * workspace.element_size(), stream_handle(stream, q), _err_ptr(err), path))
+    return out
+
+
+def sample(logits: torch.Tensor, temperature: torch.Tensor, top_k: torch.Tensor,
+           top_p: torch.Tensor, seeds: torch.Tensor, offsets: torch.Tensor,
+           out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """int32 token id per row: temperature, top-k, nucleus cut, Philox Gumbel-max."""
+    R, V = logits.shape
+    if logits.stride(1) != 1:
+        raise ValueError("logits rows must be contiguous")
+    if out is None:
+        out = torch.empty(R, dtype=torch.int32, device=logits.device)
+    check(lib().pkvd_sample(ptr(out), ptr(logits), dtype_code(logits.dtype), R, V, logits.stride(0),
+                            ptr(temperature), ptr(top_k), ptr(top_p), ptr(seeds), ptr(offsets),
+                            None, 0, stream_handle(stream, logits)))
+    return out

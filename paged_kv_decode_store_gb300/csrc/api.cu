@@ -1,0 +1,192 @@
+// The C ABI (include/pkvd.h): host-side argument checks, then one launcher
+// call per entry point.  Nothing here allocates, synchronises or keeps state
+// beyond a per-device SM-count cache.
+#include <cmath>
+
+#include "launch.h"
+
+namespace pkvd {
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+}  // namespace pkvd
+
+using namespace pkvd;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int esize(int dtype) { return dtype == PKVD_F32 ? 4 : 2; }
+
+bool valid_dtype(int dtype) { return dtype == PKVD_F32 || dtype == PKVD_F16 || dtype == PKVD_BF16; }
+
+bool pow2(long long x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// Shared checks of a cache descriptor; `for_attention` adds the layout rules
+// the bulk-copy pipeline needs.
+pkvd_status check_cache(const pkvd_cache* c, bool for_attention) {
+  if (!c || !c->k_base || !c->v_base) return PKVD_INVALID_ARG;
+  if (!valid_dtype(c->dtype)) return PKVD_UNSUPPORTED_DTYPE;
+  if (c->num_blocks <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0 || c->block_size <= 0)
+    return PKVD_INVALID_ARG;
+  if (c->head_dim != 64 && c->head_dim != 128) return PKVD_UNSUPPORTED_SHAPE;
+  if (!pow2(c->block_size)) return PKVD_UNSUPPORTED_SHAPE;
+  if (for_attention && c->block_size < 16) return PKVD_UNSUPPORTED_SHAPE;
+  if (c->block_stride <= 0 || c->token_stride <= 0 || c->head_stride < c->head_dim)
+    return PKVD_INVALID_ARG;
+  const int e = esize(c->dtype);
+  if (!aligned16(c->k_base) || !aligned16(c->v_base)) return PKVD_UNSUPPORTED_SHAPE;
+  if ((c->block_stride * e) % 16 || (c->token_stride * e) % 16 || (c->head_stride * e) % 16)
+    return PKVD_UNSUPPORTED_SHAPE;
+  return PKVD_OK;
+}
+
+pkvd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PKVD_OK : PKVD_CUDA_ERROR; }
+
+}  // namespace
+
+extern "C" {
+
+const char* pkvd_status_string(pkvd_status s) {
+  switch (s) {
+    case PKVD_OK: return "ok";
+    case PKVD_INVALID_ARG: return "invalid argument";
+    case PKVD_UNSUPPORTED_DTYPE: return "unsupported dtype";
+    case PKVD_UNSUPPORTED_SHAPE: return "unsupported shape or alignment";
+    case PKVD_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case PKVD_CUDA_ERROR: return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+int32_t pkvd_version(void) { return 100; }
+
+pkvd_status pkvd_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, int32_t num_seqs, int32_t block_size,
+                              int64_t num_blocks, void* stream, int32_t* err_flag) {
+  if (num_seqs < 0 || block_size <= 0 || num_blocks <= 0) return PKVD_INVALID_ARG;
+  if (num_seqs == 0) return PKVD_OK;
+  if (!slot_mapping || !block_tables || !context_lens || max_blocks_per_seq <= 0) return PKVD_INVALID_ARG;
+  return from_cuda(launch_slot_mapping(slot_mapping, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                                       block_size, num_blocks, static_cast<cudaStream_t>(stream), err_flag));
+}
+
+pkvd_status pkvd_kv_store(const void* k, const void* v, const int64_t* slot_mapping, int32_t num_tokens,
+                          const pkvd_cache* cache, void* stream, int32_t* err_flag) {
+  if (num_tokens < 0) return PKVD_INVALID_ARG;
+  const pkvd_status cs = check_cache(cache, false);
+  if (cs != PKVD_OK) return cs;
+  if (num_tokens == 0) return PKVD_OK;
+  if (!k || !v || !slot_mapping) return PKVD_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v)) return PKVD_UNSUPPORTED_SHAPE;
+  return from_cuda(launch_kv_store(k, v, slot_mapping, num_tokens, *cache, esize(cache->dtype),
+                                   static_cast<cudaStream_t>(stream), err_flag));
+}
+
+pkvd_status pkvd_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                        int32_t max_context_len, int32_t sm_count, size_t* bytes) {
+  if (!bytes || num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0) return PKVD_INVALID_ARG;
+  if (sm_count <= 0) sm_count = device_sm_count();
+  if (sm_count <= 0) return PKVD_CUDA_ERROR;
+  const int grid = attention_grid(num_seqs, max_context_len, sm_count);
+  *bytes = attention_workspace_bytes(num_seqs, num_q_heads, head_dim, grid);
+  return PKVD_OK;
+}
+
+pkvd_status pkvd_paged_decode_attention_ex(void* out, const void* q, const pkvd_cache* cache,
+                                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                           const int32_t* context_lens, int32_t max_context_len,
+                                           int32_t num_seqs, int32_t num_q_heads, float scale,
+                                           void* workspace, size_t workspace_bytes, void* stream,
+                                           int32_t* err_flag, int32_t path) {
+  if (num_seqs < 0 || num_q_heads <= 0 || max_context_len < 0 || !std::isfinite(scale)) return PKVD_INVALID_ARG;
+  const pkvd_status cs = check_cache(cache, true);
+  if (cs != PKVD_OK) return cs;
+  if (num_q_heads % cache->num_kv_heads) return PKVD_UNSUPPORTED_SHAPE;
+  const int G = num_q_heads / cache->num_kv_heads;
+  if (path == PKVD_PATH_AUTO) path = attention_default_path(cache->dtype, cache->head_dim, cache->num_kv_heads, G);
+  if (path != PKVD_PATH_FMA && path != PKVD_PATH_MMA) {
+    if (path == 0) return PKVD_UNSUPPORTED_SHAPE;
+    return PKVD_INVALID_ARG;
+  }
+  if (!attention_path_supported(path, cache->dtype, cache->head_dim, cache->num_kv_heads, G))
+    return PKVD_UNSUPPORTED_SHAPE;
+  if (num_seqs == 0) return PKVD_OK;
+  if (!out || !q || !block_tables || !context_lens || max_blocks_per_seq <= 0) return PKVD_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q)) return PKVD_UNSUPPORTED_SHAPE;
+  const int sms = device_sm_count();
+  if (sms <= 0) return PKVD_CUDA_ERROR;
+  const int grid = attention_grid(num_seqs, max_context_len, sms);
+  const size_t need = attention_workspace_bytes(num_seqs, num_q_heads, cache->head_dim, grid);
+  if (!workspace || workspace_bytes < need) return PKVD_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return PKVD_UNSUPPORTED_SHAPE;
+  AttnArgs a;
+  a.out = out;
+  a.q = q;
+  a.k_base = cache->k_base;
+  a.v_base = cache->v_base;
+  a.block_stride = cache->block_stride;
+  a.token_stride = cache->token_stride;
+  a.head_stride = cache->head_stride;
+  a.num_blocks = cache->num_blocks;
+  a.block_size = cache->block_size;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.num_q_heads = num_q_heads;
+  a.head_dim = cache->head_dim;
+  a.dtype = cache->dtype;
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.context_lens = context_lens;
+  a.max_context_len = max_context_len;
+  a.num_seqs = num_seqs;
+  a.scale = scale;
+  a.workspace = workspace;
+  a.err = err_flag;
+  a.grid = grid;
+  a.path = path;
+  return from_cuda(launch_attention(a, static_cast<cudaStream_t>(stream)));
+}
+
+pkvd_status pkvd_paged_decode_attention(void* out, const void* q, const pkvd_cache* cache,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* context_lens, int32_t max_context_len, int32_t num_seqs,
+                                        int32_t num_q_heads, float scale, void* workspace, size_t workspace_bytes,
+                                        void* stream, int32_t* err_flag) {
+  return pkvd_paged_decode_attention_ex(out, q, cache, block_tables, max_blocks_per_seq, context_lens,
+                                        max_context_len, num_seqs, num_q_heads, scale, workspace, workspace_bytes,
+                                        stream, err_flag, PKVD_PATH_AUTO);
+}
+
+pkvd_status pkvd_sample_workspace_bytes(int32_t num_rows, int32_t vocab, size_t* bytes) {
+  if (!bytes || num_rows < 0 || vocab <= 0) return PKVD_INVALID_ARG;
+  *bytes = 0;
+  return PKVD_OK;
+}
+
+pkvd_status pkvd_sample(int32_t* token_ids, const void* logits, int32_t dtype, int32_t num_rows, int32_t vocab,
+                        int64_t row_stride, const float* temperature, const int32_t* top_k, const float* top_p,
+                        const uint64_t* seeds, const uint64_t* offsets, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (!valid_dtype(dtype)) return PKVD_UNSUPPORTED_DTYPE;
+  if (num_rows < 0 || vocab <= 0 || row_stride < vocab) return PKVD_INVALID_ARG;
+  if (vocab > (1 << 23)) return PKVD_UNSUPPORTED_SHAPE;
+  if (num_rows == 0) return PKVD_OK;
+  if (!token_ids || !logits || !temperature || !top_k || !top_p || !seeds || !offsets) return PKVD_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(logits) % esize(dtype)) return PKVD_UNSUPPORTED_SHAPE;
+  return from_cuda(launch_sample(token_ids, logits, dtype, num_rows, vocab, row_stride, temperature, top_k, top_p,
+                                 seeds, offsets, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// Internal launchers shared between the kernel translation units and the
+// C-ABI layer (api.cu).  Host-side argument validation happens in api.cu;
+// these functions only size grids and enqueue kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pkvd.h"
+
+namespace pkvd {
+
+// Decode-attention launch geometry shared by the workspace query and the
+// launcher, so both derive the same grid.
+constexpr int kChunk = 16;            // tokens per pipeline stage
+constexpr int kConsumerWarps = 8;
+constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
+
+struct AttnArgs {
+  void* out;
+  const void* q;
+  const void* k_base;
+  const void* v_base;
+  int64_t block_stride, token_stride, head_stride;  // elements
+  int64_t num_blocks;
+  int block_size;
+  int num_kv_heads;
+  int num_q_heads;
+  int head_dim;
+  int dtype;
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  const int32_t* context_lens;
+  int max_context_len;
+  int num_seqs;
+  float scale;
+  void* workspace;
+  int32_t* err;
+  int grid;           // partition CTAs
+  int path;           // PKVD_PATH_FMA / PKVD_PATH_MMA (resolved)
+};
+
+int attention_grid(int num_seqs, int max_context_len, int sm_count);
+size_t attention_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int grid);
+bool attention_path_supported(int path, int dtype, int head_dim, int num_kv_heads, int group);
+int attention_default_path(int dtype, int head_dim, int num_kv_heads, int group);
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
+
+cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* tables, int max_blocks,
+                                const int32_t* ctx, int num_seqs, int block_size,
+                                int64_t num_blocks, cudaStream_t stream, int32_t* err);
+
+cudaError_t launch_kv_store(const void* k, const void* v, const int64_t* slots, int num_tokens,
+                            const pkvd_cache& c, int elem_bytes, cudaStream_t stream,
+                            int32_t* err);
+
+cudaError_t launch_sample(int32_t* token_ids, const void* logits, int dtype, int num_rows,
+                          int vocab, int64_t row_stride, const float* temperature,
+                          const int32_t* top_k, const float* top_p, const uint64_t* seeds,
+                          const uint64_t* offsets, cudaStream_t stream);
+
+int device_sm_count();   // current device, cached; <= 0 on failure
+
+}  // namespace pkvd

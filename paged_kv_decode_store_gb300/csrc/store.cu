@@ -1,0 +1,102 @@
+// Slot mapping and the paged KV-cache store.
+//
+// nano-vllm "Model Runner" notes, sections "prefill and decode" and
+// "allocated kv cache": the token decoded now is position context_len - 1;
+// it lives in physical block block_table[pos / block_size] at row
+// pos % block_size, i.e. slot = physical * block_size + pos % block_size,
+// and its K and V rows are written there in place (the donated-buffer
+// update of Grok-1 "第 8 章 runners.py 推理引擎", section 8.4).
+//
+// Both kernels are latency bound (a few KB per step): one warp-sized pass
+// over rows, 16-byte vector copies, 64-bit cache offsets.
+#include "common.cuh"
+#include "launch.h"
+
+namespace pkvd {
+
+__global__ void slot_mapping_kernel(int64_t* __restrict__ slots, const int32_t* __restrict__ tables,
+                                    int max_blocks, const int32_t* __restrict__ ctx, int num_seqs,
+                                    int block_size, int64_t num_blocks, int32_t* err) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= num_seqs) return;
+  const int c = ctx[i];
+  int64_t slot = -1;
+  if (c < 0) {
+    flag_error(err, PKVD_ERR_CONTEXT);
+  } else if (c > 0) {
+    const int pos = c - 1;
+    const int logical = pos / block_size;
+    if (logical >= max_blocks) {
+      flag_error(err, PKVD_ERR_CONTEXT);
+    } else {
+      const int phys = tables[(int64_t)i * max_blocks + logical];
+      if (phys < 0 || phys >= num_blocks) {
+        flag_error(err, PKVD_ERR_BLOCK_ID);
+      } else {
+        slot = (int64_t)phys * block_size + pos % block_size;
+      }
+    }
+  }
+  slots[i] = slot;
+}
+
+// One CTA per token row; threads stride over the 16-byte vectors of the K
+// row and then the V row.  Element e of a row is (head e / D, dim e % D).
+__global__ void kv_store_kernel(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v,
+                                const int64_t* __restrict__ slots, uint8_t* __restrict__ kc,
+                                uint8_t* __restrict__ vc, int64_t num_blocks, int block_size,
+                                int num_heads, int head_dim, int64_t block_stride,
+                                int64_t token_stride, int64_t head_stride, int elem_bytes,
+                                int32_t* err) {
+  const int tok = blockIdx.x;
+  const int64_t slot = slots[tok];
+  if (slot < 0) return;
+  if (slot >= num_blocks * block_size) {
+    if (threadIdx.x == 0) flag_error(err, PKVD_ERR_SLOT);
+    return;
+  }
+  const int64_t blk = slot / block_size;
+  const int64_t row = slot % block_size;
+  const int64_t base = blk * block_stride + row * token_stride;   // elements
+  const int vec_elems = 16 / elem_bytes;
+  const int row_elems = num_heads * head_dim;
+  const int nvec = row_elems / vec_elems;
+  const uint4* ksrc = reinterpret_cast<const uint4*>(k + (int64_t)tok * row_elems * elem_bytes);
+  const uint4* vsrc = reinterpret_cast<const uint4*>(v + (int64_t)tok * row_elems * elem_bytes);
+  for (int idx = threadIdx.x; idx < 2 * nvec; idx += blockDim.x) {
+    const int which = idx >= nvec;
+    const int vi = which ? idx - nvec : idx;
+    const int e = vi * vec_elems;
+    const int h = e / head_dim, d = e % head_dim;
+    const int64_t off = (base + h * head_stride + d) * elem_bytes;
+    const uint4 val = which ? __ldg(vsrc + vi) : __ldg(ksrc + vi);
+    *reinterpret_cast<uint4*>((which ? vc : kc) + off) = val;
+  }
+}
+
+cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* tables, int max_blocks,
+                                const int32_t* ctx, int num_seqs, int block_size,
+                                int64_t num_blocks, cudaStream_t stream, int32_t* err) {
+  if (num_seqs == 0) return cudaSuccess;
+  const int threads = 128;
+  slot_mapping_kernel<<<(num_seqs + threads - 1) / threads, threads, 0, stream>>>(
+      slots, tables, max_blocks, ctx, num_seqs, block_size, num_blocks, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_store(const void* k, const void* v, const int64_t* slots, int num_tokens,
+                            const pkvd_cache& c, int elem_bytes, cudaStream_t stream,
+                            int32_t* err) {
+  if (num_tokens == 0) return cudaSuccess;
+  const int nvec = c.num_kv_heads * c.head_dim * elem_bytes / 16;
+  int threads = 2 * nvec;
+  threads = threads < 64 ? 64 : (threads > 256 ? 256 : threads);
+  kv_store_kernel<<<num_tokens, threads, 0, stream>>>(
+      static_cast<const uint8_t*>(k), static_cast<const uint8_t*>(v), slots,
+      static_cast<uint8_t*>(c.k_base), static_cast<uint8_t*>(c.v_base), c.num_blocks,
+      c.block_size, c.num_kv_heads, c.head_dim, c.block_stride, c.token_stride, c.head_stride,
+      elem_bytes, err);
+  return cudaGetLastError();
+}
+
+}  // namespace pkvd

@@ -1,0 +1,105 @@
+"""The C-ABI library loads, exports every symbol pkvd.h declares, and its
+host-side checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "pkvd.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_decode_store_gb300 as pk
+    return pk.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkvd_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), n
+    from paged_kv_decode_store_gb300 import _capi
+    assert set(_capi.SIGNATURES) == set(names)
+
+
+def test_status_strings_and_version(L):
+    assert L.pkvd_status_string(0) == b"ok"
+    assert L.pkvd_status_string(4) == b"workspace too small"
+    assert L.pkvd_version() >= 100
+
+
+def _cache(**kw):
+    from paged_kv_decode_store_gb300._capi import PkvdCache
+    c = PkvdCache()
+    c.k_base, c.v_base = 1 << 20, 2 << 20          # fake, aligned, never dereferenced
+    c.dtype, c.block_size, c.num_blocks, c.num_kv_heads, c.head_dim = 2, 16, 64, 8, 128
+    c.block_stride, c.token_stride, c.head_stride = 16 * 8 * 128, 8 * 128, 128
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def _attn(L, cache, hq=48, ws=1 << 20, path=0, num_seqs=4, scale=0.088):
+    return L.pkvd_paged_decode_attention_ex(1 << 21, 1 << 22, ctypes.byref(cache), 1 << 23, 8, 1 << 24,
+                                            128, num_seqs, hq, ctypes.c_float(scale), 1 << 25, ws, None,
+                                            None, path)
+
+
+def test_attention_host_checks(L):
+    assert _attn(L, _cache(), hq=44) == 3                    # 44 % 8 != 0
+    assert _attn(L, _cache(), hq=8 * 9) == 3                 # group 9 > 8
+    assert _attn(L, _cache(head_dim=96)) == 3
+    assert _attn(L, _cache(block_size=24)) == 3              # not a power of two
+    assert _attn(L, _cache(block_size=8)) == 3               # below one 16-token chunk
+    assert _attn(L, _cache(dtype=7)) == 2
+    assert _attn(L, _cache(k_base=0)) == 1
+    assert _attn(L, _cache(token_stride=8 * 128 + 3)) == 3   # 16-byte rule
+    assert _attn(L, _cache(), scale=float("nan")) == 1
+    assert _attn(L, _cache(dtype=0), path=2) == 3             # no tensor-core path for fp32
+    assert _attn(L, _cache(num_kv_heads=4, block_stride=16 * 4 * 128, token_stride=4 * 128), hq=16,
+                 path=2) == 3
+    assert _attn(L, _cache(), path=9) == 1
+    assert _attn(L, _cache(), num_seqs=0) == 0               # nothing to do, nothing launched
+
+
+def test_workspace_query_is_host_only(L):
+    n = ctypes.c_size_t(0)
+    assert L.pkvd_decode_workspace_bytes(32, 48, 128, 2048, 152, ctypes.byref(n)) == 0
+    grid = min(152, 32 * 128)
+    prefix = ((33 * 4 + 255) // 256) * 256
+    assert n.value == prefix + grid * 2 * 48 * 130 * 4
+    assert L.pkvd_decode_workspace_bytes(4, 4, 64, 50, 152, ctypes.byref(n)) == 0
+    assert n.value == 256 + min(152, 4 * 4) * 2 * 4 * 66 * 4
+    assert L.pkvd_decode_workspace_bytes(4, 4, 64, 0, 152, ctypes.byref(n)) == 0
+    assert n.value == 256
+    assert L.pkvd_decode_workspace_bytes(-1, 4, 64, 50, 152, ctypes.byref(n)) == 1
+
+
+def test_store_slot_and_sample_host_checks(L):
+    c = _cache()
+    assert L.pkvd_kv_store(1 << 20, 1 << 21, 1 << 22, -1, ctypes.byref(c), None, None) == 1
+    assert L.pkvd_kv_store(1 << 20, 1 << 21, 1 << 22, 0, ctypes.byref(c), None, None) == 0
+    assert L.pkvd_kv_store(1 << 20, (1 << 21) + 8, 1 << 22, 3, ctypes.byref(c), None, None) == 3
+    assert L.pkvd_kv_store(1 << 20, 1 << 21, 1 << 22, 3, ctypes.byref(_cache(head_dim=32)), None, None) == 3
+    assert L.pkvd_slot_mapping(1 << 20, 1 << 21, 4, 1 << 22, 0, 16, 64, None, None) == 0
+    assert L.pkvd_slot_mapping(1 << 20, 1 << 21, 4, 1 << 22, 2, 0, 64, None, None) == 1
+    args = [1 << 20, 1 << 21]
+    tail = [1 << 22] * 5 + [None, 0, None]
+    assert L.pkvd_sample(*args, 3, 4, 100, 100, *tail) == 2           # dtype
+    assert L.pkvd_sample(*args, 2, 4, 100, 99, *tail) == 1            # row_stride < vocab
+    assert L.pkvd_sample(*args, 2, 4, (1 << 23) + 1, (1 << 23) + 1, *tail) == 3
+    assert L.pkvd_sample(*args, 2, 0, 100, 100, *tail) == 0
+    n = ctypes.c_size_t(7)
+    assert L.pkvd_sample_workspace_bytes(4, 100, ctypes.byref(n)) == 0 and n.value == 0

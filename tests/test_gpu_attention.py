@@ -1,0 +1,139 @@
+"""Paged decode attention on the GPU against the float64 oracle.
+
+Tolerances: max abs error <= 1e-4 for fp32 caches; for fp16/bf16,
+||o - ref||_inf / max(||ref||_inf, 1e-6) <= 2e-2 per (row, head), fp32
+accumulation in the kernel.  Every workload NaN-poisons cache rows outside
+the contexts and table entries past a row's blocks are -1, so a kernel that
+reads or weights them fails.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from workloads import configs
+from gpu_helpers import (require_gpu, oracle_store_f64, check_attention, gather_rows_for_oracle,
+                         oracle_sampled)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def small_variants():
+    return {
+        "tiny": configs.TINY,
+        "nanochat": configs.NANOCHAT,
+        "qwen3_small": configs.QWEN3.scaled(num_seqs=6, ctx_args=(1, 700), pool_blocks=48, num_layers=3,
+                                            vocab=2048),
+        "grok1_small": configs.GROK1.scaled(num_seqs=3, ctx_args=(300,), vocab=2048),
+        "grok1_ragged": configs.GROK1.scaled(num_seqs=5, ctx_kind="explicit", ctx_args=(1, 15, 16, 17, 250),
+                                             table_kind="perm", vocab=2048),
+        "longctx_small": configs.LONGCTX.scaled(num_seqs=6, ctx_args=(1, 3000), vocab=2048),
+        # many short rows, some empty: whole rows finish inside one CTA and
+        # empty rows must come out as zeros
+        "short_rows": configs.GROK1.scaled(num_seqs=400, num_q_heads=16, num_kv_heads=8, ctx_kind="uniform",
+                                           ctx_args=(0, 40), table_kind="perm", vocab=2048),
+        "mqa_f16": configs.QWEN3.scaled(num_seqs=4, num_q_heads=8, num_kv_heads=1, head_dim=128,
+                                        block_size=32, ctx_args=(1, 300), pool_blocks=0, num_layers=1,
+                                        vocab=2048),
+    }
+
+
+def paths_for(cfg, pk):
+    out = [pk.PATH_FMA]
+    if cfg.dtype != "f32" and cfg.num_kv_heads in (8, 16):
+        out.append(pk.PATH_MMA)
+    return out
+
+
+def run_attention(pk, w, path, cache=None):
+    lay = w.layout
+    if cache is None:
+        cache = w.cache.to(DEV)
+    kc, vc = cache[0, lay.layer], cache[1, lay.layer]
+    tables = torch.from_numpy(lay.block_tables).to(DEV)
+    ctx = torch.from_numpy(lay.context_lens).to(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    slots = pk.slot_mapping(tables, ctx, w.cfg.block_size, lay.num_blocks, err=err)
+    q = w.q.to(DEV)
+    pk.kv_store(w.k_new.to(DEV), w.v_new.to(DEV), slots, kc, vc, err=err)
+    out = pk.paged_decode_attention(q, kc, vc, tables, ctx, lay.max_context_len, w.scale, err=err, path=path)
+    torch.cuda.synchronize()
+    return out, err.item()
+
+
+@pytest.mark.parametrize("name", list(small_variants()))
+def test_attention_matches_oracle(name):
+    pk = require_gpu()
+    cfg = small_variants()[name]
+    w = workloads.make_workload(cfg)
+    kf, vf, _ = oracle_store_f64(w)
+    lay = w.layout
+    ref = oracle.attention.decode_attention(w.q.double().numpy(), kf, vf, lay.block_tables,
+                                            lay.context_lens, w.scale)
+    for path in paths_for(cfg, pk):
+        out, err = run_attention(pk, w, path)
+        assert err == 0
+        check_attention(out.double().cpu().numpy(), ref, w.q.dtype)
+        zero_rows = np.nonzero(lay.context_lens == 0)[0]
+        if len(zero_rows):
+            assert torch.all(out[torch.from_numpy(zero_rows).to(DEV)] == 0)
+
+
+def test_single_token_context_returns_v_exactly():
+    pk = require_gpu()
+    cfg = configs.GROK1.scaled(num_seqs=4, ctx_kind="explicit", ctx_args=(1, 1, 1, 1), table_kind="perm")
+    w = workloads.make_workload(cfg)
+    for path in paths_for(cfg, pk):
+        out, err = run_attention(pk, w, path)
+        assert err == 0
+        G = cfg.group
+        for i in range(4):
+            for h in range(cfg.num_q_heads):
+                assert torch.equal(out[i, h].cpu(), w.v_new[i, h // G])
+
+
+def test_bad_block_id_is_flagged_not_read():
+    pk = require_gpu()
+    cfg = configs.GROK1.scaled(num_seqs=2, ctx_args=(64,), vocab=2048)
+    w = workloads.make_workload(cfg)
+    lay = w.layout
+    lay.block_tables[1, 2] = lay.num_blocks + 5           # outside the pool
+    cache = w.cache.to(DEV)
+    tables = torch.from_numpy(lay.block_tables).to(DEV)
+    ctx = torch.from_numpy(lay.context_lens).to(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pk.paged_decode_attention(w.q.to(DEV), cache[0, 0], cache[1, 0], tables, ctx, lay.max_context_len,
+                              w.scale, err=err)
+    torch.cuda.synchronize()
+    assert err.item() & pk.ERR_BLOCK_ID
+
+
+@pytest.mark.parametrize("name", ["grok1", "qwen3", "longctx"])
+def test_full_size_sampled_rows(name):
+    """The benchmark's shapes and launch configuration, checked on sampled
+    (row, head) pairs against the oracle, plus FMA/MMA agreement on every
+    output element."""
+    pk = require_gpu()
+    cfg = configs.CONFIGS[name]
+    w = workloads.make_workload(cfg, device=DEV)
+    lay = w.layout
+    rng = np.random.default_rng(0)
+    longest = int(np.argmax(lay.context_lens))
+    rows = sorted(set([0, longest, lay.num_seqs - 1] + rng.choice(lay.num_seqs, 3, replace=False).tolist()))
+    heads = sorted(set([0, cfg.num_q_heads - 1] + rng.choice(cfg.num_q_heads, 2, replace=False).tolist()))
+    gathered = gather_rows_for_oracle(w, rows)            # before any kernel touches the cache
+    ref, pairs = oracle_sampled(w, gathered, rows, heads)
+    outs = {}
+    for path in paths_for(cfg, pk):
+        out, err = run_attention(pk, w, path, cache=w.cache)
+        assert err == 0
+        o = out[torch.tensor(rows, device=DEV)].double().cpu().numpy()
+        check_attention(o, ref, w.q.dtype, pairs=pairs)
+        assert torch.isfinite(out).all()
+        outs[path] = out.float()
+    if len(outs) == 2:
+        a, b = outs[pk.PATH_FMA], outs[pk.PATH_MMA]
+        rel = (a - b).abs().amax(dim=-1) / a.abs().amax(dim=-1).clamp_min(1e-6)
+        assert float(rel.max()) <= 2 * 2e-2

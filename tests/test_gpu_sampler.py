@@ -1,0 +1,171 @@
+"""Fused sampler on the GPU against the oracle.
+
+Greedy ids are bit-exact.  Stochastic ids must equal the oracle's for the
+same Philox stream except where the oracle's two best perturbed scores are
+closer than 1e-5 * max(1, |s1|), or the nucleus cut mass lies within 1e-6 of
+p (float rounding can move either decision); such rows are counted, and must
+be rare.  A chi-square test over 1e5 draws checks the distribution.
+"""
+import numpy as np
+import pytest
+import torch
+from scipy import stats
+
+import oracle
+import workloads
+from workloads import configs
+from gpu_helpers import require_gpu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _dev_params(si, B=None):
+    B = si.logits.shape[0] if B is None else B
+    return (torch.from_numpy(si.temperature).to(DEV), torch.from_numpy(si.top_k).to(DEV),
+            torch.from_numpy(si.top_p).to(DEV), torch.from_numpy(si.seeds.view(np.int64)).to(DEV),
+            torch.from_numpy(si.offsets.view(np.int64)).to(DEV))
+
+
+def _exempt(info, p):
+    if info["top2_gap"] < 1e-5 * max(1.0, abs(info["top1_score"])):
+        return True
+    n = info["nucleus"]
+    if n is not None and (abs(n["mass_before"] - p) < 1e-6 or abs(n["mass_after"] - p) < 1e-6):
+        return True
+    return False
+
+
+@pytest.mark.parametrize("name", list(configs.CONFIGS))
+def test_greedy_bit_exact(name):
+    pk = require_gpu()
+    si = workloads.make_sampler_inputs(configs.CONFIGS[name])
+    B = si.logits.shape[0]
+    T, k, p, s, o = _dev_params(si)
+    tok = pk.sample(si.logits.to(DEV), torch.zeros_like(T), k, p, s, o).cpu().numpy()
+    x = si.logits.double().numpy()
+    ref = [oracle.sampler.greedy(x[i]) for i in range(B)]
+    assert tok.tolist() == ref
+
+
+@pytest.mark.parametrize("name", list(configs.CONFIGS))
+def test_stochastic_matches_oracle(name):
+    pk = require_gpu()
+    si = workloads.make_sampler_inputs(configs.CONFIGS[name])
+    T, k, p, s, o = _dev_params(si)
+    tok = pk.sample(si.logits.to(DEV), T, k, p, s, o).cpu().numpy()
+    x = si.logits.double().numpy()
+    mism, exempt = 0, 0
+    for i in range(x.shape[0]):
+        ref, info = oracle.sampler.sample_row(x[i], float(si.temperature[i]), int(si.top_k[i]),
+                                              float(si.top_p[i]), int(si.seeds[i]), int(si.offsets[i]),
+                                              return_info=True)
+        if int(tok[i]) != ref:
+            if _exempt(info, float(si.top_p[i])):
+                exempt += 1
+            else:
+                mism += 1
+    assert mism == 0
+    assert exempt <= max(1, x.shape[0] // 20)
+
+
+def test_many_seeds_and_offsets_match_oracle():
+    """Same row under 512 (seed, offset) pairs: exercises the Philox stream."""
+    pk = require_gpu()
+    rng = np.random.default_rng(11)
+    V, R = 3001, 512
+    row = torch.from_numpy((rng.standard_normal(V) * 1.5).astype(np.float32)).to(torch.bfloat16)
+    logits = row.unsqueeze(0).repeat(R, 1)
+    seeds = rng.integers(0, 2**63, size=R, dtype=np.int64)
+    offs = rng.integers(0, 2**40, size=R, dtype=np.int64)
+    T32, p32 = float(np.float32(0.9)), float(np.float32(0.97))
+    T = torch.full((R,), T32, device=DEV)
+    tok = pk.sample(logits.to(DEV), T, torch.full((R,), 100, dtype=torch.int32, device=DEV),
+                    torch.full((R,), 0.97, device=DEV), torch.from_numpy(seeds).to(DEV),
+                    torch.from_numpy(offs).to(DEV)).cpu().numpy()
+    x = row.double().numpy()
+    bad = 0
+    for i in range(R):
+        ref, info = oracle.sampler.sample_row(x, T32, 100, p32, int(seeds[i]), int(offs[i]),
+                                              return_info=True)
+        if int(tok[i]) != ref and not _exempt(info, p32):
+            bad += 1
+    assert bad == 0
+
+
+@pytest.mark.parametrize("dtype,T,k,p", [(torch.float32, 1.0, 0, 1.0), (torch.bfloat16, 0.7, 0, 0.8),
+                                         (torch.float16, 1.3, 5, 1.0), (torch.bfloat16, 1.0, 6, 0.9)])
+def test_chi_square_1e5_draws(dtype, T, k, p):
+    pk = require_gpu()
+    rng = np.random.default_rng(5)
+    V, R = 40, 100_000
+    row = torch.from_numpy((rng.standard_normal(V) * 1.5).astype(np.float32)).to(dtype)
+    logits = row.unsqueeze(0).repeat(R, 1).to(DEV)
+    tok = pk.sample(logits, torch.full((R,), T, device=DEV), torch.full((R,), k, dtype=torch.int32, device=DEV),
+                    torch.full((R,), p, device=DEV), torch.full((R,), 1234, dtype=torch.int64, device=DEV),
+                    torch.arange(R, dtype=torch.int64, device=DEV)).cpu().numpy()
+    probs = oracle.sampler.truncated_probs(row.double().numpy(), float(np.float32(T)), k, float(np.float32(p)))
+    assert np.all(probs[tok] > 0)
+    support = np.nonzero(probs > 0)[0]
+    counts = np.bincount(tok, minlength=V)[support]
+    expected = probs[support] * R
+    keep = expected >= 5
+    obs = np.append(counts[keep], counts[~keep].sum())
+    exp = np.append(expected[keep], expected[~keep].sum())
+    if exp[-1] == 0:
+        obs, exp = obs[:-1], exp[:-1]
+    assert stats.chisquare(obs, exp).pvalue > 1e-3
+
+
+def test_top_k_tie_group_straddling_the_cut():
+    """Ten equal logits at the k-th value: exactly the lowest-index ones stay."""
+    pk = require_gpu()
+    V, R = 300, 4000
+    x = torch.full((V,), -3.0)
+    x[[250, 5, 77]] = 2.0                       # three clear leaders
+    ties = [290, 12, 150, 33, 199, 8, 64, 111, 275, 40]
+    x[ties] = 1.0
+    logits = x.to(torch.bfloat16).unsqueeze(0).repeat(R, 1).to(DEV)
+    tok = pk.sample(logits, torch.full((R,), 3.0, device=DEV), torch.full((R,), 7, dtype=torch.int32, device=DEV),
+                    torch.ones(R, device=DEV), torch.full((R,), 99, dtype=torch.int64, device=DEV),
+                    torch.arange(R, dtype=torch.int64, device=DEV)).cpu().numpy()
+    allowed = {250, 5, 77} | set(sorted(ties)[:4])
+    assert set(tok.tolist()) == allowed
+    ref = oracle.sampler.topk_set(x.double().numpy(), 7)
+    assert set(ref.tolist()) == allowed
+
+
+def test_degenerate_rows():
+    pk = require_gpu()
+    # vocab 1; all-equal logits (greedy -> 0, sampling uniform over ids); p = 0 keeps the top group
+    one = torch.zeros(3, 1, dtype=torch.float32, device=DEV)
+    T = torch.tensor([0.0, 1.0, 5.0], device=DEV)
+    z = torch.zeros(3, dtype=torch.int64, device=DEV)
+    tok = pk.sample(one, T, torch.zeros(3, dtype=torch.int32, device=DEV), torch.ones(3, device=DEV), z, z)
+    assert tok.cpu().tolist() == [0, 0, 0]
+    flat = torch.zeros(2, 50, dtype=torch.float16, device=DEV)
+    tok = pk.sample(flat, torch.tensor([0.0, 1.0], device=DEV), torch.zeros(2, dtype=torch.int32, device=DEV),
+                    torch.ones(2, device=DEV), z[:2], z[:2])
+    assert tok.cpu().tolist()[0] == 0
+    x = torch.randn(64, 500, device=DEV)
+    x[:, 17] = 100.0
+    tok = pk.sample(x, torch.ones(64, device=DEV), torch.zeros(64, dtype=torch.int32, device=DEV),
+                    torch.zeros(64, device=DEV), torch.arange(64, device=DEV), torch.zeros(64, dtype=torch.int64, device=DEV))
+    assert (tok == 17).all()
+    # negative zero and positive zero are the same value
+    y = torch.tensor([[-0.0, 0.0, -1.0]], dtype=torch.bfloat16, device=DEV)
+    tok = pk.sample(y, torch.zeros(1, device=DEV), torch.zeros(1, dtype=torch.int32, device=DEV),
+                    torch.ones(1, device=DEV), z[:1], z[:1])
+    assert tok.item() == 0
+
+
+def test_unaligned_rows_use_the_scalar_path():
+    pk = require_gpu()
+    rng = np.random.default_rng(3)
+    base = torch.from_numpy(rng.standard_normal((8, 1001)).astype(np.float32)).to(torch.bfloat16)
+    logits = base.to(DEV)[:, 1:]                 # rows start 2 bytes past a 16-byte boundary
+    z = torch.zeros(8, dtype=torch.int64, device=DEV)
+    tok = pk.sample(logits, torch.zeros(8, device=DEV), torch.zeros(8, dtype=torch.int32, device=DEV),
+                    torch.ones(8, device=DEV), z, z).cpu().tolist()
+    ref = [oracle.sampler.greedy(base[i, 1:].double().numpy()) for i in range(8)]
+    assert tok == ref

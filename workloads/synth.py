@@ -240,3 +240,36 @@ def make_workload(cfg: DecodeConfig, device: str = "cpu", seed: int | None = Non
 
     return Workload(cfg, layout, q, k_new, v_new, cache, logits,
                     temp, top_k, top_p, seeds, offsets)
+
+
+@dataclass
+class SamplerInputs:
+    cfg: DecodeConfig
+    logits: torch.Tensor       # [B, V] in the config's logits dtype
+    temperature: np.ndarray    # f32 [B]
+    top_k: np.ndarray          # i32 [B]
+    top_p: np.ndarray          # f32 [B]
+    seeds: np.ndarray          # u64 [B]
+    offsets: np.ndarray        # u64 [B]
+
+
+def make_sampler_inputs(cfg: DecodeConfig, device: str = "cpu", seed: int | None = None,
+                        num_rows: int | None = None) -> SamplerInputs:
+    """Only the sampler's inputs (logits + per-row parameters) of a config.
+
+    The per-row parameters come from the same stream as make_workload's; the
+    logits from their own stream, so this does not draw the KV cache."""
+    seed = cfg.seed if seed is None else seed
+    B = cfg.num_seqs if num_rows is None else num_rows
+    prng = np.random.Generator(np.random.PCG64([seed, 1]))
+    temp, top_k, top_p, seeds, offsets = _sampling_params(cfg, prng, B)
+    ldt = TORCH_DTYPES[cfg.logits_dtype]
+    if device == "cpu":
+        rng = np.random.Generator(np.random.PCG64([seed, 3]))
+        logits = torch.from_numpy(cfg.logits_std * rng.standard_normal((B, cfg.vocab), dtype=np.float32)).to(ldt)
+    else:
+        gen = torch.Generator(device=device)
+        gen.manual_seed(seed + 7919)
+        logits = torch.empty((B, cfg.vocab), dtype=ldt, device=device)
+        _fill_normal(logits, gen, cfg.logits_std)
+    return SamplerInputs(cfg, logits, temp, top_k, top_p, seeds, offsets)

@@ -158,8 +158,11 @@ pkvd_status pkvd_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  * Output: out [num_seqs, num_q_heads, head_dim], cache dtype, fp32 softmax
  *         and accumulation.
  * workspace: device scratch of at least pkvd_decode_workspace_bytes(...)
- *         bytes (16-byte aligned), used for split-context partial results;
- *         its contents need no initialisation.
+ *         bytes (16-byte aligned): per-(row, head) arrival counters followed
+ *         by split-context partial results.  Zero-fill it once before its
+ *         first use; every completed call leaves the counters at zero again,
+ *         so it can be reused (and captured in a graph) without clearing.
+ *         Calls that share a workspace must not overlap on the GPU.
  * Requirements: num_q_heads % num_kv_heads == 0, group size <= 8,
  *         num_kv_heads <= 8 or == 16.
  */

@@ -74,7 +74,7 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         out = torch.empty_like(q)
     if workspace is None:
         nbytes = decode_workspace_bytes(B, Hq, D, max_context_len)
-        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=q.device)
     check(lib().pkvd_paged_decode_attention_ex(
         ptr(out), ptr(q), ctypes.byref(c), ptr(block_tables), block_tables.shape[1],
         ptr(context_lens), max_context_len, B, Hq, ctypes.c_float(scale), ptr(workspace),

@@ -1,4 +1,4 @@
-// Paged single-query GQA decode attention: partition kernel + LSE merge.
+// Paged single-query GQA decode attention: partition kernel with a fused LSE merge.
 //
 // What is computed (nano-vllm "Model Runner" notes, sections "prefill and
 // decode" and "allocated kv cache"; Grok-1 "第 8 章 runners.py 推理引擎",
@@ -12,9 +12,11 @@
 //   slice of that list (stream-K style), so every SM moves the same number
 //   of K/V bytes whatever the length mix.  A slice may start or end inside
 //   a sequence; such partial segments leave an unnormalised (m, l, acc)
-//   record in the workspace and the merge kernel combines them with the
-//   log-sum-exp identity.  Segments wholly inside one CTA are normalised and
-//   written directly.
+//   record in the workspace and count themselves in on a per-(row, kv head)
+//   counter; the warp that arrives last combines the row's records with the
+//   log-sum-exp identity (no waiting: nobody spins on anybody) and resets
+//   the counter.  Segments wholly inside one CTA are normalised and written
+//   directly.
 // * One producer warp walks the slice, looks block ids up (32 table entries
 //   per coalesced load, shuffled to the lane that needs them) and issues
 //   cp.async.bulk (TMA engine) copies of each chunk's K and V token rows --
@@ -58,8 +60,8 @@ struct PartParams {
   int ctx_cap;
   int num_seqs;
   float scale_log2;
-  float* rec;          // partial records [grid][2][hq][D + 2]
-  int32_t* prefix;     // [num_seqs + 1] chunk prefix sums (written by CTA 0)
+  float* rec;          // partial records [grid][2][hq][D + 4]: acc[D], m, l, pad
+  int32_t* counters;   // [num_seqs][hq] arrivals per (row, kv head); zero between launches
   int32_t* err;
   int stages;
   int rowb;            // padded smem bytes of one token row (all heads)
@@ -111,6 +113,84 @@ struct SmemHdr {
   long long total;
   int abort_flag;
 };
+
+// A warp has written its partial record for (row, kv head hk).  It counts
+// itself in; the warp that arrives last (no waiting anywhere) folds every
+// record of the row with the log-sum-exp identity, writes the G output rows
+// of the group and resets the counter for the next launch.
+//   M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  o = sum_s 2^(m_s - M) acc_s / L
+template <typename T, int D>
+__device__ __forceinline__ void row_partial_done(const PartParams& p, int seq, int hk, long long P, long long n,
+                                                 long long C, int grid, int lane) {
+  __threadfence();
+  __syncwarp();
+  const int a = (int)(((P + 1) * grid - 1) / C);
+  const int b = (int)(((P + n) * grid - 1) / C);
+  // CTA a's slice starts at or before P; every later CTA up to b starts inside
+  // the row.  With C >= grid every slice is non-empty, so all of a..b
+  // contribute; otherwise empty slices are skipped.
+  const bool a_at_start = (C * a) / grid == P;
+  int contributors = b - a + 1;
+  if (C < grid) {
+    contributors = 0;
+    for (int c0 = a; c0 <= b; c0 += 32) {
+      const int c = c0 + lane;
+      bool nonempty = false;
+      if (c <= b) nonempty = (C * c) / grid < (C * (c + 1)) / grid;
+      contributors += __popc(__ballot_sync(FULL_MASK, nonempty));
+    }
+  }
+  int old = 0;
+  int32_t* ctr = p.counters + (int64_t)seq * p.hq + hk;
+  if (lane == 0) old = atomicAdd(ctr, 1);
+  old = __shfl_sync(FULL_MASK, old, 0);
+  if (old != contributors - 1) return;
+  __threadfence();
+  constexpr int Q = D / 4;
+  const int total = p.G * Q;                         // float4 outputs of the group
+  for (int base = 0; base < total; base += 32) {     // warp-uniform loops: shuffles below
+    const int idx = base + lane;
+    const bool act = idx < total;
+    const int g = act ? idx / Q : 0, d4 = act ? (idx % Q) * 4 : 0;
+    const int h = hk * p.G + g;
+    float M = -INFINITY, L = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int w0 = a; w0 <= b; w0 += 32) {
+      const int c = w0 + lane;                       // one contributing CTA per lane
+      int rid = -1;
+      if (c <= b) {
+        const bool nonempty = C >= grid || (C * c) / grid < (C * (c + 1)) / grid;
+        if (nonempty) rid = c * 2 + ((c == a && !a_at_start) ? 1 : 0);
+      }
+      const int nwin = min(32, b - w0 + 1);
+      for (int k = 0; k < nwin; ++k) {
+        const int r_id = __shfl_sync(FULL_MASK, rid, k);
+        if (r_id < 0 || !act) continue;
+        const float* r = p.rec + ((int64_t)r_id * p.hq + h) * (D + 4);
+        const float m = __ldcg(r + D), l = __ldcg(r + D + 1);
+        const float4 acc = __ldcg(reinterpret_cast<const float4*>(r + d4));
+        const float Mn = fmaxf(M, m);
+        const float cs = (M == -INFINITY) ? 0.f : exp2f(M - Mn);
+        const float cr = (m == -INFINITY) ? 0.f : exp2f(m - Mn);
+        L = L * cs + l * cr;
+        o.x = o.x * cs + acc.x * cr;
+        o.y = o.y * cs + acc.y * cr;
+        o.z = o.z * cs + acc.z * cr;
+        o.w = o.w * cs + acc.w * cr;
+        M = Mn;
+      }
+    }
+    if (act) {
+      const float inv = 1.f / L;
+      T* dst = static_cast<T*>(p.out) + ((int64_t)seq * p.hq + h) * D + d4;
+      dst[0] = DT<T>::from_f(o.x * inv);
+      dst[1] = DT<T>::from_f(o.y * inv);
+      dst[2] = DT<T>::from_f(o.z * inv);
+      dst[3] = DT<T>::from_f(o.w * inv);
+    }
+  }
+  if (lane == 0) *ctr = 0;
+}
 
 // ----------------------------------------------------------- consumers
 template <typename T, int D, int HPW, int GMAX>
@@ -196,7 +276,8 @@ struct FmaConsumer {
     }
   }
 
-  __device__ void finish(const PartParams& p, int seq, int flags, int cta, int warp, int lane) {
+  __device__ void finish(const PartParams& p, int seq, int flags, int cta, int warp, int lane, long long P,
+                         long long nrow, long long C, int grid) {
     const int li = lane % LPT;
 #pragma unroll
     for (int j = 0; j < HPW; ++j) {
@@ -230,7 +311,7 @@ struct FmaConsumer {
             *reinterpret_cast<uint4*>(o) = *reinterpret_cast<const uint4*>(tmp);
           } else {
             const int slot = (flags & F_SLOT1) ? 1 : 0;
-            float* r = p.rec + ((int64_t)(cta * 2 + slot) * p.hq + h) * (D + 2);
+            float* r = p.rec + ((int64_t)(cta * 2 + slot) * p.hq + h) * (D + 4);
 #pragma unroll
             for (int v = 0; v < VEC; ++v) r[li * VEC + v] = acc[j][g][v];
             if (li == 0) {
@@ -240,6 +321,7 @@ struct FmaConsumer {
           }
         }
       }
+      if (!(flags & F_COMPLETE)) row_partial_done<T, D>(p, seq, hk, P, nrow, C, grid, lane);
     }
   }
 };
@@ -344,7 +426,8 @@ struct MmaConsumer {
     }
   }
 
-  __device__ void finish(const PartParams& p, int seq, int flags, int cta, int warp, int lane) {
+  __device__ void finish(const PartParams& p, int seq, int flags, int cta, int warp, int lane, long long P,
+                         long long nrow, long long C, int grid) {
     const int lr = lane >> 2, lc = lane & 3;
 #pragma unroll
     for (int j = 0; j < HPW; ++j) {
@@ -373,23 +456,24 @@ struct MmaConsumer {
         }
       } else {
         const int slot = (flags & F_SLOT1) ? 1 : 0;
-        float* rb = p.rec + ((int64_t)(cta * 2 + slot) * p.hq + hk * p.G) * (D + 2);
+        float* rb = p.rec + ((int64_t)(cta * 2 + slot) * p.hq + hk * p.G) * (D + 4);
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
           const int d0 = mt * 16 + lr;
           if (gA < p.G) {
-            rb[gA * (D + 2) + d0] = acc[j][mt][0];
-            rb[gA * (D + 2) + d0 + 8] = acc[j][mt][2];
+            rb[gA * (D + 4) + d0] = acc[j][mt][0];
+            rb[gA * (D + 4) + d0 + 8] = acc[j][mt][2];
           }
           if (gB < p.G) {
-            rb[gB * (D + 2) + d0] = acc[j][mt][1];
-            rb[gB * (D + 2) + d0 + 8] = acc[j][mt][3];
+            rb[gB * (D + 4) + d0] = acc[j][mt][1];
+            rb[gB * (D + 4) + d0 + 8] = acc[j][mt][3];
           }
         }
         if (lr == 0) {
-          if (gA < p.G) { rb[gA * (D + 2) + D] = m[j][0]; rb[gA * (D + 2) + D + 1] = lA; }
-          if (gB < p.G) { rb[gB * (D + 2) + D] = m[j][1]; rb[gB * (D + 2) + D + 1] = lB; }
+          if (gA < p.G) { rb[gA * (D + 4) + D] = m[j][0]; rb[gA * (D + 4) + D + 1] = lA; }
+          if (gB < p.G) { rb[gB * (D + 4) + D] = m[j][1]; rb[gB * (D + 4) + D + 1] = lB; }
         }
+        row_partial_done<T, D>(p, seq, hk, P, nrow, C, grid, lane);
       }
     }
   }
@@ -433,9 +517,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
       const int incl = block_incl_scan(n, hdr.scan_warp, total);
       const int excl = running + incl - n;
       if (cta == 0 && i < p.num_seqs) {
-        p.prefix[i] = excl;
         const int raw = p.ctx[i];
         if (raw < 0 || raw > p.ctx_cap) flag_error(p.err, PKVD_ERR_CONTEXT);
+        if (n == 0) {
+          // an empty context attends to nothing: its output rows are zero
+          uint4* o = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + (int64_t)i * p.hq * D);
+          for (int v = 0; v < p.hq * D * (int)sizeof(T) / 16; ++v) o[v] = make_uint4(0, 0, 0, 0);
+        }
       }
       if (i < p.num_seqs && n > 0 && excl <= c0 && c0 < excl + n) {
         hdr.found_seq = i;
@@ -445,7 +533,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
       __syncthreads();
       if (cta != 0 && hdr.found_seq >= 0) break;
     }
-    if (cta == 0 && tid == 0) p.prefix[p.num_seqs] = (int)C;
   }
   if (c0 >= c1) return;
 
@@ -467,11 +554,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
     int ctx_seq = min(max(p.ctx[seq], 0), p.ctx_cap);
     int nch = (ctx_seq + kChunk - 1) / kChunk;
     int seg_start = ch;
+    long long row_start = c0 - ch;          // flat index of the row's chunk 0
     bool first_seg = true;
     int tb_seq = -1, tb_base = 0, tb_val = -1;
     int it = 0;
     for (; it < nit; ++it) {
       while (ch >= nch && seq + 1 < p.num_seqs) {
+        row_start += nch;
         ++seq;
         ctx_seq = min(max(p.ctx[seq], 0), p.ctx_cap);
         nch = (ctx_seq + kChunk - 1) / kChunk;
@@ -506,7 +595,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
       if (!first_seg) flags |= F_SLOT1;
       if (lane == 0) {
         if (!ok) flag_error(p.err, PKVD_ERR_BLOCK_ID);
-        hdr.meta[stage] = make_int4(seq, ncopy, flags, 0);
+        hdr.meta[stage] = make_int4(seq, ncopy, flags | (nch << 4), (int)row_start);
         mbar_arrive_expect_tx(&hdr.full[stage], (uint32_t)(ncopy * 2 * p.row_bytes));
       }
       __syncwarp();
@@ -557,61 +646,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
       break;
     }
     const int4 meta = hdr.meta[stage];
-    const int seq = meta.x, ntok = meta.y, flags = meta.z;
+    const int seq = meta.x, ntok = meta.y, flags = meta.z & 15;
+    const int nrow = meta.z >> 4;
+    const long long row_start = meta.w;
     if (flags & F_FIRST) cons.begin(p, seq, warp, lane);
     uint8_t* sK = stage_base + stage * stage_bytes;
     uint8_t* sV = sK + kChunk * p.rowb;
     if (ntok > 0) cons.chunk(p, sK, sV, ntok, warp, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&hdr.empty[stage]);
-    if (flags & F_LAST) cons.finish(p, seq, flags, cta, warp, lane);
-  }
-}
-
-// ------------------------------------------------------------ merge
-// One CTA per row: combines the partial records of the CTAs whose slices
-// cut the row, writes zeros for an empty context, and leaves rows that one
-// CTA finished on its own untouched.
-template <typename T>
-__global__ void __launch_bounds__(256) lse_merge_kernel(T* __restrict__ out, const float* __restrict__ rec,
-                                                        const int32_t* __restrict__ prefix, int num_seqs,
-                                                        int hq, int D, int grid) {
-  const int i = blockIdx.x;
-  T* orow = out + (int64_t)i * hq * D;
-  if (grid == 0) {
-    for (int idx = threadIdx.x; idx < hq * D; idx += blockDim.x) orow[idx] = DT<T>::from_f(0.f);
-    return;
-  }
-  const long long C = prefix[num_seqs];
-  const long long P = prefix[i];
-  const long long n = (i + 1 < num_seqs ? prefix[i + 1] : C) - P;
-  if (n <= 0) {
-    for (int idx = threadIdx.x; idx < hq * D; idx += blockDim.x) orow[idx] = DT<T>::from_f(0.f);
-    return;
-  }
-  const int a = (int)(((P + 1) * grid - 1) / C);
-  const int b = (int)(((P + n) * grid - 1) / C);
-  if (a == b) return;
-  for (int idx = threadIdx.x; idx < hq * D; idx += blockDim.x) {
-    const int h = idx / D, d = idx % D;
-    float M = -INFINITY;
-    for (int c = a; c <= b; ++c) {
-      const long long s0 = (C * c) / grid, s1 = (C * (c + 1)) / grid;
-      if (s0 >= s1) continue;
-      const int slot = s0 >= P ? 0 : 1;
-      M = fmaxf(M, rec[((int64_t)(c * 2 + slot) * hq + h) * (D + 2) + D]);
-    }
-    float L = 0.f, o = 0.f;
-    for (int c = a; c <= b; ++c) {
-      const long long s0 = (C * c) / grid, s1 = (C * (c + 1)) / grid;
-      if (s0 >= s1) continue;
-      const int slot = s0 >= P ? 0 : 1;
-      const float* r = rec + ((int64_t)(c * 2 + slot) * hq + h) * (D + 2);
-      const float w = exp2f(r[D] - M);
-      L = fmaf(w, r[D + 1], L);
-      o = fmaf(w, r[d], o);
-    }
-    orow[idx] = DT<T>::from_f(o / L);
+    if (flags & F_LAST) cons.finish(p, seq, flags, cta, warp, lane, row_start, nrow, C, grid);
   }
 }
 

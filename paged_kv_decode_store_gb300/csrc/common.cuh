@@ -8,7 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/pkvd.h"
+#include "pkvd.h"
 
 namespace pkvd {
 

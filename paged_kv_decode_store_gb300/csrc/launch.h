@@ -7,7 +7,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/pkvd.h"
+#include "pkvd.h"
 
 namespace pkvd {
 

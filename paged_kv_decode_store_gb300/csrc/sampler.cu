@@ -10,22 +10,31 @@
 //            equal to its last value; token = argmax_kept x'_j + g_j with
 //            Gumbel noise from Philox4x32-10 (Salmon et al., SC'11).
 //
-// No sort.  One CTA (1024 threads) per row, a few streaming passes over the
-// row (L2-resident after the first):
-//   1. max key and its lowest index (greedy result, softmax shift m).
-//   2. top-k: MSB-first radix select, 8 bits per pass, on order-preserving
-//      integer keys of the raw logits (16-bit keys for fp16/bf16, 32-bit for
-//      fp32) -- exact, so the top-k set matches bit for bit.
-//   3. nucleus: the same radix select, but each bin accumulates probability
-//      mass exp((x - m)/T) in 2^-40 fixed point (64-bit integer atomics, so
-//      the sums are exact and independent of thread order).  It finds the
-//      key tau where the descending cumulative mass first exceeds p * Z.
-//   4. Gumbel pass over the kept ids.  Only ids with x'_j >= max x' - 21 can
-//      win (u is in [2^-24, 1 - 2^-24], so g lies in [-2.81, 16.64]); the
-//      others are skipped exactly, which leaves a handful of Philox
-//      evaluations for peaked rows.
-// Ties at the k-th key are resolved by index (a radix select over the tie
-// group's indices), only when the tie group straddles the cut.
+// GB300 design -- no sort, one read of the row from HBM:
+// * A row is split over a cluster of CS CTAs (CS = 1..8, chosen so the grid
+//   covers the SMs).  Each CTA copies its slice into shared memory with
+//   cp.async.bulk (TMA engine) and every later pass reads shared memory.
+//   Row-wide values (max, histograms, the winning score) are exchanged
+//   through distributed shared memory (mapa / ld.shared::cluster) between
+//   cluster barriers, summed in rank order so results are deterministic.
+// * Order-preserving integer keys of the raw logits (16-bit keys for
+//   fp16/bf16) make top-k exact.  For 16-bit logits a key is one value, so
+//   exact per-key counts in a window of keys below the max give each key's
+//   probability mass as count * w(key), w in 2^-40 fixed point; ids below
+//   the window only enter the normaliser, through an f32 sum in fixed order.
+//   Top-k and the nucleus cut are found by a two-level scan of that window
+//   (256 groups, then the bins of one group).  fp32 logits, and cuts that
+//   fall below the window, use an MSB-first radix select with cluster-summed
+//   histograms instead.
+// * Gumbel pass: only ids that can win are considered (x'_j >= max x' - 21,
+//   since u lies in [2^-24, 1 - 2^-24] and g in [-2.81, 16.64]); candidates
+//   are compacted into per-warp queues so Philox and the logarithms run on
+//   full warps.
+// * Ties at the k-th key straddling the cut: slices are ordered by index, so
+//   each CTA takes its share of the lowest-index ties and resolves it with a
+//   local radix select over its tie indices.
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -35,11 +44,18 @@ constexpr int kSampThreads = 1024;
 constexpr int kSampWarps = kSampThreads / 32;
 constexpr int kHistCopies = 16;
 constexpr float kGumbelSpan = 21.0f;
+constexpr int kMaxCluster = 8;
+constexpr int kMaxChunks = 16;
+constexpr int kChunkBytes = 16384;
+constexpr int kQueue = 64;                 // per-warp candidate ring
+
+// Exact per-key counts are kept for the kWinTop keys below the row max
+// (16-bit logits: 8 binades for fp16, 64 for bf16).
+constexpr int kWinTop = 8192;                   // exact counts of the top keys below the max
 
 template <typename T> struct Keys;
 template <> struct Keys<float> {
   static constexpr int BITS = 32;
-  __device__ static uint32_t bits(float x) { return __float_as_uint(x); }
   __device__ static uint32_t key(uint32_t u) {
     if ((u & 0x7fffffffu) == 0) u = 0;
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -72,69 +88,39 @@ template <> struct Keys<__nv_bfloat16> {
   }
 };
 
-// Order-preserving key of an fp32 score (for the argmax packing).
 __device__ __forceinline__ uint32_t f32_order_key(float x) { return Keys<float>::key(__float_as_uint(x)); }
 
-// Visit every element of a row: f(index, raw bits).  Vector loads of 16 bytes
-// when the row is aligned; four loads in flight per thread.
-template <typename T, typename F>
-__device__ __forceinline__ void for_each_elem(const T* row, int V, bool vec_ok, F&& f) {
-  constexpr int E = 16 / sizeof(T);
-  if (vec_ok) {
-    const int nv = V / E;
-    const uint4* rv = reinterpret_cast<const uint4*>(row);
-    int v = threadIdx.x;
-    for (; v + 3 * kSampThreads < nv; v += 4 * kSampThreads) {
-      uint4 u[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) u[r] = __ldg(rv + v + r * kSampThreads);
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const uint32_t w[4] = {u[r].x, u[r].y, u[r].z, u[r].w};
-        const int j0 = (v + r * kSampThreads) * E;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const uint32_t b = (sizeof(T) == 4) ? w[e] : ((w[e / 2] >> (16 * (e & 1))) & 0xffffu);
-          f(j0 + e, b);
-        }
-      }
-    }
-    for (; v < nv; v += kSampThreads) {
-      const uint4 u = __ldg(rv + v);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const uint32_t b = (sizeof(T) == 4) ? w[e] : ((w[e / 2] >> (16 * (e & 1))) & 0xffffu);
-        f(v * E + e, b);
-      }
-    }
-    for (int j = nv * E + threadIdx.x; j < V; j += kSampThreads) {
-      f(j, sizeof(T) == 4 ? __float_as_uint(*reinterpret_cast<const float*>(row + j))
-                          : (uint32_t)(*reinterpret_cast<const unsigned short*>(row + j)));
-    }
-  } else {
-    for (int j = threadIdx.x; j < V; j += kSampThreads) {
-      f(j, sizeof(T) == 4 ? __float_as_uint(*reinterpret_cast<const float*>(row + j))
-                          : (uint32_t)(*reinterpret_cast<const unsigned short*>(row + j)));
-    }
-  }
+// ------------------------------------------------------------- cluster PTX
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
 }
-
-__device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v, unsigned long long* s) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long t = __shfl_xor_sync(FULL_MASK, v, o);
-    v = t > v ? t : v;
-  }
-  __syncthreads();
-  if (lane == 0) s[warp] = v;
-  __syncthreads();
-  v = s[0];
-  for (int w = 1; w < kSampWarps; ++w) v = s[w] > v ? s[w] : v;
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  return a;
+}
+__device__ __forceinline__ unsigned int dsmem_ld_u32(uint32_t a) {
+  unsigned int v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long dsmem_ld_u64(uint32_t a) {
+  unsigned long long v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
   return v;
 }
 
+// ---------------------------------------------------------------- Philox
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
   const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
   const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
@@ -160,246 +146,1088 @@ __device__ __forceinline__ float gumbel_noise(uint64_t seed, uint64_t offset, ui
   return -logf(-logf(u));
 }
 
-struct SampSmem {
-  unsigned long long hist[kHistCopies][256];   // counts (low 32 bits used) or fixed-point mass
-  unsigned long long tot[256];
+// ------------------------------------------------------------ shared state
+struct SampHdr {
+  uint64_t bar[kMaxChunks];
+  unsigned long long ex_arr[2][256];     // cluster-exchanged arrays (alternating)
+  unsigned long long xr[kMaxCluster];    // per-rank values of the last scalar exchange
+  unsigned long long ex_sc[2][4];        // cluster-exchanged scalars (alternating)
+  unsigned long long tot[256];           // row-wide totals of the last exchange
   unsigned long long red[kSampWarps];
+  float redf[kSampWarps];
   int sel_bin;
   unsigned long long sel_before;
-  int found;
+  int sel_aux;
+  unsigned long long sel_val;
+  unsigned long long zsum;
+  int cand_n;
 };
 
-// Clear the private histograms.
-__device__ __forceinline__ void hist_clear(SampSmem& sm) {
-  unsigned long long* h = &sm.hist[0][0];
-  for (int i = threadIdx.x; i < kHistCopies * 256; i += kSampThreads) h[i] = 0ull;
+struct Ctx {
+  SampHdr* h;
+  int cs;        // cluster size
+  int ex;        // next exchange slot
+};
+
+// Max or sum of a per-CTA u64 over the cluster, in rank order.  Exchange
+// slots alternate, so one cluster barrier per exchange is enough: a slot is
+// rewritten only after every peer passed the next barrier.
+template <bool MAX>
+__device__ __forceinline__ unsigned long long cluster_scalar(Ctx& c, unsigned long long v, int which) {
+  const int s = c.ex;
+  c.ex ^= 1;
+  if (threadIdx.x == 0) c.h->ex_sc[s][which] = v;
+  cluster_sync();
+  // one thread per rank fetches that rank's value (the remote loads overlap)
+  if (threadIdx.x < (unsigned)c.cs) c.h->xr[threadIdx.x] = dsmem_ld_u64(dsmem_addr(&c.h->ex_sc[s][which], threadIdx.x));
+  __syncthreads();
+  unsigned long long acc = 0;
+  for (int r = 0; r < c.cs; ++r) {
+    const unsigned long long x = c.h->xr[r];
+    acc = MAX ? (x > acc ? x : acc) : acc + x;
+  }
+  return acc;
 }
 
-// Sum the private copies into tot[].
-__device__ __forceinline__ void hist_total(SampSmem& sm) {
+// Sum the 256-entry arrays every CTA wrote to ex_arr[c.ex] into tot[].
+// Threads 0..255 own one entry each; ends with __syncthreads.
+__device__ __forceinline__ void cluster_sum_array(Ctx& c) {
+  const int s = c.ex;
+  c.ex ^= 1;
+  cluster_sync();
   if (threadIdx.x < 256) {
-    unsigned long long s = 0;
-#pragma unroll
-    for (int c = 0; c < kHistCopies; ++c) s += sm.hist[c][threadIdx.x];
-    sm.tot[threadIdx.x] = s;
+    unsigned long long acc = 0;
+    for (int r = 0; r < c.cs; ++r) acc += dsmem_ld_u64(dsmem_addr(&c.h->ex_arr[s][threadIdx.x], r));
+    c.h->tot[threadIdx.x] = acc;
   }
+  __syncthreads();
 }
 
-// Warp 0 scans tot[] from bin 255 down and finds the first bin where
-// before + tot[b] crosses the target: for counts the condition is
-// before + tot[b] >= target (target = remaining k), for mass it is
-// before + tot[b] > target.  Writes sel_bin (-1 if none) and sel_before.
-__device__ __forceinline__ void select_bin(SampSmem& sm, unsigned long long target, bool strict) {
-  if (threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
-  unsigned long long v[8], local = 0;
+__device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v, unsigned long long* s) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    v[e] = sm.tot[255 - (lane * 8 + e)];
-    local += v[e];
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long t = __shfl_xor_sync(FULL_MASK, v, o);
+    v = t > v ? t : v;
   }
-  unsigned long long incl = local;
+  __syncthreads();
+  if (lane == 0) s[warp] = v;
+  __syncthreads();
+  v = s[0];
+  for (int w = 1; w < kSampWarps; ++w) v = s[w] > v ? s[w] : v;
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, unsigned long long* s) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL_MASK, v, o);
+  __syncthreads();
+  if (lane == 0) s[warp] = v;
+  __syncthreads();
+  unsigned long long t = 0;
+  for (int w = 0; w < kSampWarps; ++w) t += s[w];
+  return t;
+}
+
+// Exclusive scan over threads of a u64 (thread order); ends with __syncthreads.
+__device__ __forceinline__ unsigned long long block_excl_scan_u64(unsigned long long v, unsigned long long* s,
+                                                                  unsigned long long& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const unsigned long long t = __shfl_up_sync(FULL_MASK, incl, o);
     if (lane >= o) incl += t;
   }
-  unsigned long long before = incl - local;
-  int found = -1;
-  unsigned long long fb = 0;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const unsigned long long after = before + v[e];
-    const bool hit = strict ? (after > target) : (after >= target);
-    if (found < 0 && hit) {
-      found = 255 - (lane * 8 + e);
-      fb = before;
-    }
-    before = after;
+  __syncthreads();
+  if (lane == 31) s[warp] = incl;
+  __syncthreads();
+  unsigned long long base = 0, tot = 0;
+  for (int w = 0; w < kSampWarps; ++w) {
+    const unsigned long long x = s[w];
+    if (w < warp) base += x;
+    tot += x;
   }
-  const unsigned ballot = __ballot_sync(FULL_MASK, found >= 0);
-  if (ballot == 0) {
-    if (lane == 0) { sm.sel_bin = -1; sm.sel_before = 0; }
-    return;
-  }
-  const int src = __ffs(ballot) - 1;
-  const int fbin = __shfl_sync(FULL_MASK, found, src);
-  const unsigned long long fbefore = __shfl_sync(FULL_MASK, fb, src);
-  if (lane == 0) { sm.sel_bin = fbin; sm.sel_before = fbefore; }
+  total = tot;
+  __syncthreads();
+  return base + incl - v;
 }
 
+// Sum of one float per thread in a fixed order (same result every run).
+__device__ __forceinline__ float block_sum_f32(float v, float* s) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL_MASK, v, o);
+  __syncthreads();
+  if (lane == 0) s[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+  for (int w = 0; w < kSampWarps; ++w) t += s[w];
+  return t;
+}
+
+// Warp 0 walks tot[] (descending bin order if DESC) and finds the first bin
+// where before + tot[b] crosses target (>= for counts, > for mass).
+// sel_bin = -1 if none; ends with __syncthreads.
+template <bool DESC>
+__device__ __forceinline__ void select_bin(SampHdr& h, unsigned long long target, bool strict) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    unsigned long long v[8], local = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int b = lane * 8 + e;
+      v[e] = h.tot[DESC ? 255 - b : b];
+      local += v[e];
+    }
+    unsigned long long incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long t = __shfl_up_sync(FULL_MASK, incl, o);
+      if (lane >= o) incl += t;
+    }
+    unsigned long long before = incl - local;
+    int found = -1;
+    unsigned long long fb = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const unsigned long long after = before + v[e];
+      if (found < 0 && (strict ? after > target : after >= target)) {
+        const int b = lane * 8 + e;
+        found = DESC ? 255 - b : b;
+        fb = before;
+      }
+      before = after;
+    }
+    const unsigned ballot = __ballot_sync(FULL_MASK, found >= 0);
+    if (ballot == 0) {
+      if (lane == 0) { h.sel_bin = -1; h.sel_before = 0; }
+    } else {
+      const int src = __ffs(ballot) - 1;
+      const int fbin = __shfl_sync(FULL_MASK, found, src);
+      const unsigned long long fbefore = __shfl_sync(FULL_MASK, fb, src);
+      if (lane == 0) { h.sel_bin = fbin; h.sel_before = fbefore; }
+    }
+  }
+  __syncthreads();
+}
+
+// round(w * 2^40) for w in [0, 1], built from the float's bits (no 64-bit
+// float conversion, which runs on the slow fp64 pipe of this part).
+__device__ __forceinline__ unsigned long long fixed_weight(float w) {
+  const uint32_t b = __float_as_uint(w);
+  const int ex = (int)((b >> 23) & 0xffu);
+  if (ex == 0) return 0ull;
+  const unsigned long long man = (b & 0x7fffffu) | 0x800000u;
+  const int sh = ex - 127 + 40 - 23;
+  if (sh >= 0) return man << sh;
+  if (sh < -24) return 0ull;
+  return (man + (1ull << (-sh - 1))) >> (-sh);
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL_MASK, v, o);
+  return v;
+}
+
+// Warp 0: first entry i of tot[0..N) (ascending) where base + tot[0..i]
+// crosses target (>= if !strict, > if strict).  Writes sel_bin = i (-1 if
+// none), sel_before = base + tot[0..i), sel_aux = tot[i]; ends with __syncthreads.
+template <int N>
+__device__ __forceinline__ void find_first(SampHdr& h, unsigned long long base, unsigned long long target,
+                                           bool strict) {
+  constexpr int PER = N / 32;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    unsigned long long v[PER], local = 0;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      v[e] = h.tot[lane * PER + e];
+      local += v[e];
+    }
+    unsigned long long incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long t = __shfl_up_sync(FULL_MASK, incl, o);
+      if (lane >= o) incl += t;
+    }
+    unsigned long long before = base + incl - local;
+    int found = -1;
+    unsigned long long fb = 0, fv = 0;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const unsigned long long after = before + v[e];
+      if (found < 0 && (strict ? after > target : after >= target)) {
+        found = lane * PER + e;
+        fb = before;
+        fv = v[e];
+      }
+      before = after;
+    }
+    const unsigned ballot = __ballot_sync(FULL_MASK, found >= 0);
+    if (ballot == 0) {
+      if (lane == 0) { h.sel_bin = -1; h.sel_before = 0; h.sel_val = 0; }
+    } else {
+      const int src = __ffs(ballot) - 1;
+      const int fi = __shfl_sync(FULL_MASK, found, src);
+      const unsigned long long b2 = __shfl_sync(FULL_MASK, fb, src);
+      const unsigned long long v2 = __shfl_sync(FULL_MASK, fv, src);
+      if (lane == 0) { h.sel_bin = fi; h.sel_before = b2; h.sel_val = v2; }
+    }
+  }
+  __syncthreads();
+}
+
+// Warp 0 sums tot[0..256) into h.zsum; ends with __syncthreads.
+__device__ __forceinline__ unsigned long long sum_tot(SampHdr& h) {
+  if (threadIdx.x < 32) {
+    unsigned long long s = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s += h.tot[threadIdx.x * 8 + e];
+    s = warp_sum_u64(s);
+    if (threadIdx.x == 0) h.zsum = s;
+  }
+  __syncthreads();
+  return h.zsum;
+}
+
+// Visit the CTA's elements: f(local index, raw bits).  `src` is shared or
+// global memory; 16-byte vectors when aligned.
+template <typename T, typename F>
+__device__ __forceinline__ void visit(const T* src, int n, bool vec, F&& f) {
+  constexpr int E = 16 / sizeof(T);
+  int done = 0;
+  if (vec) {
+    const int nv = n / E;
+    const uint4* sv = reinterpret_cast<const uint4*>(src);
+    for (int v = threadIdx.x; v < nv; v += kSampThreads) {
+      const uint4 u = sv[v];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const uint32_t b = (sizeof(T) == 4) ? w[e] : ((w[e / 2] >> (16 * (e & 1))) & 0xffffu);
+        f(v * E + e, b);
+      }
+    }
+    done = nv * E;
+  }
+  for (int j = done + threadIdx.x; j < n; j += kSampThreads)
+    f(j, sizeof(T) == 4 ? __float_as_uint(*reinterpret_cast<const float*>(src + j))
+                        : (uint32_t)(*reinterpret_cast<const unsigned short*>(src + j)));
+}
+
+struct SampArgs {
+  int fast;             // 16-bit keys, resident slice of <= 65535 ids: windowed path
+  int32_t* token_ids;
+  const void* logits;
+  int V;
+  int64_t row_stride;
+  int slice;            // elements per CTA (a multiple of 16 bytes)
+  int resident;         // slice held in shared memory
+  int vec;              // 16-byte aligned rows
+  const float* temperature;
+  const int32_t* top_k;
+  const float* top_p;
+  const uint64_t* seeds;
+  const uint64_t* offsets;
+};
+
 template <typename T>
-__global__ void __launch_bounds__(kSampThreads, 1)
-sample_kernel(int32_t* __restrict__ token_ids, const T* __restrict__ logits, int V, int64_t row_stride,
-              bool vec_ok, const float* __restrict__ temperature, const int32_t* __restrict__ top_k,
-              const float* __restrict__ top_p, const uint64_t* __restrict__ seeds,
-              const uint64_t* __restrict__ offsets) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  SampSmem& sm = *reinterpret_cast<SampSmem*>(smem_raw);
+constexpr int region_bytes() {
+  constexpr int w = sizeof(T) == 2 ? kWinTop * 4 : 0;
+  constexpr int hst = kHistCopies * 256 * 8;
+  constexpr int q = kSampWarps * kQueue * 8;
+  return (w > hst ? (w > q ? w : q) : (hst > q ? hst : q));
+}
+
+// Order-preserving keys of the two 16-bit floats of a word, in one go:
+// -0 is first folded onto +0, then key = b ^ 0xffff (negative) or b ^ 0x8000.
+__device__ __forceinline__ uint32_t keys2(uint32_t w) {
+  const uint32_t nz = ((w & 0x7fff7fffu) + 0x7fff7fffu) & 0x80008000u;   // magnitude != 0, per half
+  w &= nz | 0x7fff7fffu;
+  const uint32_t s = (w >> 15) & 0x00010001u;
+  return w ^ ((s * 0x7fffu) | 0x80008000u);
+}
+
+
+
+template <typename T>
+__global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs a) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
   using K = Keys<T>;
   constexpr int KB = K::BITS;
-  const int r = blockIdx.x;
-  const T* row = logits + (int64_t)r * row_stride;
-  const int copy = (threadIdx.x >> 5) & (kHistCopies - 1);
+  constexpr int E = 16 / sizeof(T);
+  SampHdr& h = *reinterpret_cast<SampHdr*>(smem_raw);
+  uint8_t* region = smem_raw + ((sizeof(SampHdr) + 127) / 128) * 128;
+  T* slice_smem = reinterpret_cast<T*>(region + region_bytes<T>());
+  // the region is reused: window counts, then radix bins, then Gumbel queues
+  uint32_t* win = reinterpret_cast<uint32_t*>(region);
+  unsigned long long (*hist)[256] = reinterpret_cast<unsigned long long (*)[256]>(region);
+  uint32_t* q_idx = reinterpret_cast<uint32_t*>(region);
+  float* q_x = reinterpret_cast<float*>(region + kSampWarps * kQueue * 4);
 
-  // ---- 1. max key, lowest index among maxima
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  Ctx c{&h, (int)cluster_size(), 0};
+  const uint32_t crank = cluster_rank();
+  const int row_id = blockIdx.x / c.cs;
+  const T* row = static_cast<const T*>(a.logits) + (int64_t)row_id * a.row_stride;
+  const int lo = (int)crank * a.slice;
+  const int n = max(0, min(a.V, lo + a.slice) - lo);
+  const int copy = warp & (kHistCopies - 1);
+
+  // ---- 0. slice -> shared memory (bulk copies, one barrier per chunk)
+  const T* src = row + lo;
+  bool vec = a.vec != 0;
+  if (a.resident) {
+    const int bytes = n * (int)sizeof(T);
+    const int bulk = bytes & ~15;
+    const int nch = (bulk + kChunkBytes - 1) / kChunkBytes;
+    if (tid == 0) {
+      for (int i = 0; i < nch; ++i) mbar_init(&h.bar[i], 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      for (int i = 0; i < nch; ++i) {
+        const int off = i * kChunkBytes;
+        const int sz = min(kChunkBytes, bulk - off);
+        mbar_arrive_expect_tx(&h.bar[i], (uint32_t)sz);
+        bulk_g2s(reinterpret_cast<uint8_t*>(slice_smem) + off, reinterpret_cast<const uint8_t*>(src) + off,
+                 (uint32_t)sz, &h.bar[i]);
+      }
+    }
+    for (int j = bulk / (int)sizeof(T) + tid; j < n; j += kSampThreads) slice_smem[j] = src[j];
+    for (int i = 0; i < nch; ++i) mbar_wait_bounded(&h.bar[i], 0);
+    __syncthreads();
+    src = slice_smem;
+    vec = true;
+  }
+
+  if constexpr (sizeof(T) == 2) {
+    if (a.fast) {
+      // ================= 16-bit logits, resident slice
+      const uint4* sv = reinterpret_cast<const uint4*>(src);
+      const int nvec = n / 8;
+      const int rest = nvec * 8;
+      auto bits_at = [&](int j) -> uint32_t { return (uint32_t)(*reinterpret_cast<const unsigned short*>(src + j)); };
+
+      // ---- F1. row max key
+      uint32_t mx = 0;
+      for (int v = tid; v < nvec; v += kSampThreads) {
+        const uint4 u = sv[v];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t k2 = keys2(w[q]);
+          mx = max(mx, max(k2 & 0xffffu, k2 >> 16));
+        }
+      }
+      for (int j = rest + tid; j < n; j += kSampThreads) mx = max(mx, K::key(bits_at(j)));
+      const uint32_t kmax = (uint32_t)cluster_scalar<true>(c, block_max_u64(mx, h.red), 0);
+      const float Tr = a.temperature[row_id];
+      if (!(Tr > 0.f)) {
+        // greedy: the lowest index holding the max key
+        uint32_t first = 0xffffffffu;
+        for (int v = tid; v < nvec; v += kSampThreads) {
+          const uint4 u = sv[v];
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t k2 = keys2(w[q]);
+            if ((k2 & 0xffffu) == kmax) first = min(first, (uint32_t)(v * 8 + q * 2));
+            if ((k2 >> 16) == kmax) first = min(first, (uint32_t)(v * 8 + q * 2 + 1));
+          }
+        }
+        for (int j = rest + tid; j < n; j += kSampThreads)
+          if (K::key(bits_at(j)) == kmax) first = min(first, (uint32_t)j);
+        // max of the complement = min index (lo + first, or 0 if none here)
+        const unsigned long long inv = first == 0xffffffffu ? 0ull : 0xffffffffull - (unsigned long long)(lo + first);
+        const unsigned long long best_inv = cluster_scalar<true>(c, block_max_u64(inv, h.red), 1);
+        if (crank == 0 && tid == 0) a.token_ids[row_id] = (int)(0xffffffffull - best_inv);
+        cluster_sync();               // peers may still read this CTA's shared memory
+        return;
+      }
+      const float m = K::value_of_key(kmax);
+      const float l2t = 1.4426950408889634f / Tr;
+      auto wfix = [&](float x) -> unsigned long long { return fixed_weight(exp2f((x - m) * l2t)); };
+      const int k = a.top_k[row_id];
+      const bool topk_on = k > 0 && k < a.V;
+      const float p = a.top_p[row_id];
+      const bool nucleus_on = p < 1.f;
+      uint32_t kth = 0, tau = 0;
+      long long need_eq = 0, cnt_eq = 0;
+      bool topk_done = !topk_on, nucleus_done = !nucleus_on;
+
+      // ---- F2. exact counts of the top kWinTop keys below the max; for the
+      // nucleus without top-k, the normaliser Z over every id as a
+      // compensated f32 sum per thread (fixed point from there on)
+      uint32_t* win = reinterpret_cast<uint32_t*>(region);
+      if (topk_on || nucleus_on) {
+        for (int i = tid; i < kWinTop; i += kSampThreads) win[i] = 0u;
+        __syncthreads();
+        const uint32_t kmax2 = kmax | (kmax << 16);
+        const bool need_z = nucleus_on && !topk_on;
+        float zs = 0.f, zc = 0.f;                 // compensated running sum
+        auto zadd = [&](float y) {
+          y -= zc;
+          const float t = zs + y;
+          zc = (t - zs) - y;
+          zs = t;
+        };
+        auto wexp = [&](uint32_t b) { return exp2f((K::value(b) - m) * l2t); };
+        for (int v = tid; v < nvec; v += kSampThreads) {
+          const uint4 u = sv[v];
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+          float vs = 0.f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t d2 = __vsub2(kmax2, keys2(w[q]));
+            const uint32_t dlo = d2 & 0xffffu, dhi = d2 >> 16;
+            if (dlo < (uint32_t)kWinTop) atomicAdd(&win[dlo], 1u);
+            if (dhi < (uint32_t)kWinTop) atomicAdd(&win[dhi], 1u);
+            if (need_z) vs += wexp(w[q] & 0xffffu) + wexp(w[q] >> 16);
+          }
+          if (need_z) zadd(vs);
+        }
+        for (int j = rest + tid; j < n; j += kSampThreads) {
+          const uint32_t b = bits_at(j);
+          const uint32_t d = kmax - K::key(b);
+          if (d < (uint32_t)kWinTop) atomicAdd(&win[d], 1u);
+          if (need_z) zadd(wexp(b));
+        }
+        // one cluster barrier: Z travels with it, and from here on every
+        // CTA's window is final, so peers read it in place over DSMEM
+        const unsigned long long zrow = cluster_scalar<false>(c, block_sum_u64(need_z ? fixed_weight(zs) : 0ull, h.red), 2);
+
+        // Walk the window down from the max, kWinBlock bins per step (4 per
+        // thread, contiguous); counts are the cluster sums of the bins.
+        constexpr int kPer = 4;
+        constexpr int kWinBlock = kSampThreads * kPer;
+        auto row_counts = [&](int d0, unsigned int* cnt) {
+          const int d = d0 + tid * kPer;
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) cnt[e] = 0;
+          for (int r = 0; r < c.cs; ++r) {
+            const uint32_t a4 = dsmem_addr(&win[d], (uint32_t)r);
+            uint4 x;
+            asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w) : "r"(a4) : "memory");
+            cnt[0] += x.x; cnt[1] += x.y; cnt[2] += x.z; cnt[3] += x.w;
+          }
+        };
+        if (topk_on) {
+          unsigned long long before = 0;
+          for (int d0 = 0; d0 < kWinTop && !topk_done; d0 += kWinBlock) {
+            unsigned int cnt[kPer];
+            row_counts(d0, cnt);
+            const unsigned long long mine = (unsigned long long)cnt[0] + cnt[1] + cnt[2] + cnt[3];
+            unsigned long long tot;
+            unsigned long long acc = before + block_excl_scan_u64(mine, h.red, tot);
+            if (acc < (unsigned long long)k && (unsigned long long)k <= acc + mine) {
+#pragma unroll
+              for (int e = 0; e < kPer; ++e) {
+                if (acc + cnt[e] >= (unsigned long long)k) {
+                  h.sel_aux = d0 + tid * kPer + e;
+                  h.sel_before = acc;
+                  h.sel_val = cnt[e];
+                  break;
+                }
+                acc += cnt[e];
+              }
+            }
+            __syncthreads();
+            if (before + tot >= (unsigned long long)k) {
+              kth = kmax - (uint32_t)h.sel_aux;
+              need_eq = k - (long long)h.sel_before;
+              cnt_eq = (long long)h.sel_val;
+              topk_done = true;
+            }
+            before += tot;
+            __syncthreads();
+          }
+        }
+        if (nucleus_on && topk_done) {
+          const int dk = topk_on ? (int)(kmax - kth) : kWinTop;   // bins past the k-th key are out
+          const unsigned long long tie_mass = topk_on ? (unsigned long long)need_eq * wfix(K::value_of_key(kth)) : 0ull;
+          auto bin_mass = [&](int d, unsigned int cnt) -> unsigned long long {
+            if (d > dk) return 0ull;
+            if (topk_on && d == dk) return tie_mass;
+            return cnt ? (unsigned long long)cnt * wfix(K::value_of_key(kmax - (uint32_t)d)) : 0ull;
+          };
+          unsigned long long Z = zrow;
+          if (topk_on) {          // Z of the top-k set: its bins all lie in the window
+            Z = 0;
+            for (int d0 = 0; d0 <= dk; d0 += kWinBlock) {
+              unsigned int cnt[kPer];
+              row_counts(d0, cnt);
+              unsigned long long mine = 0;
+#pragma unroll
+              for (int e = 0; e < kPer; ++e) mine += bin_mass(d0 + tid * kPer + e, cnt[e]);
+              Z += block_sum_u64(mine, h.red);
+            }
+          }
+          const unsigned long long P = (unsigned long long)((double)p * (double)Z);
+          unsigned long long before = 0;
+          for (int d0 = 0; d0 < kWinTop && d0 <= dk && !nucleus_done; d0 += kWinBlock) {
+            unsigned int cnt[kPer];
+            row_counts(d0, cnt);
+            unsigned long long mb[kPer], mine = 0;
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) {
+              mb[e] = bin_mass(d0 + tid * kPer + e, cnt[e]);
+              mine += mb[e];
+            }
+            unsigned long long tot;
+            unsigned long long acc = before + block_excl_scan_u64(mine, h.red, tot);
+            if (acc <= P && P < acc + mine) {
+#pragma unroll
+              for (int e = 0; e < kPer; ++e) {
+                if (acc + mb[e] > P) {
+                  h.sel_aux = d0 + tid * kPer + e;
+                  break;
+                }
+                acc += mb[e];
+              }
+            }
+            __syncthreads();
+            if (before + tot > P) {
+              tau = kmax - (uint32_t)h.sel_aux;
+              nucleus_done = true;
+            }
+            before += tot;
+            __syncthreads();
+          }
+        }
+        cluster_sync();          // every peer is done reading this CTA's window
+      }
+      // cuts the window cannot answer: radix selection over the slice
+      if (!topk_done) {
+        uint32_t prefix = 0;
+        unsigned long long remaining = (unsigned long long)k;
+        for (int shift = 8; shift >= 0; shift -= 8) {
+          for (int i = tid; i < kHistCopies * 256; i += kSampThreads) (&hist[0][0])[i] = 0ull;
+          __syncthreads();
+          const uint32_t hi_mask = shift == 8 ? 0u : 0xff00u;
+          visit<T>(src, n, true, [&](int, uint32_t b) {
+            const uint32_t key = K::key(b);
+            if ((key & hi_mask) == (prefix & hi_mask))
+              atomicAdd(reinterpret_cast<unsigned int*>(&hist[copy][(key >> shift) & 255u]), 1u);
+          });
+          __syncthreads();
+          if (tid < 256) {
+            unsigned long long s2 = 0;
+            for (int cp = 0; cp < kHistCopies; ++cp) s2 += (unsigned int)(hist[cp][tid] & 0xffffffffull);
+            h.ex_arr[c.ex][tid] = s2;
+          }
+          cluster_sum_array(c);
+          select_bin<true>(h, remaining, false);
+          const int bin = h.sel_bin;
+          remaining -= h.sel_before;
+          prefix |= (uint32_t)bin << shift;
+          if (shift == 0) cnt_eq = (long long)h.tot[bin];
+          __syncthreads();
+        }
+        kth = prefix;
+        need_eq = (long long)remaining;
+        topk_done = true;
+      }
+      if (!nucleus_done) {
+        uint32_t prefix = 0;
+        unsigned long long target = 0, above = 0;
+        for (int shift = 8; shift >= 0; shift -= 8) {
+          for (int i = tid; i < kHistCopies * 256; i += kSampThreads) (&hist[0][0])[i] = 0ull;
+          __syncthreads();
+          const uint32_t hi_mask = shift == 8 ? 0u : 0xff00u;
+          visit<T>(src, n, true, [&](int, uint32_t b) {
+            const uint32_t key = K::key(b);
+            if ((key & hi_mask) != (prefix & hi_mask)) return;
+            if (topk_on && key <= kth) return;
+            atomicAdd(&hist[copy][(key >> shift) & 255u], wfix(K::value(b)));
+          });
+          __syncthreads();
+          if (tid < 256) {
+            unsigned long long s2 = 0;
+            for (int cp = 0; cp < kHistCopies; ++cp) s2 += hist[cp][tid];
+            if (crank == 0 && topk_on && need_eq > 0 && (kth & hi_mask) == (prefix & hi_mask) &&
+                (int)((kth >> shift) & 255u) == tid)
+              s2 += (unsigned long long)need_eq * wfix(K::value_of_key(kth));
+            h.ex_arr[c.ex][tid] = s2;
+          }
+          cluster_sum_array(c);
+          if (shift == 8) target = (unsigned long long)((double)p * (double)sum_tot(h));
+          select_bin<true>(h, target - above, true);
+          const int bin = h.sel_bin;
+          const unsigned long long sb = h.sel_before;
+          __syncthreads();
+          if (bin < 0) { prefix = 0; break; }
+          above += sb;
+          prefix |= (uint32_t)bin << shift;
+        }
+        tau = prefix;
+      }
+
+      // ---- F3. this CTA's share of the lowest-index ties at the k-th key
+      int tie_lim = 0x7fffffff;
+      if (topk_on && need_eq < cnt_eq) {
+        unsigned long long mine = 0;
+        visit<T>(src, n, true, [&](int, uint32_t b) { mine += K::key(b) == kth; });
+        mine = block_sum_u64(mine, h.red);
+        long long before = 0;
+        {
+          const int sl = c.ex;
+          c.ex ^= 1;
+          if (tid == 0) h.ex_sc[sl][2] = mine;
+          cluster_sync();
+          for (int r = 0; r < (int)crank; ++r) before += (long long)dsmem_ld_u64(dsmem_addr(&h.ex_sc[sl][2], r));
+        }
+        const long long want = min(max(need_eq - before, 0ll), (long long)mine);
+        if (want == 0) {
+          tie_lim = -1;
+        } else if (want < (long long)mine) {
+          uint32_t prefix = 0;
+          unsigned long long remaining = (unsigned long long)want;
+          for (int shift = 16; shift >= 0; shift -= 8) {       // 24-bit slice-local indices
+            for (int i = tid; i < kHistCopies * 256; i += kSampThreads) (&hist[0][0])[i] = 0ull;
+            __syncthreads();
+            const uint32_t hi_mask = (shift + 8 >= 24) ? 0u : ((~0u << (shift + 8)) & 0xffffffu);
+            visit<T>(src, n, true, [&](int j, uint32_t b) {
+              if (K::key(b) != kth) return;
+              const uint32_t ik = 0xffffffu - (uint32_t)j;
+              if ((ik & hi_mask) == (prefix & hi_mask))
+                atomicAdd(reinterpret_cast<unsigned int*>(&hist[copy][(ik >> shift) & 255u]), 1u);
+            });
+            __syncthreads();
+            if (tid < 256) {
+              unsigned long long s2 = 0;
+              for (int cp = 0; cp < kHistCopies; ++cp) s2 += (unsigned int)(hist[cp][tid] & 0xffffffffull);
+              h.tot[tid] = s2;
+            }
+            __syncthreads();
+            select_bin<true>(h, remaining, false);
+            remaining -= h.sel_before;
+            prefix |= (uint32_t)h.sel_bin << shift;
+            __syncthreads();
+          }
+          tie_lim = (int)(0xffffffu - prefix);
+        }
+      }
+
+      // ---- F4. Gumbel-max over the kept ids.  A packed key test (two keys per
+      // step) finds the few candidates; only they get Philox noise.
+      uint32_t thr = tau;
+      if (topk_on && kth > thr) thr = kth;
+      {
+        // ids below m - 22 T can never win: fold that into the key threshold
+        const float vmin = m - 22.f * Tr;
+        T tv;
+        if constexpr (std::is_same<T, __half>::value) tv = __float2half_rd(vmin);
+        else tv = __float2bfloat16_rd(vmin);
+        const uint32_t kp = K::key((uint32_t)(*reinterpret_cast<const unsigned short*>(&tv)));
+        if (!isinf(vmin) && kp > thr) thr = kp;
+      }
+      const uint32_t thr2 = thr | (thr << 16);
+      const uint64_t seed = a.seeds[row_id], off = a.offsets[row_id];
+      const float invT = 1.f / Tr;
+      auto keep = [&](int j, uint32_t b) -> bool {
+        const uint32_t key = K::key(b);
+        if (key < tau) return false;
+        if (topk_on && (key < kth || (key == kth && j > tie_lim))) return false;
+        return (K::value(b) - m) * invT >= -kGumbelSpan;
+      };
+      auto score_of = [&](int jg, uint32_t b) -> unsigned long long {
+        const float sc = __fdiv_rn(K::value(b), Tr) + gumbel_noise(seed, off, (uint32_t)jg);
+        return ((unsigned long long)f32_order_key(sc) << 32) | (0xffffffffu - (uint32_t)jg);
+      };
+      // per-thread candidate slots, slot-major so the stores do not collide;
+      // a thread that meets more than kSlots candidates flags the CTA, which
+      // then scores through per-warp queues instead
+      constexpr int kSlots = region_bytes<T>() / 4 / kSampThreads;
+      uint32_t* slot = reinterpret_cast<uint32_t*>(region);
+      if (tid == 0) h.cand_n = 0;                   // overflow flag
+      __syncthreads();
+      int mine = 0;
+      auto take = [&](int j, uint32_t b) {
+        if (K::key(b) < thr) return;
+        if (mine < kSlots) slot[mine * kSampThreads + tid] = (uint32_t)j;
+        ++mine;
+      };
+      for (int v = tid; v < nvec; v += kSampThreads) {
+        const uint4 u = sv[v];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        uint32_t cb = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t ge = __vcmpgeu2(keys2(w[q]), thr2);
+          cb |= ((ge & 1u) | ((ge >> 15) & 2u)) << (2 * q);
+        }
+        while (cb) {
+          const int e = __ffs(cb) - 1;
+          cb &= cb - 1;
+          take(v * 8 + e, (w[e / 2] >> (16 * (e & 1))) & 0xffffu);
+        }
+      }
+      for (int j = rest + tid; j < n; j += kSampThreads) take(j, bits_at(j));
+      if (mine > kSlots) h.cand_n = 1;
+      __syncthreads();
+      unsigned long long bestg = 0;
+      if (!h.cand_n) {
+        for (int i = 0; i < mine; ++i) {
+          const int j = (int)slot[i * kSampThreads + tid];
+          const uint32_t b = bits_at(j);
+          if (keep(j, b)) {
+            const unsigned long long pk = score_of(lo + j, b);
+            bestg = pk > bestg ? pk : bestg;
+          }
+        }
+      } else {
+        // dense kept set: every warp queues its candidates and scores them
+        // 32 at a time (full warps)
+        __syncthreads();
+        uint32_t* qi = reinterpret_cast<uint32_t*>(region) + warp * kQueue;
+        int qh = 0, qn = 0;
+        auto drain = [&](int cnt) {
+          if (lane < cnt) {
+            const int j = (int)qi[(qh + lane) & (kQueue - 1)];
+            const unsigned long long pk = score_of(lo + j, bits_at(j));
+            bestg = pk > bestg ? pk : bestg;
+          }
+          __syncwarp();
+          qh = (qh + cnt) & (kQueue - 1);
+          qn -= cnt;
+        };
+        for (int jb = warp * 32; jb < n; jb += kSampThreads) {      // warp-uniform trip count
+          const int j = jb + lane;
+          const bool cand = j < n && keep(j, bits_at(j));
+          const unsigned mask = __ballot_sync(FULL_MASK, cand);
+          if (mask) {
+            if (cand) qi[(qh + qn + __popc(mask & ((1u << lane) - 1u))) & (kQueue - 1)] = (uint32_t)j;
+            qn += __popc(mask);
+            __syncwarp();
+            if (qn >= 32) drain(32);
+          }
+        }
+        if (qn > 0) drain(qn);
+      }
+      bestg = block_max_u64(bestg, h.red);
+      bestg = cluster_scalar<true>(c, bestg, 3);
+      // the max id always passes every filter, so bestg is never 0 here
+      if (crank == 0 && tid == 0) a.token_ids[row_id] = (int)(0xffffffffu - (uint32_t)(bestg & 0xffffffffull));
+      cluster_sync();               // peers may still read this CTA's shared memory
+      return;
+    }
+  }
+
+  // ---- 1. max key and the lowest index holding it (row-wide)
   unsigned long long best = 0;
-  for_each_elem<T>(row, V, vec_ok, [&](int j, uint32_t b) {
-    const unsigned long long pk = ((unsigned long long)K::key(b) << 32) | (0xffffffffu - (uint32_t)j);
+  visit<T>(src, n, vec, [&](int j, uint32_t b) {
+    const unsigned long long pk = ((unsigned long long)K::key(b) << 32) | (0xffffffffu - (uint32_t)(lo + j));
     best = pk > best ? pk : best;
   });
-  best = block_max_u64(best, sm.red);
+  best = block_max_u64(best, h.red);
+  best = cluster_scalar<true>(c, best, 0);
   const uint32_t kmax = (uint32_t)(best >> 32);
   const int imax = (int)(0xffffffffu - (uint32_t)(best & 0xffffffffu));
-  const float T_ = temperature[r];
-  if (!(T_ > 0.f)) {
-    if (threadIdx.x == 0) token_ids[r] = imax;
+  const float Tr = a.temperature[row_id];
+  if (!(Tr > 0.f)) {
+    if (crank == 0 && tid == 0) a.token_ids[row_id] = imax;
+    cluster_sync();               // peers may still read this CTA's shared memory
     return;
   }
   const float m = K::value_of_key(kmax);
-  const float log2e_over_T = 1.4426950408889634f / T_;
+  const float l2t = 1.4426950408889634f / Tr;
+  auto wfix = [&](float x) -> unsigned long long { return fixed_weight(exp2f((x - m) * l2t)); };
 
-  // ---- 2. top-k threshold key (exactly k kept)
-  const int k = top_k[r];
-  const bool topk_on = k > 0 && k < V;
+  const int k = a.top_k[row_id];
+  const bool topk_on = k > 0 && k < a.V;
+  const float p = a.top_p[row_id];
+  const bool nucleus_on = p < 1.f;
   uint32_t kth = 0;          // key of the k-th largest
-  int need_eq = 0, cnt_eq = 0;
-  if (topk_on) {
+  long long need_eq = 0, cnt_eq = 0;
+  uint32_t tau = 0;          // keep key >= tau
+  bool topk_done = false, nucleus_done = false;
+
+  // ---- 3. generic top-k: MSB-first radix select with cluster-summed bins
+  if (topk_on && !topk_done) {
     uint32_t prefix = 0;
     unsigned long long remaining = (unsigned long long)k;
     for (int shift = KB - 8; shift >= 0; shift -= 8) {
-      hist_clear(sm);
+      for (int i = tid; i < kHistCopies * 256; i += kSampThreads) (&hist[0][0])[i] = 0ull;
       __syncthreads();
       const uint32_t hi_mask = (shift + 8 >= 32) ? 0u : (~0u << (shift + 8));
-      for_each_elem<T>(row, V, vec_ok, [&](int, uint32_t b) {
+      visit<T>(src, n, vec, [&](int, uint32_t b) {
         const uint32_t key = K::key(b);
         if ((key & hi_mask) == (prefix & hi_mask))
-          atomicAdd(reinterpret_cast<unsigned int*>(&sm.hist[copy][(key >> shift) & 255u]), 1u);
+          atomicAdd(reinterpret_cast<unsigned int*>(&hist[copy][(key >> shift) & 255u]), 1u);
       });
       __syncthreads();
-      if (threadIdx.x < 256) {
+      if (tid < 256) {
         unsigned long long s = 0;
-#pragma unroll
-        for (int c = 0; c < kHistCopies; ++c)
-          s += (unsigned int)(sm.hist[c][threadIdx.x] & 0xffffffffull);
-        sm.tot[threadIdx.x] = s;
+        for (int cp = 0; cp < kHistCopies; ++cp) s += (unsigned int)(hist[cp][tid] & 0xffffffffull);
+        h.ex_arr[c.ex][tid] = s;
       }
-      __syncthreads();
-      select_bin(sm, remaining, false);
-      __syncthreads();
-      const int bin = sm.sel_bin;
-      remaining -= sm.sel_before;
+      cluster_sum_array(c);
+      select_bin<true>(h, remaining, false);
+      const int bin = h.sel_bin;
+      remaining -= h.sel_before;
       prefix |= (uint32_t)bin << shift;
-      if (shift == 0) cnt_eq = (int)sm.tot[bin];
+      if (shift == 0) cnt_eq = (long long)h.tot[bin];
       __syncthreads();
     }
     kth = prefix;
-    need_eq = (int)remaining;
+    need_eq = (long long)remaining;
   }
 
-  // fixed-point weight of a value: exp((x - m) / T) * 2^40, rounded
-  auto wfix = [&](float x) -> unsigned long long {
-    const float w = exp2f((x - m) * log2e_over_T);
-    return __float2ull_rn(w * 1099511627776.0f);
-  };
-
-  // ---- 3. nucleus threshold key tau (keep key >= tau)
-  const float p = top_p[r];
-  uint32_t tau = 0;
-  if (p < 1.f) {
+  // ---- 4. generic nucleus: radix select on cluster-summed fixed-point mass
+  if (nucleus_on && !nucleus_done) {
     uint32_t prefix = 0;
     unsigned long long target = 0, above = 0;
-    bool done = false;
-    for (int shift = KB - 8; shift >= 0 && !done; shift -= 8) {
-      hist_clear(sm);
+    for (int shift = KB - 8; shift >= 0; shift -= 8) {
+      for (int i = tid; i < kHistCopies * 256; i += kSampThreads) (&hist[0][0])[i] = 0ull;
       __syncthreads();
       const uint32_t hi_mask = (shift + 8 >= 32) ? 0u : (~0u << (shift + 8));
-      for_each_elem<T>(row, V, vec_ok, [&](int, uint32_t b) {
+      visit<T>(src, n, vec, [&](int, uint32_t b) {
         const uint32_t key = K::key(b);
         if ((key & hi_mask) != (prefix & hi_mask)) return;
-        if (topk_on && key <= kth) return;     // ties at the k-th key added below
-        atomicAdd(&sm.hist[copy][(key >> shift) & 255u], wfix(K::value(b)));
+        if (topk_on && key <= kth) return;     // the k-th key's ties are added below
+        atomicAdd(&hist[copy][(key >> shift) & 255u], wfix(K::value(b)));
       });
       __syncthreads();
-      if (threadIdx.x == 0 && topk_on && need_eq > 0 && (kth & hi_mask) == (prefix & hi_mask))
-        sm.hist[0][(kth >> shift) & 255u] += (unsigned long long)need_eq * wfix(K::value_of_key(kth));
-      __syncthreads();
-      hist_total(sm);
-      __syncthreads();
+      if (tid < 256) {
+        unsigned long long s = 0;
+        for (int cp = 0; cp < kHistCopies; ++cp) s += hist[cp][tid];
+        if (crank == 0 && topk_on && need_eq > 0 && (kth & hi_mask) == (prefix & hi_mask) &&
+            (int)((kth >> shift) & 255u) == tid)
+          s += (unsigned long long)need_eq * wfix(K::value_of_key(kth));
+        h.ex_arr[c.ex][tid] = s;
+      }
+      cluster_sum_array(c);
       if (shift == KB - 8) {
         unsigned long long Z = 0;
-        for (int b = 0; b < 256; ++b) Z += sm.tot[b];   // same value in every thread
+        for (int b = 0; b < 256; ++b) Z += h.tot[b];
         target = (unsigned long long)((double)p * (double)Z);
       }
-      select_bin(sm, target - above, true);
+      select_bin<true>(h, target - above, true);
+      const int bin = h.sel_bin;
+      const unsigned long long sb = h.sel_before;
       __syncthreads();
-      const int bin = sm.sel_bin;
-      if (bin < 0) {
-        prefix = 0;          // the whole set is needed to exceed p: keep all
-        done = true;
-      } else {
-        above += sm.sel_before;
-        prefix |= (uint32_t)bin << shift;
+      if (bin < 0) {            // the whole set is needed to exceed p: keep all
+        prefix = 0;
+        break;
       }
-      __syncthreads();
+      above += sb;
+      prefix |= (uint32_t)bin << shift;
     }
     tau = prefix;
   }
 
-  // ---- 4. Gumbel-max over the kept ids
-  const uint64_t seed = seeds[r], off = offsets[r];
-  const float span = -kGumbelSpan;
-  unsigned long long win = 0;
-  auto consider = [&](int j, uint32_t b, bool tie_ok) {
-    const uint32_t key = K::key(b);
-    if (key < tau) return;
-    if (topk_on && (key < kth || (key == kth && !tie_ok))) return;
-    const float x = K::value(b);
-    if ((x - m) * (1.f / T_) < span) return;
-    const float score = __fdiv_rn(x, T_) + gumbel_noise(seed, off, (uint32_t)j);
-    const unsigned long long pk = ((unsigned long long)f32_order_key(score) << 32) | (0xffffffffu - (uint32_t)j);
-    win = pk > win ? pk : win;
-  };
-  // ties at the k-th key straddle the cut: keep the need_eq lowest indices,
-  // i.e. those <= the need_eq-th smallest index of the tie group (radix
-  // select on 24-bit inverted indices, counting tie elements only)
-  const bool need_rank = topk_on && need_eq < cnt_eq;
-  uint32_t tie_cut = 0xffffffffu;
-  if (need_rank) {
-    uint32_t prefix = 0;
-    unsigned long long remaining = (unsigned long long)need_eq;
-    for (int shift = 16; shift >= 0; shift -= 8) {
-      hist_clear(sm);
-      __syncthreads();
-      const uint32_t hi_mask = (shift + 8 >= 24) ? 0u : ((~0u << (shift + 8)) & 0xffffffu);
-      for_each_elem<T>(row, V, vec_ok, [&](int j, uint32_t b) {
-        if (K::key(b) != kth) return;
-        const uint32_t ik = 0xffffffu - (uint32_t)j;
-        if ((ik & hi_mask) == (prefix & hi_mask))
-          atomicAdd(reinterpret_cast<unsigned int*>(&sm.hist[copy][(ik >> shift) & 255u]), 1u);
-      });
-      __syncthreads();
-      if (threadIdx.x < 256) {
-        unsigned long long s = 0;
-#pragma unroll
-        for (int c = 0; c < kHistCopies; ++c)
-          s += (unsigned int)(sm.hist[c][threadIdx.x] & 0xffffffffull);
-        sm.tot[threadIdx.x] = s;
-      }
-      __syncthreads();
-      select_bin(sm, remaining, false);
-      __syncthreads();
-      remaining -= sm.sel_before;
-      prefix |= (uint32_t)sm.sel_bin << shift;
-      __syncthreads();
+  // ---- 5. ties at the k-th key straddling the cut: this CTA's share of the
+  // lowest-index ties (slices are ordered by index), found by a local radix
+  // select over its tie indices; tie_lim = largest local index kept
+  int tie_lim = 0x7fffffff;
+  if (topk_on && need_eq < cnt_eq) {
+    unsigned long long mine = 0;
+    visit<T>(src, n, vec, [&](int, uint32_t b) { mine += K::key(b) == kth; });
+    mine = block_sum_u64(mine, h.red);
+    long long before = 0;
+    {
+      const int s = c.ex;
+      c.ex ^= 1;
+      if (tid == 0) h.ex_sc[s][2] = mine;
+      cluster_sync();
+      for (int r = 0; r < (int)crank; ++r) before += (long long)dsmem_ld_u64(dsmem_addr(&h.ex_sc[s][2], r));
     }
-    tie_cut = 0xffffffu - prefix;
+    const long long want = min(max(need_eq - before, 0ll), (long long)mine);
+    if (want == 0) {
+      tie_lim = -1;
+    } else if (want < (long long)mine) {
+      uint32_t prefix = 0;
+      unsigned long long remaining = (unsigned long long)want;
+      for (int shift = 16; shift >= 0; shift -= 8) {
+        for (int i = tid; i < kHistCopies * 256; i += kSampThreads) (&hist[0][0])[i] = 0ull;
+        __syncthreads();
+        const uint32_t hi_mask = (shift + 8 >= 24) ? 0u : ((~0u << (shift + 8)) & 0xffffffu);
+        visit<T>(src, n, vec, [&](int j, uint32_t b) {
+          if (K::key(b) != kth) return;
+          const uint32_t ik = 0xffffffu - (uint32_t)j;
+          if ((ik & hi_mask) == (prefix & hi_mask))
+            atomicAdd(reinterpret_cast<unsigned int*>(&hist[copy][(ik >> shift) & 255u]), 1u);
+        });
+        __syncthreads();
+        if (tid < 256) {
+          unsigned long long s = 0;
+          for (int cp = 0; cp < kHistCopies; ++cp) s += (unsigned int)(hist[cp][tid] & 0xffffffffull);
+          h.tot[tid] = s;
+        }
+        __syncthreads();
+        select_bin<true>(h, remaining, false);
+        remaining -= h.sel_before;
+        prefix |= (uint32_t)h.sel_bin << shift;
+        __syncthreads();
+      }
+      tie_lim = (int)(0xffffffu - prefix);
+    }
   }
-  for_each_elem<T>(row, V, vec_ok, [&](int j, uint32_t b) { consider(j, b, (uint32_t)j <= tie_cut); });
-  win = block_max_u64(win, sm.red);
-  if (threadIdx.x == 0) {
-    token_ids[r] = win ? (int)(0xffffffffu - (uint32_t)(win & 0xffffffffull)) : imax;
+
+  // ---- 6. Gumbel-max over the kept ids, candidates queued per warp
+  const uint64_t seed = a.seeds[row_id], off = a.offsets[row_id];
+  const float invT = 1.f / Tr;
+  unsigned long long bestg = 0;
+  uint32_t* qi = q_idx + warp * kQueue;
+  float* qx = q_x + warp * kQueue;
+  int qh = 0, qn = 0;
+  __syncthreads();                              // the region now holds the queues
+  auto keep = [&](int j, uint32_t b) -> bool {
+    const uint32_t key = K::key(b);
+    if (key < tau) return false;
+    if (topk_on && (key < kth || (key == kth && j > tie_lim))) return false;
+    return (K::value(b) - m) * invT >= -kGumbelSpan;
+  };
+  auto drain = [&](int cnt) {
+    if (lane < cnt) {
+      const int slot = (qh + lane) & (kQueue - 1);
+      const uint32_t j = qi[slot];
+      const float score = __fdiv_rn(qx[slot], Tr) + gumbel_noise(seed, off, j);
+      const unsigned long long pk = ((unsigned long long)f32_order_key(score) << 32) | (0xffffffffu - j);
+      bestg = pk > bestg ? pk : bestg;
+    }
+    __syncwarp();
+    qh = (qh + cnt) & (kQueue - 1);
+    qn -= cnt;
+  };
+  auto push = [&](bool cand, int j, uint32_t b) {
+    const unsigned mask = __ballot_sync(FULL_MASK, cand);
+    if (mask) {
+      if (cand) {
+        const int slot = (qh + qn + __popc(mask & ((1u << lane) - 1u))) & (kQueue - 1);
+        qi[slot] = (uint32_t)(lo + j);
+        qx[slot] = K::value(b);
+      }
+      qn += __popc(mask);
+      __syncwarp();
+      if (qn >= 32) drain(32);
+    }
+  };
+  {
+    const int nvec = vec ? n / E : 0;
+    const uint4* sv = reinterpret_cast<const uint4*>(src);
+    for (int vb = warp * 32; vb < nvec; vb += kSampThreads) {     // warp-uniform trip count
+      const int v = vb + lane;
+      uint4 u = make_uint4(0, 0, 0, 0);
+      if (v < nvec) u = sv[v];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const uint32_t b = (sizeof(T) == 4) ? w[e] : ((w[e / 2] >> (16 * (e & 1))) & 0xffffu);
+        const int j = v * E + e;
+        push(v < nvec && keep(j, b), j, b);
+      }
+    }
+    for (int jb = nvec * E + warp * 32; jb < n; jb += kSampThreads) {
+      const int j = jb + lane;
+      uint32_t b = 0;
+      if (j < n)
+        b = sizeof(T) == 4 ? __float_as_uint(*reinterpret_cast<const float*>(src + j))
+                           : (uint32_t)(*reinterpret_cast<const unsigned short*>(src + j));
+      push(j < n && keep(j, b), j, b);
+    }
+    if (qn > 0) drain(qn);
   }
+  bestg = block_max_u64(bestg, h.red);
+  bestg = cluster_scalar<true>(c, bestg, 3);
+  if (crank == 0 && tid == 0)
+    a.token_ids[row_id] = bestg ? (int)(0xffffffffu - (uint32_t)(bestg & 0xffffffffull)) : imax;
+  cluster_sync();               // peers may still read this CTA's shared memory
+}
+
+
+// Clusters of `cs` CTAs with `smem` bytes each that the GPU runs at once
+// (cached per size; a failed query falls back to an SM-count estimate).
+template <typename T>
+static int max_active_clusters(int cs, size_t smem, int sms) {
+  static int cache[4][64];
+  static size_t cache_smem[4][64];
+  int li = cs == 1 ? 0 : cs == 2 ? 1 : cs == 4 ? 2 : 3;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  dev &= 63;
+  if (cache[li][dev] > 0 && cache_smem[li][dev] == smem) return cache[li][dev];
+  int n = 0;
+  if (cudaFuncSetAttribute(sample_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cs);
+    cfg.blockDim = dim3(kSampThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, sample_kernel<T>, &cfg) != cudaSuccess) n = 0;
+  }
+  (void)cudaGetLastError();
+  if (n <= 0) n = sms / cs > 0 ? sms / cs : 1;
+  cache[li][dev] = n;
+  cache_smem[li][dev] = smem;
+  return n;
+}
+
+template <typename T>
+static cudaError_t launch_sample_t(const SampArgs& base, int num_rows, cudaStream_t stream) {
+  constexpr int kMaxSmem = 232448;
+  const size_t hdr = ((sizeof(SampHdr) + 127) / 128) * 128;
+  const size_t region = (size_t)region_bytes<T>();
+  const int esz = (int)sizeof(T);
+  const int align = 16 / esz;
+  const int sms = device_sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  // cluster size: for CS in 1, 2, 4, 8 whose slice fits on chip, estimate
+  // the time as (waves of clusters the GPU co-schedules) x (ids per CTA)
+  // and keep the cheapest, preferring the smaller cluster on a tie
+  auto slice_of = [&](int c) { return ((base.V + c - 1) / c + align - 1) / align * align; };
+  const size_t budget = kMaxSmem - hdr - region;
+  const size_t chunk_cap = (size_t)kMaxChunks * kChunkBytes;
+  const size_t cap = budget < chunk_cap ? budget : chunk_cap;
+  int cs = 0;
+  long long best_cost = 0;
+  for (int c = 1; c <= kMaxCluster; c *= 2) {
+    const size_t sb = (size_t)slice_of(c) * esz;
+    const bool res = base.vec && sb <= cap;
+    if (!res && c < kMaxCluster) continue;
+    const size_t sm = hdr + region + (res ? sb : 0);
+    const int act = max_active_clusters<T>(c, sm, sms);
+    const long long waves = ((long long)num_rows + act - 1) / act;
+    const long long cost = waves * slice_of(c);
+    if (cs == 0 || cost < best_cost) {
+      cs = c;
+      best_cost = cost;
+    }
+  }
+  SampArgs a = base;
+  a.slice = slice_of(cs);
+  const size_t sbytes = (size_t)a.slice * esz;
+  a.resident = (a.vec && sbytes <= cap) ? 1 : 0;
+  a.fast = (esz == 2 && a.resident && a.slice < (1 << 24)) ? 1 : 0;
+  const size_t smem = hdr + region + (a.resident ? sbytes : 0);
+  {
+    cudaError_t e = cudaFuncSetAttribute(sample_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(num_rows * cs));
+  cfg.blockDim = dim3(kSampThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, sample_kernel<T>, a);
 }
 
 cudaError_t launch_sample(int32_t* token_ids, const void* logits, int dtype, int num_rows, int vocab,
@@ -408,26 +1236,25 @@ cudaError_t launch_sample(int32_t* token_ids, const void* logits, int dtype, int
                           cudaStream_t stream) {
   if (num_rows == 0) return cudaSuccess;
   const int esz = dtype == PKVD_F32 ? 4 : 2;
-  const bool vec_ok = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && ((row_stride * esz) % 16 == 0);
-  const size_t smem = sizeof(SampSmem);
-  cudaError_t e = cudaSuccess;
-#define PKVD_LAUNCH_SAMPLE(TYPE)                                                                     \
-  do {                                                                                               \
-    static bool configured = false;                                                                  \
-    if (!configured) {                                                                               \
-      e = cudaFuncSetAttribute(sample_kernel<TYPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,    \
-                               (int)smem);                                                           \
-      if (e != cudaSuccess) return e;                                                                \
-      configured = true;                                                                             \
-    }                                                                                                \
-    sample_kernel<TYPE><<<num_rows, kSampThreads, smem, stream>>>(                                   \
-        token_ids, static_cast<const TYPE*>(logits), vocab, row_stride, vec_ok, temperature, top_k,  \
-        top_p, seeds, offsets);                                                                      \
-  } while (0)
-  if (dtype == PKVD_F32) PKVD_LAUNCH_SAMPLE(float);
-  else if (dtype == PKVD_F16) PKVD_LAUNCH_SAMPLE(__half);
-  else PKVD_LAUNCH_SAMPLE(__nv_bfloat16);
-#undef PKVD_LAUNCH_SAMPLE
+  SampArgs a;
+  a.fast = 0;
+  a.token_ids = token_ids;
+  a.logits = logits;
+  a.V = vocab;
+  a.row_stride = row_stride;
+  a.slice = vocab;
+  a.resident = 0;
+  a.vec = ((reinterpret_cast<uintptr_t>(logits) % 16 == 0) && ((row_stride * esz) % 16 == 0)) ? 1 : 0;
+  a.temperature = temperature;
+  a.top_k = top_k;
+  a.top_p = top_p;
+  a.seeds = seeds;
+  a.offsets = offsets;
+  cudaError_t e;
+  if (dtype == PKVD_F32) e = launch_sample_t<float>(a, num_rows, stream);
+  else if (dtype == PKVD_F16) e = launch_sample_t<__half>(a, num_rows, stream);
+  else e = launch_sample_t<__nv_bfloat16>(a, num_rows, stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

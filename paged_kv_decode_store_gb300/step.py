@@ -9,7 +9,7 @@ device buffer owned by this object; a step is: write the inputs into those
 buffers, replay.
 
 Step order (all library kernels):
-    slot_mapping -> kv_store -> paged_decode_attention (partition + merge) -> sample
+    slot_mapping -> kv_store -> paged_decode_attention (partition, fused merge) -> sample
 """
 from __future__ import annotations
 
@@ -52,10 +52,10 @@ class DecodeStep:
         nbytes = ctypes.c_size_t(0)
         _capi.check(_capi.lib().pkvd_decode_workspace_bytes(B, Hq, D, max_context_len, 0,
                                                             ctypes.byref(nbytes)))
-        self.workspace = torch.empty(max(int(nbytes.value), 16), dtype=torch.uint8, device=dev)
+        self.workspace = torch.zeros(max(int(nbytes.value), 16), dtype=torch.uint8, device=dev)
         self.cache = _capi.cache_desc(k_cache, v_cache)
         self.graph = None
-        self.kernels_per_step = 5     # slot, store, partition, merge, sample
+        self.kernels_per_step = 4     # slot, store, attention (partition + fused merge), sample
 
     def enqueue(self, stream=None) -> None:
         L = _capi.lib()

@@ -169,3 +169,41 @@ def test_unaligned_rows_use_the_scalar_path():
                     torch.ones(8, device=DEV), z, z).cpu().tolist()
     ref = [oracle.sampler.greedy(base[i, 1:].double().numpy()) for i in range(8)]
     assert tok == ref
+
+
+def test_window_fallback_when_top_k_lies_below_the_window():
+    """Keys more than 32768 steps below the max force the radix fallback."""
+    pk = require_gpu()
+    V, R = 4096, 3000
+    x = torch.full((V,), -65000.0)
+    x[1234] = 65000.0
+    logits = x.to(torch.float16).unsqueeze(0).repeat(R, 1).to(DEV)
+    tok = pk.sample(logits, torch.full((R,), 1e6, device=DEV), torch.full((R,), 5, dtype=torch.int32, device=DEV),
+                    torch.ones(R, device=DEV), torch.full((R,), 5, dtype=torch.int64, device=DEV),
+                    torch.arange(R, dtype=torch.int64, device=DEV)).cpu().numpy()
+    ref = set(oracle.sampler.topk_set(x.to(torch.float16).double().numpy(), 5).tolist())
+    assert ref == {1234, 0, 1, 2, 3}
+    assert set(tok.tolist()) == ref
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_unaligned_rows_stochastic_match_oracle(dtype):
+    """Rows that cannot be bulk-copied take the generic radix path."""
+    pk = require_gpu()
+    rng = np.random.default_rng(9)
+    R, V = 24, 5001
+    base = torch.from_numpy((rng.standard_normal((R, V + 1)) * 2).astype(np.float32)).to(dtype)
+    logits = base.to(DEV)[:, 1:]
+    T = torch.from_numpy(rng.uniform(0.5, 1.5, R).astype(np.float32))
+    K = torch.from_numpy(rng.choice([0, 7, 40], R).astype(np.int32))
+    P = torch.from_numpy(rng.choice([1.0, 0.9, 0.6], R).astype(np.float32))
+    S = torch.from_numpy(rng.integers(0, 2**62, R, dtype=np.int64))
+    O = torch.from_numpy(rng.integers(0, 2**30, R, dtype=np.int64))
+    tok = pk.sample(logits, T.to(DEV), K.to(DEV), P.to(DEV), S.to(DEV), O.to(DEV)).cpu().numpy()
+    bad = 0
+    for i in range(R):
+        ref, info = oracle.sampler.sample_row(base[i, 1:].double().numpy(), float(T[i]), int(K[i]), float(P[i]),
+                                              int(S[i]), int(O[i]), return_info=True)
+        if int(tok[i]) != ref and not _exempt(info, float(P[i])):
+            bad += 1
+    assert bad == 0

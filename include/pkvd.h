@@ -182,6 +182,31 @@ pkvd_status pkvd_paged_decode_attention_ex(void* out, const void* q, const pkvd_
                                            void* workspace, size_t workspace_bytes,
                                            void* stream, int32_t* err_flag, int32_t path);
 
+/*
+ * pkvd_paged_decode_attention_noalloc -- the same attention as
+ * pkvd_paged_decode_attention (same arguments, results and errors), for
+ * callers that cannot allocate device memory where they call it: code that
+ * runs while a CUDA graph is captured, hosts embedded in a runtime that owns
+ * every device allocation, plain C callers without an allocator.  The pages
+ * describe no such entry point; it exists for those callers only.
+ *
+ * Instead of a caller workspace it uses one 16 MiB scratch array built into
+ * the library (held on every GPU that loads the library until the process
+ * exits).  Shapes whose workspace (pkvd_decode_workspace_bytes) exceeds
+ * 16 MiB are rejected with PKVD_WORKSPACE_TOO_SMALL before anything is
+ * enqueued.  All calls on a GPU share the array: calls that overlap on the
+ * GPU (unordered streams) race and give wrong results.  The first call on
+ * each device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture.
+ * Each call clears the array's counters with an async memset on `stream`.
+ * Nothing is allocated.
+ */
+pkvd_status pkvd_paged_decode_attention_noalloc(void* out, const void* q, const pkvd_cache* cache,
+                                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                                const int32_t* context_lens, int32_t max_context_len,
+                                                int32_t num_seqs, int32_t num_q_heads, float scale,
+                                                void* stream, int32_t* err_flag);
+
 /* Workspace bytes pkvd_sample needs (host only; currently always 0). */
 pkvd_status pkvd_sample_workspace_bytes(int32_t num_rows, int32_t vocab, size_t* bytes);
 

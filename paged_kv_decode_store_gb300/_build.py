@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpkvd.so")
 
-SOURCES = ["api.cu", "store.cu", "attention.cu", "attention_f32.cu", "attention_f16.cu",
+SOURCES = ["api.cu", "api_noalloc.cu", "store.cu", "attention.cu", "attention_f32.cu", "attention_f16.cu",
            "attention_bf16.cu", "sampler.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

@@ -1,0 +1,73 @@
+"""The allocation-free attention entry point.
+
+pkvd_paged_decode_attention_noalloc serves callers that cannot allocate
+device memory where they call (inside graph capture, runtimes that own all
+allocations, plain C hosts): it runs the same attention on a scratch array
+built into the library.  Here it is called through the C ABI and compared,
+on two calls in a row, with the regular entry point that takes a workspace.
+This file is collected last so that a failure here leaves every other test
+already run.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from workloads import configs
+from gpu_helpers import require_gpu, check_attention
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _inputs(cfg):
+    pk = require_gpu()
+    w = workloads.make_workload(cfg)
+    lay = w.layout
+    cache = w.cache.to(DEV)
+    kc, vc = cache[0, lay.layer], cache[1, lay.layer]
+    tables = torch.from_numpy(lay.block_tables).to(DEV)
+    ctx = torch.from_numpy(lay.context_lens).to(DEV)
+    slots = pk.slot_mapping(tables, ctx, cfg.block_size, lay.num_blocks)
+    pk.kv_store(w.k_new.to(DEV), w.v_new.to(DEV), slots, kc, vc)
+    return pk, w, lay, kc, vc, tables, ctx
+
+
+def _call_noalloc(pk, q, kc, vc, tables, ctx, lay, scale, out, err):
+    from paged_kv_decode_store_gb300 import _capi
+    c = _capi.cache_desc(kc, vc)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return pk.lib().pkvd_paged_decode_attention_noalloc(
+        out.data_ptr(), q.data_ptr(), ctypes.byref(c), tables.data_ptr(), tables.shape[1], ctx.data_ptr(),
+        lay.max_context_len, lay.num_seqs, q.shape[1], ctypes.c_float(scale), stream, err.data_ptr())
+
+
+@pytest.mark.parametrize("cfg", [configs.GROK1.scaled(num_seqs=9, ctx_kind="explicit",
+                                                      ctx_args=(700, 1, 0, 333, 2048, 17, 1500, 64, 999),
+                                                      table_kind="perm", vocab=2048),
+                                 configs.NANOCHAT],
+                         ids=["grok1_ragged", "nanochat"])
+def test_noalloc_matches_workspace_entry_point_twice(cfg):
+    pk, w, lay, kc, vc, tables, ctx = _inputs(cfg)
+    q = w.q.to(DEV)
+    for _ in range(2):                             # the scratch keeps the last call's contents
+        ref = pk.paged_decode_attention(q, kc, vc, tables, ctx, lay.max_context_len, w.scale)
+        out = torch.full_like(q, float("nan"))
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        assert _call_noalloc(pk, q, kc, vc, tables, ctx, lay, w.scale, out, err) == 0
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        assert torch.isfinite(out).all()
+        check_attention(out.double().cpu().numpy(), ref.double().cpu().numpy(), q.dtype)
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch():
+    pk, w, lay, kc, vc, tables, ctx = _inputs(configs.GROK1.scaled(num_seqs=2, ctx_args=(64,), vocab=2048))
+    big_seqs = 1 << 20                             # counters alone exceed the built-in scratch
+    from paged_kv_decode_store_gb300 import _capi
+    c = _capi.cache_desc(kc, vc)
+    st = pk.lib().pkvd_paged_decode_attention_noalloc(
+        0, 0, ctypes.byref(c), 0, 1, 0, 64, big_seqs, 48, ctypes.c_float(0.1), None, None)
+    assert st == 4                                 # PKVD_WORKSPACE_TOO_SMALL, nothing enqueued

@@ -59,7 +59,7 @@ class L2Flush:
     def add_(self, _):
         self.wbuf.add_(1)
         torch.sum(self.rbuf, dim=0, out=self.sink)
-KERNELS_PER_STEP = 4            # slot mapping, kv store, attention (fused merge), sampler
+KERNELS_PER_STEP = 5            # slot mapping, kv store, partition, merge, sampler
 
 
 # ----------------------------------------------------------------- bytes
@@ -457,12 +457,12 @@ def main():
         "tokens_per_s": ws * lay.num_seqs / (ms_per_step * 1e-3),
         "step_bytes": nbytes["step"], "attention_bytes": nbytes["attention"],
         "attention_ms": attn_mean, "attention_path": args.path,
-        "roofline": {"kernel": "paged_decode_partition_kernel (LSE merge fused)", "bound": "hbm",
+        "roofline": {"kernel": "paged_decode_attention (partition + LSE merge kernels)", "bound": "hbm",
                      "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
                      "peak_source": peak_src, "traffic": recorded_traffic(cfg.name)},
         "e2e": {"value": ws * nbytes["step"] / (e2e_total / args.steps * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_total / args.steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": KERNELS_PER_STEP * args.steps + args.steps,
+        "gpu_launches": KERNELS_PER_STEP * args.steps + 2 * args.steps,
         "clocks": clocks, "device_err_flag": err,
     }
     if not args.no_cpu_baseline and ws == 1:

@@ -158,11 +158,9 @@ pkvd_status pkvd_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  * Output: out [num_seqs, num_q_heads, head_dim], cache dtype, fp32 softmax
  *         and accumulation.
  * workspace: device scratch of at least pkvd_decode_workspace_bytes(...)
- *         bytes (16-byte aligned): per-(row, head) arrival counters followed
- *         by split-context partial results.  Zero-fill it once before its
- *         first use; every completed call leaves the counters at zero again,
- *         so it can be reused (and captured in a graph) without clearing.
- *         Calls that share a workspace must not overlap on the GPU.
+ *         bytes (16-byte aligned), used for split-context partial results;
+ *         its contents need no initialisation.  Calls that share a
+ *         workspace must not overlap on the GPU.
  * Requirements: num_q_heads % num_kv_heads == 0, group size <= 8,
  *         num_kv_heads <= 8 or == 16.
  */
@@ -198,7 +196,6 @@ pkvd_status pkvd_paged_decode_attention_ex(void* out, const void* q, const pkvd_
  * GPU (unordered streams) race and give wrong results.  The first call on
  * each device looks up the array's device address (cudaGetSymbolAddress)
  * with that device current; make that first call before any stream capture.
- * Each call clears the array's counters with an async memset on `stream`.
  * Nothing is allocated.
  */
 pkvd_status pkvd_paged_decode_attention_noalloc(void* out, const void* q, const pkvd_cache* cache,

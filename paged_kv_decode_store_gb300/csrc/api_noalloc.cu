@@ -69,12 +69,6 @@ pkvd_status pkvd_paged_decode_attention_noalloc(void* out, const void* q, const 
   if (need > kNoAllocScratchBytes) return PKVD_WORKSPACE_TOO_SMALL;   // larger than the built-in scratch
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return PKVD_CUDA_ERROR;
-  // the per-(row, head) arrival counters must start at zero; a completed
-  // call leaves them zeroed, but an earlier call that stopped early may not
-  const size_t counters = ((size_t)num_seqs * num_q_heads * sizeof(int32_t) + 255) / 256 * 256;
-  if (num_seqs > 0 && counters > 0 &&
-      cudaMemsetAsync(scratch, 0, counters, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return PKVD_CUDA_ERROR;
   return pkvd_paged_decode_attention(out, q, cache, block_tables, max_blocks_per_seq, context_lens,
                                      max_context_len, num_seqs, num_q_heads, scale, scratch, need, stream,
                                      err_flag);

@@ -1,4 +1,5 @@
-// Decode-attention launch: grid sizing, workspace layout and path choice.
+// Decode-attention launch: grid sizing, workspace layout, path choice, and
+// the merge kernel that follows the partition kernel.
 #include "attention_dispatch.cuh"
 
 namespace pkvd {
@@ -8,9 +9,7 @@ constexpr int kMaxDynSmem = 232448;    // 227 KB opt-in per CTA on sm_100-family
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-size_t counter_bytes(int num_seqs, int num_q_heads) {
-  return align_up(sizeof(int32_t) * (size_t)num_seqs * num_q_heads, 256);
-}
+size_t prefix_bytes(int num_seqs) { return align_up(sizeof(int32_t) * ((size_t)num_seqs + 1), 256); }
 
 int elem_bytes(int dtype) { return dtype == PKVD_F32 ? 4 : 2; }
 
@@ -29,11 +28,11 @@ int attention_grid(int num_seqs, int max_context_len, int sm_count) {
   if (num_seqs <= 0 || max_context_len <= 0 || sm_count <= 0) return 0;
   const long long units = (long long)num_seqs * ((max_context_len + kChunk - 1) / kChunk);
   long long g = units < sm_count ? units : sm_count;
-  return (int)g;
+  return (int)(g < kMaxMergeRecords ? g : kMaxMergeRecords);
 }
 
 size_t attention_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int grid) {
-  return counter_bytes(num_seqs, num_q_heads) + (size_t)grid * 2 * num_q_heads * (head_dim + 4) * sizeof(float);
+  return prefix_bytes(num_seqs) + (size_t)grid * 2 * num_q_heads * (head_dim + 4) * sizeof(float);
 }
 
 bool attention_path_supported(int path, int dtype, int head_dim, int num_kv_heads, int group) {
@@ -55,8 +54,8 @@ int attention_default_path(int dtype, int head_dim, int num_kv_heads, int group)
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   const int esz = elem_bytes(a.dtype);
   const int G = a.num_q_heads / a.num_kv_heads;
-  int32_t* counters = static_cast<int32_t*>(a.workspace);
-  float* rec = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + counter_bytes(a.num_seqs, a.num_q_heads));
+  int32_t* prefix = static_cast<int32_t*>(a.workspace);
+  float* rec = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + prefix_bytes(a.num_seqs));
   if (a.grid > 0) {
     PartParams pp;
     pp.out = a.out;
@@ -79,7 +78,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
     pp.num_seqs = a.num_seqs;
     pp.scale_log2 = a.scale * 1.4426950408889634f;
     pp.rec = rec;
-    pp.counters = counters;
+    pp.prefix = prefix;
     pp.err = a.err;
     pp.stages = stage_count(a.dtype, a.head_dim, a.num_kv_heads);
     pp.row_bytes = a.num_kv_heads * a.head_dim * esz;
@@ -95,10 +94,30 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
     else e = partition_bf16(pp, a.head_dim, hpw, gmax, a.path, a.grid, smem, stream);
     if (e != cudaSuccess) return e;
   }
-  if (a.grid == 0 && a.num_seqs > 0) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  if (a.grid == 0) {
     // no context anywhere: every output row is zero
     return cudaMemsetAsync(a.out, 0, (size_t)a.num_seqs * a.num_q_heads * a.head_dim * esz, stream);
   }
+  // the merge kernel as a programmatic dependent of the partition kernel
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.num_seqs);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (a.dtype == PKVD_F32)
+    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<float>, static_cast<float*>(a.out), (const float*)rec,
+                              (const int32_t*)prefix, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
+  if (a.dtype == PKVD_F16)
+    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<__half>, static_cast<__half*>(a.out), (const float*)rec,
+                              (const int32_t*)prefix, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
+  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<__nv_bfloat16>, static_cast<__nv_bfloat16*>(a.out),
+                            (const float*)rec, (const int32_t*)prefix, a.num_seqs, a.num_q_heads, a.head_dim,
+                            a.grid);
   return cudaSuccess;
 }
 

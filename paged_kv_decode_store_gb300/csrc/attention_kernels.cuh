@@ -1,4 +1,4 @@
-// Paged single-query GQA decode attention: partition kernel with a fused LSE merge.
+// Paged single-query GQA decode attention: partition kernel + LSE merge.
 //
 // What is computed (nano-vllm "Model Runner" notes, sections "prefill and
 // decode" and "allocated kv cache"; Grok-1 "第 8 章 runners.py 推理引擎",
@@ -12,11 +12,10 @@
 //   slice of that list (stream-K style), so every SM moves the same number
 //   of K/V bytes whatever the length mix.  A slice may start or end inside
 //   a sequence; such partial segments leave an unnormalised (m, l, acc)
-//   record in the workspace and count themselves in on a per-(row, kv head)
-//   counter; the warp that arrives last combines the row's records with the
-//   log-sum-exp identity (no waiting: nobody spins on anybody) and resets
-//   the counter.  Segments wholly inside one CTA are normalised and written
-//   directly.
+//   record in the workspace and the merge kernel, launched as a
+//   programmatic dependent so its launch overlaps this kernel's tail,
+//   combines them with the log-sum-exp identity.  Segments wholly inside one
+//   CTA are normalised and written directly.
 // * One producer warp walks the slice, looks block ids up (32 table entries
 //   per coalesced load, shuffled to the lane that needs them) and issues
 //   cp.async.bulk (TMA engine) copies of each chunk's K and V token rows --
@@ -61,7 +60,7 @@ struct PartParams {
   int num_seqs;
   float scale_log2;
   float* rec;          // partial records [grid][2][hq][D + 4]: acc[D], m, l, pad
-  int32_t* counters;   // [num_seqs][hq] arrivals per (row, kv head); zero between launches
+  int32_t* prefix;     // [num_seqs + 1] chunk prefix sums (written by CTA 0)
   int32_t* err;
   int stages;
   int rowb;            // padded smem bytes of one token row (all heads)
@@ -113,84 +112,6 @@ struct SmemHdr {
   long long total;
   int abort_flag;
 };
-
-// A warp has written its partial record for (row, kv head hk).  It counts
-// itself in; the warp that arrives last (no waiting anywhere) folds every
-// record of the row with the log-sum-exp identity, writes the G output rows
-// of the group and resets the counter for the next launch.
-//   M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  o = sum_s 2^(m_s - M) acc_s / L
-template <typename T, int D>
-__device__ __forceinline__ void row_partial_done(const PartParams& p, int seq, int hk, long long P, long long n,
-                                                 long long C, int grid, int lane) {
-  __threadfence();
-  __syncwarp();
-  const int a = (int)(((P + 1) * grid - 1) / C);
-  const int b = (int)(((P + n) * grid - 1) / C);
-  // CTA a's slice starts at or before P; every later CTA up to b starts inside
-  // the row.  With C >= grid every slice is non-empty, so all of a..b
-  // contribute; otherwise empty slices are skipped.
-  const bool a_at_start = (C * a) / grid == P;
-  int contributors = b - a + 1;
-  if (C < grid) {
-    contributors = 0;
-    for (int c0 = a; c0 <= b; c0 += 32) {
-      const int c = c0 + lane;
-      bool nonempty = false;
-      if (c <= b) nonempty = (C * c) / grid < (C * (c + 1)) / grid;
-      contributors += __popc(__ballot_sync(FULL_MASK, nonempty));
-    }
-  }
-  int old = 0;
-  int32_t* ctr = p.counters + (int64_t)seq * p.hq + hk;
-  if (lane == 0) old = atomicAdd(ctr, 1);
-  old = __shfl_sync(FULL_MASK, old, 0);
-  if (old != contributors - 1) return;
-  __threadfence();
-  constexpr int Q = D / 4;
-  const int total = p.G * Q;                         // float4 outputs of the group
-  for (int base = 0; base < total; base += 32) {     // warp-uniform loops: shuffles below
-    const int idx = base + lane;
-    const bool act = idx < total;
-    const int g = act ? idx / Q : 0, d4 = act ? (idx % Q) * 4 : 0;
-    const int h = hk * p.G + g;
-    float M = -INFINITY, L = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int w0 = a; w0 <= b; w0 += 32) {
-      const int c = w0 + lane;                       // one contributing CTA per lane
-      int rid = -1;
-      if (c <= b) {
-        const bool nonempty = C >= grid || (C * c) / grid < (C * (c + 1)) / grid;
-        if (nonempty) rid = c * 2 + ((c == a && !a_at_start) ? 1 : 0);
-      }
-      const int nwin = min(32, b - w0 + 1);
-      for (int k = 0; k < nwin; ++k) {
-        const int r_id = __shfl_sync(FULL_MASK, rid, k);
-        if (r_id < 0 || !act) continue;
-        const float* r = p.rec + ((int64_t)r_id * p.hq + h) * (D + 4);
-        const float m = __ldcg(r + D), l = __ldcg(r + D + 1);
-        const float4 acc = __ldcg(reinterpret_cast<const float4*>(r + d4));
-        const float Mn = fmaxf(M, m);
-        const float cs = (M == -INFINITY) ? 0.f : exp2f(M - Mn);
-        const float cr = (m == -INFINITY) ? 0.f : exp2f(m - Mn);
-        L = L * cs + l * cr;
-        o.x = o.x * cs + acc.x * cr;
-        o.y = o.y * cs + acc.y * cr;
-        o.z = o.z * cs + acc.z * cr;
-        o.w = o.w * cs + acc.w * cr;
-        M = Mn;
-      }
-    }
-    if (act) {
-      const float inv = 1.f / L;
-      T* dst = static_cast<T*>(p.out) + ((int64_t)seq * p.hq + h) * D + d4;
-      dst[0] = DT<T>::from_f(o.x * inv);
-      dst[1] = DT<T>::from_f(o.y * inv);
-      dst[2] = DT<T>::from_f(o.z * inv);
-      dst[3] = DT<T>::from_f(o.w * inv);
-    }
-  }
-  if (lane == 0) *ctr = 0;
-}
 
 // ----------------------------------------------------------- consumers
 template <typename T, int D, int HPW, int GMAX>
@@ -321,7 +242,6 @@ struct FmaConsumer {
           }
         }
       }
-      if (!(flags & F_COMPLETE)) row_partial_done<T, D>(p, seq, hk, P, nrow, C, grid, lane);
     }
   }
 };
@@ -473,7 +393,6 @@ struct MmaConsumer {
           if (gA < p.G) { rb[gA * (D + 4) + D] = m[j][0]; rb[gA * (D + 4) + D + 1] = lA; }
           if (gB < p.G) { rb[gB * (D + 4) + D] = m[j][1]; rb[gB * (D + 4) + D + 1] = lB; }
         }
-        row_partial_done<T, D>(p, seq, hk, P, nrow, C, grid, lane);
       }
     }
   }
@@ -517,13 +436,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
       const int incl = block_incl_scan(n, hdr.scan_warp, total);
       const int excl = running + incl - n;
       if (cta == 0 && i < p.num_seqs) {
+        p.prefix[i] = excl;
         const int raw = p.ctx[i];
         if (raw < 0 || raw > p.ctx_cap) flag_error(p.err, PKVD_ERR_CONTEXT);
-        if (n == 0) {
-          // an empty context attends to nothing: its output rows are zero
-          uint4* o = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + (int64_t)i * p.hq * D);
-          for (int v = 0; v < p.hq * D * (int)sizeof(T) / 16; ++v) o[v] = make_uint4(0, 0, 0, 0);
-        }
       }
       if (i < p.num_seqs && n > 0 && excl <= c0 && c0 < excl + n) {
         hdr.found_seq = i;
@@ -533,7 +448,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
       __syncthreads();
       if (cta != 0 && hdr.found_seq >= 0) break;
     }
+    if (cta == 0 && tid == 0) p.prefix[p.num_seqs] = (int)C;
   }
+  // the merge kernel may be scheduled now; it waits for this grid to finish
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (c0 >= c1) return;
 
   if (tid == 0) {
@@ -656,6 +574,94 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
     __syncwarp();
     if (lane == 0) mbar_arrive(&hdr.empty[stage]);
     if (flags & F_LAST) cons.finish(p, seq, flags, cta, warp, lane, row_start, nrow, C, grid);
+  }
+}
+
+// ------------------------------------------------------------ merge
+// One CTA per row, launched as a programmatic dependent of the partition
+// kernel: it waits for that grid, then combines the partial records of the
+// CTAs whose slices cut the row (log-sum-exp identity), writes zeros for an
+// empty context, and leaves rows one CTA finished on its own untouched.
+//   M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  o = sum_s 2^(m_s - M) acc_s / L
+// Each thread owns float4 output slices; for every chunk of 8 records all
+// loads are issued before any is used (one L2 round trip per chunk).
+constexpr int kMaxMergeRecords = 1024;     // >= any partition grid (one CTA per SM)
+
+template <typename T>
+__global__ void __launch_bounds__(256) lse_merge_kernel(T* __restrict__ out, const float* __restrict__ rec,
+                                                        const int32_t* __restrict__ prefix, int num_seqs,
+                                                        int hq, int D, int grid) {
+  __shared__ int s_rec[kMaxMergeRecords];
+  __shared__ int s_n;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int i = blockIdx.x;
+  T* orow = out + (int64_t)i * hq * D;
+  const long long C = prefix[num_seqs];
+  const long long P = prefix[i];
+  const long long n = prefix[i + 1] - P;
+  if (n <= 0) {
+    for (int idx = threadIdx.x; idx < hq * D; idx += blockDim.x) orow[idx] = DT<T>::from_f(0.f);
+    return;
+  }
+  const int a = (int)(((P + 1) * grid - 1) / C);
+  const int b = (int)(((P + n) * grid - 1) / C);
+  if (a == b) return;
+  if (threadIdx.x == 0) {
+    // CTA a's slice starts at or before P (its record of this row is its
+    // last segment unless it starts exactly at P); later CTAs start inside
+    // the row.  Empty slices (only when C < grid) are skipped.
+    const bool a_at_start = (C * a) / grid == P;
+    int cnt = 0;
+    for (int c = a; c <= b && cnt < kMaxMergeRecords; ++c) {
+      if (C < grid && (C * c) / grid >= (C * (c + 1)) / grid) continue;
+      s_rec[cnt++] = c * 2 + ((c == a && !a_at_start) ? 1 : 0);
+    }
+    s_n = cnt;
+  }
+  __syncthreads();
+  const int nrec = s_n;
+  const int Q = D / 4;
+  constexpr int R = 8;
+  for (int idx = threadIdx.x; idx < hq * Q; idx += blockDim.x) {
+    const int h = idx / Q, d4 = (idx % Q) * 4;
+    float M = -INFINITY, L = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = 0; k0 < nrec; k0 += R) {
+      float mk[R], lk[R];
+      float4 ak[R];
+#pragma unroll
+      for (int e = 0; e < R; ++e) {
+        mk[e] = -INFINITY;
+        lk[e] = 0.f;
+        ak[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k0 + e < nrec) {
+          const float* r = rec + ((int64_t)s_rec[k0 + e] * hq + h) * (D + 4);
+          mk[e] = r[D];
+          lk[e] = r[D + 1];
+          ak[e] = *reinterpret_cast<const float4*>(r + d4);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < R; ++e) {
+        const float m = mk[e];
+        if (m == -INFINITY) continue;
+        const float Mn = fmaxf(M, m);
+        const float cs = (M == -INFINITY) ? 0.f : exp2f(M - Mn);
+        const float cr = exp2f(m - Mn);
+        L = L * cs + lk[e] * cr;
+        o.x = o.x * cs + ak[e].x * cr;
+        o.y = o.y * cs + ak[e].y * cr;
+        o.z = o.z * cs + ak[e].z * cr;
+        o.w = o.w * cs + ak[e].w * cr;
+        M = Mn;
+      }
+    }
+    const float inv = 1.f / L;
+    T* dst = orow + h * D + d4;
+    dst[0] = DT<T>::from_f(o.x * inv);
+    dst[1] = DT<T>::from_f(o.y * inv);
+    dst[2] = DT<T>::from_f(o.z * inv);
+    dst[3] = DT<T>::from_f(o.w * inv);
   }
 }
 

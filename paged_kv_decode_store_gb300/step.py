@@ -9,7 +9,7 @@ device buffer owned by this object; a step is: write the inputs into those
 buffers, replay.
 
 Step order (all library kernels):
-    slot_mapping -> kv_store -> paged_decode_attention (partition, fused merge) -> sample
+    slot_mapping -> kv_store -> paged_decode_attention (partition + merge) -> sample
 """
 from __future__ import annotations
 
@@ -55,7 +55,7 @@ class DecodeStep:
         self.workspace = torch.zeros(max(int(nbytes.value), 16), dtype=torch.uint8, device=dev)
         self.cache = _capi.cache_desc(k_cache, v_cache)
         self.graph = None
-        self.kernels_per_step = 4     # slot, store, attention (partition + fused merge), sample
+        self.kernels_per_step = 5     # slot, store, partition, merge, sample
 
     def enqueue(self, stream=None) -> None:
         L = _capi.lib()

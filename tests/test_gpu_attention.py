@@ -139,9 +139,8 @@ def test_full_size_sampled_rows(name):
         assert float(rel.max()) <= 2 * 2e-2
 
 
-def test_workspace_is_left_zeroed_and_reusable():
-    """The fused merge's arrival counters return to zero after every call, so
-    one workspace serves repeated calls (and graph replays) unchanged."""
+def test_workspace_is_reusable_without_clearing():
+    """One workspace, never cleared, serves repeated calls unchanged."""
     pk = require_gpu()
     cfg = configs.GROK1.scaled(num_seqs=7, ctx_kind="explicit", ctx_args=(700, 1, 0, 333, 2048, 17, 1500),
                                table_kind="perm", vocab=2048)
@@ -153,12 +152,10 @@ def test_workspace_is_left_zeroed_and_reusable():
     slots = pk.slot_mapping(tables, ctx, cfg.block_size, lay.num_blocks)
     pk.kv_store(w.k_new.to(DEV), w.v_new.to(DEV), slots, cache[0, 0], cache[1, 0])
     nbytes = pk.decode_workspace_bytes(lay.num_seqs, cfg.num_q_heads, cfg.head_dim, lay.max_context_len)
-    ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device=DEV)      # garbage on purpose
     outs = [pk.paged_decode_attention(w.q.to(DEV), cache[0, 0], cache[1, 0], tables, ctx, lay.max_context_len,
                                       w.scale, workspace=ws) for _ in range(3)]
     torch.cuda.synchronize()
     assert torch.isfinite(outs[0]).all()
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
-    counters = ws[: lay.num_seqs * cfg.num_q_heads * 4].view(torch.int32)
-    assert int(counters.abs().sum()) == 0
     assert torch.all(outs[0][2] == 0)                     # the empty row

@@ -444,6 +444,29 @@ constexpr int region_bytes() {
 
 // Order-preserving keys of the two 16-bit floats of a word, in one go:
 // -0 is first folded onto +0, then key = b ^ 0xffff (negative) or b ^ 0x8000.
+// Two 16-bit floats of one 32-bit word, as the packed type of T.
+template <typename T> struct Pack2;
+template <> struct Pack2<__half> {
+  using T2 = __half2;
+  static constexpr uint32_t kNegInf2 = 0xfc00fc00u;
+  __device__ static float2 to_float2(uint32_t w) { return __half22float2(*reinterpret_cast<const __half2*>(&w)); }
+};
+template <> struct Pack2<__nv_bfloat16> {
+  using T2 = __nv_bfloat162;
+  static constexpr uint32_t kNegInf2 = 0xff80ff80u;
+  __device__ static float2 to_float2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
+};
+template <typename T>
+__device__ __forceinline__ typename Pack2<T>::T2 as_t2(uint32_t w) {
+  return *reinterpret_cast<const typename Pack2<T>::T2*>(&w);
+}
+template <typename T>
+__device__ __forceinline__ uint32_t t2_bits(typename Pack2<T>::T2 v) {
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 __device__ __forceinline__ uint32_t keys2(uint32_t w) {
   const uint32_t nz = ((w & 0x7fff7fffu) + 0x7fff7fffu) & 0x80008000u;   // magnitude != 0, per half
   w &= nz | 0x7fff7fffu;
@@ -513,17 +536,16 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
       const int rest = nvec * 8;
       auto bits_at = [&](int j) -> uint32_t { return (uint32_t)(*reinterpret_cast<const unsigned short*>(src + j)); };
 
-      // ---- F1. row max key
-      uint32_t mx = 0;
+      // ---- F1. row max key: packed max of the values (one instruction per
+      // two logits), keyed once at the end
+      using T2 = typename Pack2<T>::T2;
+      T2 mx2 = as_t2<T>(Pack2<T>::kNegInf2);
       for (int v = tid; v < nvec; v += kSampThreads) {
         const uint4 u = sv[v];
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t k2 = keys2(w[q]);
-          mx = max(mx, max(k2 & 0xffffu, k2 >> 16));
-        }
+        mx2 = __hmax2(mx2, __hmax2(__hmax2(as_t2<T>(u.x), as_t2<T>(u.y)), __hmax2(as_t2<T>(u.z), as_t2<T>(u.w))));
       }
+      const uint32_t mw = t2_bits<T>(mx2);
+      uint32_t mx = max(K::key(mw & 0xffffu), K::key(mw >> 16));
       for (int j = rest + tid; j < n; j += kSampThreads) mx = max(mx, K::key(bits_at(j)));
       const uint32_t kmax = (uint32_t)cluster_scalar<true>(c, block_max_u64(mx, h.red), 0);
       const float Tr = a.temperature[row_id];
@@ -577,17 +599,22 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
           zs = t;
         };
         auto wexp = [&](uint32_t b) { return exp2f((K::value(b) - m) * l2t); };
+        const float ml2t = m * l2t;
         for (int v = tid; v < nvec; v += kSampThreads) {
           const uint4 u = sv[v];
           const uint32_t w[4] = {u.x, u.y, u.z, u.w};
           float vs = 0.f;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const uint32_t d2 = __vsub2(kmax2, keys2(w[q]));
+            // per-half kmax - key: no borrow crosses the halves, as every key <= kmax
+            const uint32_t d2 = kmax2 - keys2(w[q]);
             const uint32_t dlo = d2 & 0xffffu, dhi = d2 >> 16;
             if (dlo < (uint32_t)kWinTop) atomicAdd(&win[dlo], 1u);
             if (dhi < (uint32_t)kWinTop) atomicAdd(&win[dhi], 1u);
-            if (need_z) vs += wexp(w[q] & 0xffffu) + wexp(w[q] >> 16);
+            if (need_z) {
+              const float2 f = Pack2<T>::to_float2(w[q]);
+              vs += exp2f(fmaf(f.x, l2t, -ml2t)) + exp2f(fmaf(f.y, l2t, -ml2t));
+            }
           }
           if (need_z) zadd(vs);
         }
@@ -826,7 +853,6 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
         const uint32_t kp = K::key((uint32_t)(*reinterpret_cast<const unsigned short*>(&tv)));
         if (!isinf(vmin) && kp > thr) thr = kp;
       }
-      const uint32_t thr2 = thr | (thr << 16);
       const uint64_t seed = a.seeds[row_id], off = a.offsets[row_id];
       const float invT = 1.f / Tr;
       auto keep = [&](int j, uint32_t b) -> bool {
@@ -852,13 +878,18 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
         if (mine < kSlots) slot[mine * kSampThreads + tid] = (uint32_t)j;
         ++mine;
       };
+      // value of the threshold key (or -inf when every id passes): a packed
+      // compare of the values is the same test as comparing keys
+      uint32_t tb = thr == 0 ? (Pack2<T>::kNegInf2 & 0xffffu)
+                             : ((thr & 0x8000u) ? (thr & 0x7fffu) : (~thr & 0xffffu));
+      const T2 thr_v2 = as_t2<T>(tb | (tb << 16));
       for (int v = tid; v < nvec; v += kSampThreads) {
         const uint4 u = sv[v];
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
         uint32_t cb = 0;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint32_t ge = __vcmpgeu2(keys2(w[q]), thr2);
+          const uint32_t ge = __hge2_mask(as_t2<T>(w[q]), thr_v2);
           cb |= ((ge & 1u) | ((ge >> 15) & 2u)) << (2 * q);
         }
         while (cb) {

@@ -22,14 +22,16 @@
 //   exact per-key counts in a window of keys below the max give each key's
 //   probability mass as count * w(key), w in 2^-40 fixed point; ids below
 //   the window only enter the normaliser, through an f32 sum in fixed order.
-//   Top-k and the nucleus cut are found by a two-level scan of that window
-//   (256 groups, then the bins of one group).  fp32 logits, and cuts that
-//   fall below the window, use an MSB-first radix select with cluster-summed
-//   histograms instead.
+//   Top-k and the nucleus cut are found by walking that window down from
+//   the max, 2048 bins per step; the window is counted in two stages (the
+//   first 2048 keys, then the rest only when a cut lies deeper).  fp32
+//   logits, and cuts that fall below the window, use an MSB-first radix
+//   select with cluster-summed histograms instead.
 // * Gumbel pass: only ids that can win are considered (x'_j >= max x' - 21,
-//   since u lies in [2^-24, 1 - 2^-24] and g in [-2.81, 16.64]); candidates
-//   are compacted into per-warp queues so Philox and the logarithms run on
-//   full warps.
+//   since u lies in [2^-24, 1 - 2^-24] and g in [-2.81, 16.64]).  For 16-bit
+//   logits the candidates are compacted in index order into one list per CTA
+//   and scored evenly by all threads; the generic path queues them per warp.
+//   Either way Philox and the logarithms run on full warps.
 // * Ties at the k-th key straddling the cut: slices are ordered by index, so
 //   each CTA takes its share of the lowest-index ties and resolves it with a
 //   local radix select over its tie indices.
@@ -47,11 +49,17 @@ constexpr float kGumbelSpan = 21.0f;
 constexpr int kMaxCluster = 8;
 constexpr int kMaxChunks = 16;
 constexpr int kChunkBytes = 16384;
+static_assert(kChunkBytes / 16 == kSampThreads, "one 16-byte word per thread and chunk");
 constexpr int kQueue = 64;                 // per-warp candidate ring
 
 // Exact per-key counts are kept for the kWinTop keys below the row max
 // (16-bit logits: 8 binades for fp16, 64 for bf16).
 constexpr int kWinTop = 8192;                   // exact counts of the top keys below the max
+constexpr int kWinBlock = 2048;                 // bins per walk step (two per thread)
+// First counting stage: the keys of the two binades below the max (fp16 has
+// 1024 keys per binade, bf16 128).
+template <typename T>
+constexpr int win1_bins() { return std::is_same<T, __half>::value ? 2048 : 256; }
 
 template <typename T> struct Keys;
 template <> struct Keys<float> {
@@ -137,30 +145,41 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
   return c;
 }
 
-__device__ __forceinline__ float gumbel_noise(uint64_t seed, uint64_t offset, uint32_t j) {
+// E_j = -ln u_j for id j's uniform: word (j mod 4) of Philox4x32-10 at
+// counter (j / 4, offset), u = ((w >> 9) + 1/2) 2^-23, exact in f32 and
+// strictly inside (0, 1), so E_j > 0 (accurate near u = 1, where it is tiny)
+__device__ __forceinline__ float exp_noise(uint64_t seed, uint64_t offset, uint32_t j) {
   const uint4 ctr = make_uint4(j >> 2, (uint32_t)offset, (uint32_t)(offset >> 32), 0u);
   const uint4 w4 = philox4x32_10(ctr, make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
   const uint32_t sel = j & 3u;
   const uint32_t w = sel == 0 ? w4.x : (sel == 1 ? w4.y : (sel == 2 ? w4.z : w4.w));
   const float u = (__uint2float_rn(w >> 9) + 0.5f) * 1.1920928955078125e-07f;   // * 2^-23, exact
-  return -logf(-logf(u));
+  return -logf(u);
+}
+
+// Gumbel-max as an exponential race: argmax_j x_j / T - ln(-ln u_j) is
+// argmin_j E_j exp((m - x_j) / T) for any m; with m the row max (or a bound
+// above every x_j of the slice) the factor lies in [1, 2^31) for every id
+// that can win.  The packed key makes the smallest race time the largest
+// key, and the lowest id the winner among equal times.  d2 = (m - x) / (T ln 2).
+__device__ __forceinline__ unsigned long long race_key(uint64_t seed, uint64_t offset, uint32_t j, float d2) {
+  const float t = exp_noise(seed, offset, j) * exp2f(d2);
+  return ((unsigned long long)(uint32_t)~f32_order_key(t) << 32) | (0xffffffffu - j);
 }
 
 // ------------------------------------------------------------ shared state
 struct SampHdr {
+  ulonglong2 px[2][kMaxCluster];          // pushed cluster exchanges (alternating)
   uint64_t bar[kMaxChunks];
+  int gap[kMaxCluster];                  // row max key - each rank's max key
   unsigned long long ex_arr[2][256];     // cluster-exchanged arrays (alternating)
-  unsigned long long xr[kMaxCluster];    // per-rank values of the last scalar exchange
-  unsigned long long ex_sc[2][4];        // cluster-exchanged scalars (alternating)
   unsigned long long tot[256];           // row-wide totals of the last exchange
   unsigned long long red[kSampWarps];
-  float redf[kSampWarps];
   int sel_bin;
   unsigned long long sel_before;
   int sel_aux;
   unsigned long long sel_val;
   unsigned long long zsum;
-  int cand_n;
 };
 
 struct Ctx {
@@ -169,21 +188,32 @@ struct Ctx {
   int ex;        // next exchange slot
 };
 
-// Max or sum of a per-CTA u64 over the cluster, in rank order.  Exchange
-// slots alternate, so one cluster barrier per exchange is enough: a slot is
-// rewritten only after every peer passed the next barrier.
-template <bool MAX>
-__device__ __forceinline__ unsigned long long cluster_scalar(Ctx& c, unsigned long long v, int which) {
+// Cluster exchange of two u64 per CTA: threads 0..cs-1 store this CTA's
+// pair into slot [rank] of every CTA's table (its own included), then one
+// cluster barrier; afterwards every rank's pair is in local shared memory
+// and no CTA reads a peer after the barrier.  Consecutive exchanges use
+// alternate tables: a peer can only write a table again after the next
+// barrier, which every reader of the previous values has reached.
+// v0 and v1 must be uniform over the block.
+__device__ __forceinline__ const ulonglong2* cluster_push(Ctx& c, uint32_t crank, unsigned long long v0,
+                                                          unsigned long long v1) {
   const int s = c.ex;
   c.ex ^= 1;
-  if (threadIdx.x == 0) c.h->ex_sc[s][which] = v;
+  if (threadIdx.x < (unsigned)c.cs) {
+    const uint32_t addr = dsmem_addr(&c.h->px[s][crank], threadIdx.x);
+    asm volatile("st.shared::cluster.v2.u64 [%0], {%1, %2};" ::"r"(addr), "l"(v0), "l"(v1) : "memory");
+  }
   cluster_sync();
-  // one thread per rank fetches that rank's value (the remote loads overlap)
-  if (threadIdx.x < (unsigned)c.cs) c.h->xr[threadIdx.x] = dsmem_ld_u64(dsmem_addr(&c.h->ex_sc[s][which], threadIdx.x));
-  __syncthreads();
+  return c.h->px[s];
+}
+
+// Max or sum of a block-uniform u64 over the cluster, in rank order.
+template <bool MAX>
+__device__ __forceinline__ unsigned long long cluster_scalar(Ctx& c, unsigned long long v) {
+  const ulonglong2* px = cluster_push(c, cluster_rank(), v, 0ull);
   unsigned long long acc = 0;
   for (int r = 0; r < c.cs; ++r) {
-    const unsigned long long x = c.h->xr[r];
+    const unsigned long long x = px[r].x;
     acc = MAX ? (x > acc ? x : acc) : acc + x;
   }
   return acc;
@@ -203,6 +233,10 @@ __device__ __forceinline__ void cluster_sum_array(Ctx& c) {
   __syncthreads();
 }
 
+// Block-wide max / sum / exclusive scan of a u64 per thread.  Warp partials
+// go through s[0..32); every warp then reduces the 32 partials with
+// shuffles, so two barriers suffice.  The first barrier also protects s[]
+// from the previous user; none of these ends with a barrier.
 __device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v, unsigned long long* s) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -213,8 +247,12 @@ __device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v
   __syncthreads();
   if (lane == 0) s[warp] = v;
   __syncthreads();
-  v = s[0];
-  for (int w = 1; w < kSampWarps; ++w) v = s[w] > v ? s[w] : v;
+  v = s[lane];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long t = __shfl_xor_sync(FULL_MASK, v, o);
+    v = t > v ? t : v;
+  }
   return v;
 }
 
@@ -225,12 +263,12 @@ __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v
   __syncthreads();
   if (lane == 0) s[warp] = v;
   __syncthreads();
-  unsigned long long t = 0;
-  for (int w = 0; w < kSampWarps; ++w) t += s[w];
-  return t;
+  v = s[lane];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL_MASK, v, o);
+  return v;
 }
 
-// Exclusive scan over threads of a u64 (thread order); ends with __syncthreads.
 __device__ __forceinline__ unsigned long long block_excl_scan_u64(unsigned long long v, unsigned long long* s,
                                                                   unsigned long long& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -243,28 +281,16 @@ __device__ __forceinline__ unsigned long long block_excl_scan_u64(unsigned long 
   __syncthreads();
   if (lane == 31) s[warp] = incl;
   __syncthreads();
-  unsigned long long base = 0, tot = 0;
-  for (int w = 0; w < kSampWarps; ++w) {
-    const unsigned long long x = s[w];
-    if (w < warp) base += x;
-    tot += x;
-  }
-  total = tot;
-  __syncthreads();
-  return base + incl - v;
-}
-
-// Sum of one float per thread in a fixed order (same result every run).
-__device__ __forceinline__ float block_sum_f32(float v, float* s) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned long long x = s[lane];
+  unsigned long long xin = x;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL_MASK, v, o);
-  __syncthreads();
-  if (lane == 0) s[warp] = v;
-  __syncthreads();
-  float t = 0.f;
-  for (int w = 0; w < kSampWarps; ++w) t += s[w];
-  return t;
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(FULL_MASK, xin, o);
+    if (lane >= o) xin += t;
+  }
+  total = __shfl_sync(FULL_MASK, xin, 31);
+  const unsigned long long wbase = __shfl_sync(FULL_MASK, xin - x, warp);
+  return wbase + incl - v;
 }
 
 // Warp 0 walks tot[] (descending bin order if DESC) and finds the first bin
@@ -419,7 +445,8 @@ __device__ __forceinline__ void visit(const T* src, int n, bool vec, F&& f) {
 }
 
 struct SampArgs {
-  int fast;             // 16-bit keys, resident slice of <= 65535 ids: windowed path
+  int fast;             // 16-bit keys, resident slice: windowed path
+  int list_cap;         // fast path: list entries after the first window's bins
   int32_t* token_ids;
   const void* logits;
   int V;
@@ -474,6 +501,51 @@ __device__ __forceinline__ uint32_t keys2(uint32_t w) {
   return w ^ ((s * 0x7fffu) | 0x80008000u);
 }
 
+// Eight bits, one per logit of a 16-byte word of 16-bit floats (bit e for
+// logit e), set where the value is >= the threshold value held in both
+// halves of t.  A value compare is the same test as a key compare.
+template <typename T>
+__device__ __forceinline__ uint32_t pass_bits(const uint4 u, const typename Pack2<T>::T2 t) {
+  const uint32_t g0 = __hge2_mask(as_t2<T>(u.x), t), g1 = __hge2_mask(as_t2<T>(u.y), t);
+  const uint32_t g2 = __hge2_mask(as_t2<T>(u.z), t), g3 = __hge2_mask(as_t2<T>(u.w), t);
+  const uint32_t lo4 = (g0 & 0x00010001u) | ((g1 & 0x00010001u) << 2) | ((g2 & 0x00010001u) << 4) |
+                       ((g3 & 0x00010001u) << 6);
+  // bits 0,2,4,6 hold the low halves, bits 16,18,20,22 the high halves
+  return (lo4 & 0x55u) | ((lo4 >> 15) & 0xaau);
+}
+
+// Threshold value of a 16-bit key, in both halves of a word (-inf for key 0,
+// which every value reaches).
+template <typename T>
+__device__ __forceinline__ typename Pack2<T>::T2 key_threshold2(uint32_t key) {
+  const uint32_t tb = key == 0 ? (Pack2<T>::kNegInf2 & 0xffffu) : ((key & 0x8000u) ? (key & 0x7fffu) : (~key & 0xffffu));
+  return as_t2<T>(tb | (tb << 16));
+}
+
+// Add one to win[d] for every id of a resident 16-bit slice whose key lies
+// at distance d in [d_lo, d_lo + width) below kmax (every key <= kmax).
+template <typename T>
+__device__ __forceinline__ void count_bins16(const uint4* sv, int nvec, int rest, int n, const T* slice,
+                                             uint32_t kmax, uint32_t* win, uint32_t d_lo, uint32_t width) {
+  const uint32_t kmax2 = kmax | (kmax << 16);
+  for (int v = threadIdx.x; v < nvec; v += kSampThreads) {
+    const uint4 u = sv[v];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      // per-half kmax - key: no borrow crosses the halves, as every key <= kmax
+      const uint32_t d2 = kmax2 - keys2(w[q]);
+      const uint32_t dl = (d2 & 0xffffu) - d_lo, dh = (d2 >> 16) - d_lo;
+      if (dl < width) atomicAdd(&win[d_lo + dl], 1u);
+      if (dh < width) atomicAdd(&win[d_lo + dh], 1u);
+    }
+  }
+  for (int j = rest + threadIdx.x; j < n; j += kSampThreads) {
+    const uint32_t d = kmax - Keys<T>::key((uint32_t)(*reinterpret_cast<const unsigned short*>(slice + j))) - d_lo;
+    if (d < width) atomicAdd(&win[d_lo + d], 1u);
+  }
+}
+
 
 
 template <typename T>
@@ -483,10 +555,11 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
   constexpr int KB = K::BITS;
   constexpr int E = 16 / sizeof(T);
   SampHdr& h = *reinterpret_cast<SampHdr*>(smem_raw);
-  uint8_t* region = smem_raw + ((sizeof(SampHdr) + 127) / 128) * 128;
-  T* slice_smem = reinterpret_cast<T*>(region + region_bytes<T>());
-  // the region is reused: window counts, then radix bins, then Gumbel queues
-  uint32_t* win = reinterpret_cast<uint32_t*>(region);
+  // [header][resident slice][region]; the region is reused: window counts
+  // and candidate lists, radix bins, Gumbel queues
+  T* slice_smem = reinterpret_cast<T*>(smem_raw + ((sizeof(SampHdr) + 127) / 128) * 128);
+  uint8_t* region = reinterpret_cast<uint8_t*>(slice_smem) +
+                    (a.resident ? (((size_t)a.slice * sizeof(T) + 127) / 128) * 128 : 0);
   unsigned long long (*hist)[256] = reinterpret_cast<unsigned long long (*)[256]>(region);
   uint32_t* q_idx = reinterpret_cast<uint32_t*>(region);
   float* q_x = reinterpret_cast<float*>(region + kSampWarps * kQueue * 4);
@@ -499,6 +572,584 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
   const int lo = (int)crank * a.slice;
   const int n = max(0, min(a.V, lo + a.slice) - lo);
   const int copy = warp & (kHistCopies - 1);
+
+  if constexpr (sizeof(T) == 2) {
+    if (a.fast) {
+      // ================= 16-bit logits, resident slice
+      constexpr int kWin1 = win1_bins<T>();
+      using T2 = typename Pack2<T>::T2;
+      const uint4* sv = reinterpret_cast<const uint4*>(slice_smem);
+      const int nvec = n / 8;
+      const int rest = nvec * 8;
+      auto bits_at = [&](int j) -> uint32_t {
+        return (uint32_t)(*reinterpret_cast<const unsigned short*>(slice_smem + j));
+      };
+      // ---- F0 + F1. slice -> shared memory in 16 KB bulk copies; each
+      // thread folds its word of a chunk into a packed max (one instruction
+      // per two logits) as soon as the chunk lands
+      T2 mx2 = as_t2<T>(Pack2<T>::kNegInf2);
+      {
+        const int bulk = nvec * 16;
+        const int nch = (bulk + kChunkBytes - 1) / kChunkBytes;
+        if (tid == 0) {
+          for (int i = 0; i < nch; ++i) mbar_init(&h.bar[i], 1);
+          fence_mbar_init();
+        }
+        __syncthreads();
+        if (tid == 0) {
+          for (int i = 0; i < nch; ++i) {
+            const int off = i * kChunkBytes;
+            const int sz = min(kChunkBytes, bulk - off);
+            mbar_arrive_expect_tx(&h.bar[i], (uint32_t)sz);
+            bulk_g2s(reinterpret_cast<uint8_t*>(slice_smem) + off, reinterpret_cast<const uint8_t*>(row + lo) + off,
+                     (uint32_t)sz, &h.bar[i]);
+          }
+        }
+        for (int j = rest + tid; j < n; j += kSampThreads) slice_smem[j] = row[lo + j];
+        for (int i = 0; i < nch; ++i) {
+          mbar_wait_bounded(&h.bar[i], 0);
+          const int v = i * (kChunkBytes / 16) + tid;           // one 16-byte word per thread and chunk
+          if (v < nvec) {
+            const uint4 u = sv[v];
+            mx2 = __hmax2(mx2, __hmax2(__hmax2(as_t2<T>(u.x), as_t2<T>(u.y)), __hmax2(as_t2<T>(u.z), as_t2<T>(u.w))));
+          }
+        }
+        __syncthreads();
+      }
+      uint32_t kmr;        // this CTA's max key
+      {
+        const uint32_t mw = t2_bits<T>(mx2);
+        uint32_t mx = max(K::key(mw & 0xffffu), K::key(mw >> 16));
+        for (int j = rest + tid; j < n; j += kSampThreads) mx = max(mx, K::key(bits_at(j)));
+        kmr = (uint32_t)block_max_u64(mx, h.red);
+      }
+      const float Tr = a.temperature[row_id];
+      if (!(Tr > 0.f)) {
+        // greedy: this slice's lowest index holding its max key, then one
+        // exchange; the packed (key, ~index) max is the row's answer
+        uint32_t first = 0xffffffffu;
+        const uint32_t km2 = kmr | (kmr << 16);
+        for (int v = tid; v < nvec; v += kSampThreads) {
+          const uint4 u = sv[v];
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t x2 = keys2(w[q]) ^ km2;
+            if ((x2 & 0xffffu) == 0) first = min(first, (uint32_t)(v * 8 + q * 2));
+            if ((x2 >> 16) == 0) first = min(first, (uint32_t)(v * 8 + q * 2 + 1));
+          }
+        }
+        for (int j = rest + tid; j < n; j += kSampThreads)
+          if (K::key(bits_at(j)) == kmr) first = min(first, (uint32_t)j);
+        // the min index among the threads that saw the max key is the max of
+        // its complement
+        const unsigned long long mine =
+            first == 0xffffffffu ? 0ull : (((unsigned long long)kmr << 32) | (0xffffffffull - (unsigned long long)(lo + (int)first)));
+        const unsigned long long pk = block_max_u64(mine, h.red);
+        const ulonglong2* px = cluster_push(c, crank, pk, 0ull);
+        if (crank == 0 && tid == 0) {
+          unsigned long long best = 0;
+          for (int r = 0; r < c.cs; ++r) best = px[r].x > best ? px[r].x : best;
+          a.token_ids[row_id] = (int)(0xffffffffu - (uint32_t)(best & 0xffffffffull));
+        }
+        return;
+      }
+      const float l2t = 1.4426950408889634f / Tr;
+      const int k = a.top_k[row_id];
+      const bool topk_on = k > 0 && k < a.V;
+      const float p = a.top_p[row_id];
+      const bool nucleus_on = p < 1.f;
+      const bool need_win = topk_on || nucleus_on;
+      const bool need_z = nucleus_on && !topk_on;
+      uint32_t kth = 0, tau = 0;
+      long long need_eq = 0, cnt_eq = 0;
+      bool topk_done = !topk_on, nucleus_done = !nucleus_on;
+      uint32_t kmax = kmr;       // the row's max key (known after the window exchange)
+      float m = K::value_of_key(kmr);
+      bool list_ok = false;      // the list below holds every id of the first window
+      bool windows_free = false; // no peer reads this CTA's window any more (cluster-uniform)
+      int list_n = 0;
+
+      // ---- F2. exact counts per key in a window of keys below the max.
+      // Bins are distances from this CTA's own max key, so no exchange is
+      // needed before counting; the walk shifts each peer's bins by the gap
+      // between the row max and that peer's max.  Counting is staged: ids of
+      // the first kWin1 keys are compacted into a list (count, block scan,
+      // write) and binned from there in full warps, the normaliser Z of the
+      // nucleus rides along the count pass (a compensated f32 sum per
+      // thread, relative to this CTA's max, fixed point from there on); keys
+      // down to kWinTop are counted straight from the slice only when a cut
+      // lies that deep.
+      uint32_t* win = reinterpret_cast<uint32_t*>(region);
+      uint32_t* list = win + kWin1;
+      if (need_win) {
+        for (int i = tid; i < kWin1; i += kSampThreads) win[i] = 0u;
+        const float mr = m;
+        const float ml2t = mr * l2t;
+        // packed test "key >= kmr - (kWin1 - 1)" on the values
+        const uint32_t k1 = kmr >= (uint32_t)(kWin1 - 1) ? kmr - (uint32_t)(kWin1 - 1) : 0u;
+        const T2 t1v2 = key_threshold2<T>(k1);
+        float zs = 0.f, zc = 0.f;                 // compensated running sum
+        auto zadd = [&](float y) {
+          y -= zc;
+          const float t = zs + y;
+          zc = (t - zs) - y;
+          zs = t;
+        };
+        int hits = 0;
+        for (int v = tid; v < nvec; v += kSampThreads) {
+          const uint4 u = sv[v];
+          hits += __popc(pass_bits<T>(u, t1v2));
+          if (need_z) {
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            float vs = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float2 f = Pack2<T>::to_float2(w[q]);
+              vs += exp2f(fmaf(f.x, l2t, -ml2t)) + exp2f(fmaf(f.y, l2t, -ml2t));
+            }
+            zadd(vs);
+          }
+        }
+        for (int j = rest + tid; j < n; j += kSampThreads) {
+          const uint32_t b = bits_at(j);
+          hits += K::key(b) >= k1;
+          if (need_z) zadd(exp2f((K::value(b) - mr) * l2t));
+        }
+        unsigned long long tot_u;
+        const int first = (int)block_excl_scan_u64((unsigned long long)hits, h.red, tot_u);
+        list_n = (int)tot_u;
+        list_ok = list_n <= a.list_cap;
+        if (list_ok) {
+          if (hits > 0) {
+            int kk = first;
+            for (int v = tid; v < nvec; v += kSampThreads) {
+              uint32_t cb = pass_bits<T>(sv[v], t1v2);
+              while (cb) {
+                const int e = __ffs(cb) - 1;
+                cb &= cb - 1;
+                list[kk++] = (uint32_t)(v * 8 + e);
+              }
+            }
+            for (int j = rest + tid; j < n; j += kSampThreads)
+              if (K::key(bits_at(j)) >= k1) list[kk++] = (uint32_t)j;
+          }
+          __syncthreads();
+          for (int i = tid; i < list_n; i += kSampThreads) atomicAdd(&win[kmr - K::key(bits_at((int)list[i]))], 1u);
+        } else {
+          count_bins16<T>(sv, nvec, rest, n, slice_smem, kmr, win, 0u, (uint32_t)kWin1);
+        }
+        // one exchange: (max key, list flag) and Z relative to this CTA's
+        // max; from here on every CTA's first window is final, so peers read
+        // it in place over DSMEM
+        const unsigned long long zr = block_sum_u64(need_z ? fixed_weight(zs) : 0ull, h.red);
+        const ulonglong2* px = cluster_push(c, crank, ((unsigned long long)(list_ok ? 0u : 1u) << 32) | kmr, zr);
+        for (int r = 0; r < c.cs; ++r) {
+          kmax = max(kmax, (uint32_t)(px[r].x & 0xffffffffu));
+          if (px[r].x >> 32) list_ok = false;
+        }
+        m = K::value_of_key(kmax);
+        if (tid < c.cs) h.gap[tid] = (int)(kmax - (uint32_t)(px[tid].x & 0xffffffffu));
+        if (tid == 0) {
+          // Z = sum over ranks of Z_r * 2^((m_r - m) / T ln 2), each Z_r
+          // relative to its rank's max (fp64 for the few products only)
+          double zd = 0.0;
+          if (need_z)
+            for (int r = 0; r < c.cs; ++r)
+              zd += (double)px[r].y * (double)exp2f((K::value_of_key((uint32_t)(px[r].x & 0xffffffffu)) - m) * l2t);
+          h.zsum = (unsigned long long)zd;
+        }
+        __syncthreads();                                  // gap[] and zsum visible
+        const unsigned long long zrow = h.zsum;
+        auto wfix = [&](float x) -> unsigned long long { return fixed_weight(exp2f((x - m) * l2t)); };
+        int covered = kWin1;
+        // the second stage: the bins it writes were never read (they held
+        // the list), so peers may still be walking the first window
+        // meanwhile; cluster-uniform
+        auto widen = [&]() {
+          __syncthreads();
+          for (int i = kWin1 + tid; i < kWinTop; i += kSampThreads) win[i] = 0u;
+          __syncthreads();
+          count_bins16<T>(sv, nvec, rest, n, slice_smem, kmr, win, (uint32_t)kWin1, (uint32_t)(kWinTop - kWin1));
+          cluster_sync();
+          covered = kWinTop;
+          list_ok = false;
+        };
+
+        // Walk the window down from the row max, kWinBlock bins per step
+        // (two per thread); counts are the cluster sums of the bins, so
+        // every CTA of the cluster takes the same branches.
+        static_assert(kWinBlock == 2 * kSampThreads, "two bins per thread and walk step");
+        // bins [d0, d1) of the row, d1 <= covered: every rank has counted
+        // them (a rank's bin for row distance d is d - gap, below covered)
+        auto row_counts = [&](int d0, int d1, unsigned int* cnt) {
+          const int d = d0 + tid * 2;
+          cnt[0] = cnt[1] = 0;
+          for (int r = 0; r < c.cs; ++r) {
+            const int dr = d - h.gap[r];               // the same key in rank r's bins
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+              if (d + e < d1 && dr + e >= 0) cnt[e] += dsmem_ld_u32(dsmem_addr(&win[dr + e], (uint32_t)r));
+          }
+        };
+        if (topk_on) {
+          unsigned long long before = 0;
+          for (int d0 = 0, d1 = 0; d0 < kWinTop && !topk_done; d0 = d1) {
+            if (d0 >= covered) widen();
+            d1 = min(d0 + kWinBlock, covered);
+            unsigned int cnt[2];
+            row_counts(d0, d1, cnt);
+            const unsigned long long mine = (unsigned long long)cnt[0] + cnt[1];
+            unsigned long long tot;
+            unsigned long long acc = before + block_excl_scan_u64(mine, h.red, tot);
+            if (acc < (unsigned long long)k && (unsigned long long)k <= acc + mine) {
+              const int e = acc + cnt[0] >= (unsigned long long)k ? 0 : 1;
+              h.sel_aux = d0 + tid * 2 + e;
+              h.sel_before = e ? acc + cnt[0] : acc;
+              h.sel_val = e ? cnt[1] : cnt[0];
+            }
+            __syncthreads();
+            if (before + tot >= (unsigned long long)k) {
+              kth = kmax - (uint32_t)h.sel_aux;
+              need_eq = k - (long long)h.sel_before;
+              cnt_eq = (long long)h.sel_val;
+              topk_done = true;
+            }
+            before += tot;
+          }
+        }
+        if (nucleus_on && topk_done) {
+          const int dk = topk_on ? (int)(kmax - kth) : kWinTop;   // bins past the k-th key are out
+          const unsigned long long tie_mass = topk_on ? (unsigned long long)need_eq * wfix(K::value_of_key(kth)) : 0ull;
+          auto bin_mass = [&](int d, int d1, unsigned int cnt) -> unsigned long long {
+            if (d >= d1 || d > dk) return 0ull;
+            if (topk_on && d == dk) return tie_mass;
+            return cnt ? (unsigned long long)cnt * wfix(K::value_of_key(kmax - (uint32_t)d)) : 0ull;
+          };
+          unsigned long long Z = zrow;
+          if (topk_on) {          // Z of the top-k set: its bins all lie in the window
+            Z = 0;
+            for (int d0 = 0, d1 = 0; d0 <= dk; d0 = d1) {      // dk < covered
+              d1 = min(d0 + kWinBlock, covered);
+              unsigned int cnt[2];
+              row_counts(d0, d1, cnt);
+              Z += block_sum_u64(bin_mass(d0 + tid * 2, d1, cnt[0]) + bin_mass(d0 + tid * 2 + 1, d1, cnt[1]), h.red);
+            }
+          }
+          const unsigned long long P = (unsigned long long)((double)p * (double)Z);
+          unsigned long long before = 0;
+          for (int d0 = 0, d1 = 0; d0 < kWinTop && d0 <= dk && !nucleus_done; d0 = d1) {
+            if (d0 >= covered) widen();
+            d1 = min(d0 + kWinBlock, covered);
+            unsigned int cnt[2];
+            row_counts(d0, d1, cnt);
+            const unsigned long long mb0 = bin_mass(d0 + tid * 2, d1, cnt[0]), mb1 = bin_mass(d0 + tid * 2 + 1, d1, cnt[1]);
+            const unsigned long long mine = mb0 + mb1;
+            unsigned long long tot;
+            const unsigned long long acc = before + block_excl_scan_u64(mine, h.red, tot);
+            if (acc <= P && P < acc + mine) h.sel_aux = d0 + tid * 2 + (acc + mb0 > P ? 0 : 1);
+            __syncthreads();
+            if (before + tot > P) {
+              tau = kmax - (uint32_t)h.sel_aux;
+              nucleus_done = true;
+            }
+            before += tot;
+          }
+        }
+      }
+      const float mrow = m;     // the row max (this CTA's own when no window was needed: a safe bound)
+
+      // cuts the window cannot answer: radix selection over the slice.  The
+      // bins overlay the windows, so first wait until no peer reads them.
+      if (!topk_done) {
+        cluster_sync();
+        windows_free = true;
+        list_ok = false;
+        uint32_t prefix = 0;
+        unsigned long long remaining = (unsigned long long)k;
+        for (int shift = 8; shift >= 0; shift -= 8) {
+          for (int i = tid; i < kHistCopies * 256; i += kSampThreads) (&hist[0][0])[i] = 0ull;
+          __syncthreads();
+          const uint32_t hi_mask = shift == 8 ? 0u : 0xff00u;
+          visit<T>(slice_smem, n, true, [&](int, uint32_t b) {
+            const uint32_t key = K::key(b);
+            if ((key & hi_mask) == (prefix & hi_mask))
+              atomicAdd(reinterpret_cast<unsigned int*>(&hist[copy][(key >> shift) & 255u]), 1u);
+          });
+          __syncthreads();
+          if (tid < 256) {
+            unsigned long long s2 = 0;
+            for (int cp = 0; cp < kHistCopies; ++cp) s2 += (unsigned int)(hist[cp][tid] & 0xffffffffull);
+            h.ex_arr[c.ex][tid] = s2;
+          }
+          cluster_sum_array(c);
+          select_bin<true>(h, remaining, false);
+          const int bin = h.sel_bin;
+          remaining -= h.sel_before;
+          prefix |= (uint32_t)bin << shift;
+          if (shift == 0) cnt_eq = (long long)h.tot[bin];
+          __syncthreads();
+        }
+        kth = prefix;
+        need_eq = (long long)remaining;
+        topk_done = true;
+      }
+      if (!nucleus_done) {
+        if (!windows_free) cluster_sync();
+        windows_free = true;
+        list_ok = false;
+        auto wfix = [&](float x) -> unsigned long long { return fixed_weight(exp2f((x - mrow) * l2t)); };
+        uint32_t prefix = 0;
+        unsigned long long target = 0, above = 0;
+        for (int shift = 8; shift >= 0; shift -= 8) {
+          for (int i = tid; i < kHistCopies * 256; i += kSampThreads) (&hist[0][0])[i] = 0ull;
+          __syncthreads();
+          const uint32_t hi_mask = shift == 8 ? 0u : 0xff00u;
+          visit<T>(slice_smem, n, true, [&](int, uint32_t b) {
+            const uint32_t key = K::key(b);
+            if ((key & hi_mask) != (prefix & hi_mask)) return;
+            if (topk_on && key <= kth) return;
+            atomicAdd(&hist[copy][(key >> shift) & 255u], wfix(K::value(b)));
+          });
+          __syncthreads();
+          if (tid < 256) {
+            unsigned long long s2 = 0;
+            for (int cp = 0; cp < kHistCopies; ++cp) s2 += hist[cp][tid];
+            if (crank == 0 && topk_on && need_eq > 0 && (kth & hi_mask) == (prefix & hi_mask) &&
+                (int)((kth >> shift) & 255u) == tid)
+              s2 += (unsigned long long)need_eq * wfix(K::value_of_key(kth));
+            h.ex_arr[c.ex][tid] = s2;
+          }
+          cluster_sum_array(c);
+          if (shift == 8) target = (unsigned long long)((double)p * (double)sum_tot(h));
+          select_bin<true>(h, target - above, true);
+          const int bin = h.sel_bin;
+          const unsigned long long sb = h.sel_before;
+          __syncthreads();
+          if (bin < 0) { prefix = 0; break; }
+          above += sb;
+          prefix |= (uint32_t)bin << shift;
+        }
+        tau = prefix;
+      }
+
+      // ---- F3. this CTA's share of the lowest-index ties at the k-th key
+      // (slices are ordered by index, so lower ranks take theirs first).
+      // The exchange of the tie counts is also the barrier after which no
+      // peer reads this CTA's window any more.
+      int tie_lim = 0x7fffffff;
+      if (topk_on && need_eq < cnt_eq) {
+        const bool hi_ok = kth < 0xffffu;
+        const T2 ge_k = key_threshold2<T>(kth), ge_k1 = key_threshold2<T>(hi_ok ? kth + 1u : kth);
+        auto tie_bits = [&](const uint4 u) -> uint32_t {
+          return pass_bits<T>(u, ge_k) & (hi_ok ? ~pass_bits<T>(u, ge_k1) : 0xffu);
+        };
+        int tn = 0;
+        for (int v = tid; v < nvec; v += kSampThreads) tn += __popc(tie_bits(sv[v]));
+        for (int j = rest + tid; j < n; j += kSampThreads) tn += K::key(bits_at(j)) == kth;
+        const unsigned long long mine = block_sum_u64((unsigned long long)tn, h.red);
+        long long before = 0;
+        {
+          const ulonglong2* px = cluster_push(c, crank, mine, 0ull);
+          for (int r = 0; r < (int)crank; ++r) before += (long long)px[r].x;
+        }
+        windows_free = true;
+        const long long want = min(max(need_eq - before, 0ll), (long long)mine);
+        // the tie list goes after the candidate list (or anywhere in the
+        // region once that list is gone)
+        uint32_t* tl = list_ok ? list + list_n : win;
+        const long long tcap = list_ok ? (long long)a.list_cap - list_n : (long long)a.list_cap + kWin1;
+        if (want == 0) {
+          tie_lim = -1;
+        } else if (want < (long long)mine && (long long)mine <= tcap) {
+          // ties in index order: each thread takes a contiguous run of
+          // words (the few ids past the last word go to the last thread),
+          // a block scan places the runs, and the want-th tie is the limit
+          const int per = (nvec + kSampThreads - 1) / kSampThreads;
+          const int v0 = min(nvec, tid * per), v1 = min(nvec, v0 + per);
+          int cnt = 0;
+          for (int v = v0; v < v1; ++v) cnt += __popc(tie_bits(sv[v]));
+          if (tid == kSampThreads - 1)
+            for (int j = rest; j < n; ++j) cnt += K::key(bits_at(j)) == kth;
+          unsigned long long tot_t;
+          int pos = (int)block_excl_scan_u64((unsigned long long)cnt, h.red, tot_t);
+          for (int v = v0; v < v1; ++v) {
+            uint32_t tb = tie_bits(sv[v]);
+            while (tb) {
+              const int e = __ffs(tb) - 1;
+              tb &= tb - 1;
+              tl[pos++] = (uint32_t)(v * 8 + e);
+            }
+          }
+          if (tid == kSampThreads - 1)
+            for (int j = rest; j < n; ++j)
+              if (K::key(bits_at(j)) == kth) tl[pos++] = (uint32_t)j;
+          __syncthreads();
+          tie_lim = (int)tl[want - 1];
+        } else if (want < (long long)mine) {
+          // too many ties for the free space: local radix select over the
+          // tie indices, in bins that overlay the region
+          list_ok = false;
+          uint32_t prefix = 0;
+          unsigned long long remaining = (unsigned long long)want;
+          for (int shift = 16; shift >= 0; shift -= 8) {       // 24-bit slice-local indices
+            for (int i = tid; i < kHistCopies * 256; i += kSampThreads) (&hist[0][0])[i] = 0ull;
+            __syncthreads();
+            const uint32_t hi_mask = (shift + 8 >= 24) ? 0u : ((~0u << (shift + 8)) & 0xffffffu);
+            visit<T>(slice_smem, n, true, [&](int j, uint32_t b) {
+              if (K::key(b) != kth) return;
+              const uint32_t ik = 0xffffffu - (uint32_t)j;
+              if ((ik & hi_mask) == (prefix & hi_mask))
+                atomicAdd(reinterpret_cast<unsigned int*>(&hist[copy][(ik >> shift) & 255u]), 1u);
+            });
+            __syncthreads();
+            if (tid < 256) {
+              unsigned long long s2 = 0;
+              for (int cp = 0; cp < kHistCopies; ++cp) s2 += (unsigned int)(hist[cp][tid] & 0xffffffffull);
+              h.tot[tid] = s2;
+            }
+            __syncthreads();
+            select_bin<true>(h, remaining, false);
+            remaining -= h.sel_before;
+            prefix |= (uint32_t)h.sel_bin << shift;
+            __syncthreads();
+          }
+          tie_lim = (int)(0xffffffu - prefix);
+        }
+      }
+
+      // ---- F4. Gumbel-max over the kept ids
+      uint32_t thr = tau;
+      if (topk_on && kth > thr) thr = kth;
+      {
+        // ids below m - 22 T can never win: fold that into the key threshold
+        const float vmin = mrow - 22.f * Tr;
+        T tv;
+        if constexpr (std::is_same<T, __half>::value) tv = __float2half_rd(vmin);
+        else tv = __float2bfloat16_rd(vmin);
+        const uint32_t kp = K::key((uint32_t)(*reinterpret_cast<const unsigned short*>(&tv)));
+        if (!isinf(vmin) && kp > thr) thr = kp;
+      }
+      const uint64_t seed = a.seeds[row_id], off = a.offsets[row_id];
+      const float invT = 1.f / Tr;
+      auto keep = [&](int j, uint32_t b) -> bool {
+        const uint32_t key = K::key(b);
+        if (key < tau) return false;
+        if (topk_on && (key < kth || (key == kth && j > tie_lim))) return false;
+        return (K::value(b) - mrow) * invT >= -kGumbelSpan;
+      };
+      auto score_of = [&](int jg, uint32_t b) -> unsigned long long {
+        return race_key(seed, off, (uint32_t)jg, (mrow - K::value(b)) * l2t);
+      };
+      unsigned long long bestg = 0;
+      // The first window's list holds every candidate when the cut lies in
+      // the window (thr >= its lowest key); each warp then compacts its
+      // own segment of the list in place and scores it.  Otherwise the
+      // candidates are compacted from the slice into a CTA-wide list after
+      // the full window (count pass, block scan, write pass), in rounds if
+      // they do not fit.  Either way Philox and the logarithms run on full
+      // warps.
+      if (list_ok) {
+        const int seg = ((list_n + kSampWarps - 1) / kSampWarps + 31) & ~31;
+        const int s0 = min(list_n, warp * seg), s1 = min(list_n, s0 + seg);
+        int wpos = s0;
+        for (int base = s0; base < s1; base += 32) {
+          const int i = base + lane;
+          const uint32_t j = i < s1 ? list[i] : 0u;
+          const bool pass = i < s1 && K::key(bits_at((int)j)) >= thr;
+          const unsigned mask = __ballot_sync(FULL_MASK, pass);
+          // every lane loaded before the ballot, and writes land at or
+          // below the slots this warp has read
+          if (pass) list[wpos + __popc(mask & ((1u << lane) - 1u))] = j;
+          wpos += __popc(mask);
+        }
+        __syncwarp();
+        for (int i = s0 + lane; i < wpos; i += 32) {
+          const int j = (int)list[i];
+          const uint32_t b = bits_at(j);
+          if (keep(j, b)) {
+            const unsigned long long pk = score_of(lo + j, b);
+            bestg = pk > bestg ? pk : bestg;
+          }
+        }
+      } else {
+        // the windows are free once no peer walks them; list_ok is
+        // cluster-uniform until the windows are free, so this is too
+        if (need_win && !windows_free) cluster_sync();
+        const int cap = a.list_cap + kWin1;      // every entry of the region
+        uint32_t* cl = win;
+        const T2 thr_v2 = key_threshold2<T>(thr);
+        int mine = 0;
+        for (int v = tid; v < nvec; v += kSampThreads) mine += __popc(pass_bits<T>(sv[v], thr_v2));
+        for (int j = rest + tid; j < n; j += kSampThreads) mine += K::key(bits_at(j)) >= thr;
+        unsigned long long total_u;
+        const int first = (int)block_excl_scan_u64((unsigned long long)mine, h.red, total_u);
+        const int total = (int)total_u;
+        for (int r0 = 0; r0 < total; r0 += cap) {          // block-uniform
+          const int r1 = min(total, r0 + cap);
+          if (mine > 0 && first < r1 && first + mine > r0) {
+            int kk = first;                                 // list rank of this thread's next candidate
+            for (int v = tid; v < nvec && kk < r1; v += kSampThreads) {
+              uint32_t cb = pass_bits<T>(sv[v], thr_v2);
+              while (cb) {
+                const int e = __ffs(cb) - 1;
+                cb &= cb - 1;
+                if (kk >= r0 && kk < r1) cl[kk - r0] = (uint32_t)(v * 8 + e);
+                ++kk;
+              }
+            }
+            for (int j = rest + tid; j < n && kk < r1; j += kSampThreads) {
+              if (K::key(bits_at(j)) < thr) continue;
+              if (kk >= r0) cl[kk - r0] = (uint32_t)j;
+              ++kk;
+            }
+          }
+          __syncthreads();
+          for (int i = tid; i < r1 - r0; i += kSampThreads) {
+            const int j = (int)cl[i];
+            const uint32_t b = bits_at(j);
+            if (keep(j, b)) {
+              const unsigned long long pk = score_of(lo + j, b);
+              bestg = pk > bestg ? pk : bestg;
+            }
+          }
+          __syncthreads();
+        }
+      }
+      bestg = block_max_u64(bestg, h.red);
+      // Race times were taken against this CTA's bound mrow.  When every
+      // rank used the same bound (the row max) the packed keys compare as
+      // they are; otherwise each rank's best time moves to the row max in
+      // log2 units: log2 t + (max - mrow) / (T ln 2).
+      const ulonglong2* px = cluster_push(c, crank, bestg, (unsigned long long)__float_as_uint(mrow));
+      // the max id always passes every filter, so the row's best is never 0
+      if (crank == 0 && tid == 0) {
+        bool same = true;
+        float mm = __uint_as_float((uint32_t)px[0].y);
+        for (int r = 1; r < c.cs; ++r) {
+          same = same && px[r].y == px[0].y;
+          mm = fmaxf(mm, __uint_as_float((uint32_t)px[r].y));
+        }
+        unsigned long long best = 0;
+        if (same) {
+          for (int r = 0; r < c.cs; ++r) best = px[r].x > best ? px[r].x : best;
+        } else {
+          float bl = 0.f;
+          for (int r = 0; r < c.cs; ++r) {
+            if (px[r].x == 0) continue;
+            const float t = Keys<float>::value_of_key(~(uint32_t)(px[r].x >> 32));
+            const float lr = log2f(t) + (mm - __uint_as_float((uint32_t)px[r].y)) * l2t;
+            if (best == 0 || lr < bl || (lr == bl && (uint32_t)px[r].x > (uint32_t)best)) {
+              bl = lr;
+              best = px[r].x;
+            }
+          }
+        }
+        a.token_ids[row_id] = (int)(0xffffffffu - (uint32_t)(best & 0xffffffffull));
+      }
+      return;
+    }
+  }
 
   // ---- 0. slice -> shared memory (bulk copies, one barrier per chunk)
   const T* src = row + lo;
@@ -528,427 +1179,6 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
     vec = true;
   }
 
-  if constexpr (sizeof(T) == 2) {
-    if (a.fast) {
-      // ================= 16-bit logits, resident slice
-      const uint4* sv = reinterpret_cast<const uint4*>(src);
-      const int nvec = n / 8;
-      const int rest = nvec * 8;
-      auto bits_at = [&](int j) -> uint32_t { return (uint32_t)(*reinterpret_cast<const unsigned short*>(src + j)); };
-
-      // ---- F1. row max key: packed max of the values (one instruction per
-      // two logits), keyed once at the end
-      using T2 = typename Pack2<T>::T2;
-      T2 mx2 = as_t2<T>(Pack2<T>::kNegInf2);
-      for (int v = tid; v < nvec; v += kSampThreads) {
-        const uint4 u = sv[v];
-        mx2 = __hmax2(mx2, __hmax2(__hmax2(as_t2<T>(u.x), as_t2<T>(u.y)), __hmax2(as_t2<T>(u.z), as_t2<T>(u.w))));
-      }
-      const uint32_t mw = t2_bits<T>(mx2);
-      uint32_t mx = max(K::key(mw & 0xffffu), K::key(mw >> 16));
-      for (int j = rest + tid; j < n; j += kSampThreads) mx = max(mx, K::key(bits_at(j)));
-      const uint32_t kmax = (uint32_t)cluster_scalar<true>(c, block_max_u64(mx, h.red), 0);
-      const float Tr = a.temperature[row_id];
-      if (!(Tr > 0.f)) {
-        // greedy: the lowest index holding the max key
-        uint32_t first = 0xffffffffu;
-        for (int v = tid; v < nvec; v += kSampThreads) {
-          const uint4 u = sv[v];
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t k2 = keys2(w[q]);
-            if ((k2 & 0xffffu) == kmax) first = min(first, (uint32_t)(v * 8 + q * 2));
-            if ((k2 >> 16) == kmax) first = min(first, (uint32_t)(v * 8 + q * 2 + 1));
-          }
-        }
-        for (int j = rest + tid; j < n; j += kSampThreads)
-          if (K::key(bits_at(j)) == kmax) first = min(first, (uint32_t)j);
-        // max of the complement = min index (lo + first, or 0 if none here)
-        const unsigned long long inv = first == 0xffffffffu ? 0ull : 0xffffffffull - (unsigned long long)(lo + first);
-        const unsigned long long best_inv = cluster_scalar<true>(c, block_max_u64(inv, h.red), 1);
-        if (crank == 0 && tid == 0) a.token_ids[row_id] = (int)(0xffffffffull - best_inv);
-        cluster_sync();               // peers may still read this CTA's shared memory
-        return;
-      }
-      const float m = K::value_of_key(kmax);
-      const float l2t = 1.4426950408889634f / Tr;
-      auto wfix = [&](float x) -> unsigned long long { return fixed_weight(exp2f((x - m) * l2t)); };
-      const int k = a.top_k[row_id];
-      const bool topk_on = k > 0 && k < a.V;
-      const float p = a.top_p[row_id];
-      const bool nucleus_on = p < 1.f;
-      uint32_t kth = 0, tau = 0;
-      long long need_eq = 0, cnt_eq = 0;
-      bool topk_done = !topk_on, nucleus_done = !nucleus_on;
-
-      // ---- F2. exact counts of the top kWinTop keys below the max; for the
-      // nucleus without top-k, the normaliser Z over every id as a
-      // compensated f32 sum per thread (fixed point from there on)
-      uint32_t* win = reinterpret_cast<uint32_t*>(region);
-      if (topk_on || nucleus_on) {
-        for (int i = tid; i < kWinTop; i += kSampThreads) win[i] = 0u;
-        __syncthreads();
-        const uint32_t kmax2 = kmax | (kmax << 16);
-        const bool need_z = nucleus_on && !topk_on;
-        float zs = 0.f, zc = 0.f;                 // compensated running sum
-        auto zadd = [&](float y) {
-          y -= zc;
-          const float t = zs + y;
-          zc = (t - zs) - y;
-          zs = t;
-        };
-        auto wexp = [&](uint32_t b) { return exp2f((K::value(b) - m) * l2t); };
-        const float ml2t = m * l2t;
-        for (int v = tid; v < nvec; v += kSampThreads) {
-          const uint4 u = sv[v];
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-          float vs = 0.f;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            // per-half kmax - key: no borrow crosses the halves, as every key <= kmax
-            const uint32_t d2 = kmax2 - keys2(w[q]);
-            const uint32_t dlo = d2 & 0xffffu, dhi = d2 >> 16;
-            if (dlo < (uint32_t)kWinTop) atomicAdd(&win[dlo], 1u);
-            if (dhi < (uint32_t)kWinTop) atomicAdd(&win[dhi], 1u);
-            if (need_z) {
-              const float2 f = Pack2<T>::to_float2(w[q]);
-              vs += exp2f(fmaf(f.x, l2t, -ml2t)) + exp2f(fmaf(f.y, l2t, -ml2t));
-            }
-          }
-          if (need_z) zadd(vs);
-        }
-        for (int j = rest + tid; j < n; j += kSampThreads) {
-          const uint32_t b = bits_at(j);
-          const uint32_t d = kmax - K::key(b);
-          if (d < (uint32_t)kWinTop) atomicAdd(&win[d], 1u);
-          if (need_z) zadd(wexp(b));
-        }
-        // one cluster barrier: Z travels with it, and from here on every
-        // CTA's window is final, so peers read it in place over DSMEM
-        const unsigned long long zrow = cluster_scalar<false>(c, block_sum_u64(need_z ? fixed_weight(zs) : 0ull, h.red), 2);
-
-        // Walk the window down from the max, kWinBlock bins per step (4 per
-        // thread, contiguous); counts are the cluster sums of the bins.
-        constexpr int kPer = 4;
-        constexpr int kWinBlock = kSampThreads * kPer;
-        auto row_counts = [&](int d0, unsigned int* cnt) {
-          const int d = d0 + tid * kPer;
-#pragma unroll
-          for (int e = 0; e < kPer; ++e) cnt[e] = 0;
-          for (int r = 0; r < c.cs; ++r) {
-            const uint32_t a4 = dsmem_addr(&win[d], (uint32_t)r);
-            uint4 x;
-            asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w) : "r"(a4) : "memory");
-            cnt[0] += x.x; cnt[1] += x.y; cnt[2] += x.z; cnt[3] += x.w;
-          }
-        };
-        if (topk_on) {
-          unsigned long long before = 0;
-          for (int d0 = 0; d0 < kWinTop && !topk_done; d0 += kWinBlock) {
-            unsigned int cnt[kPer];
-            row_counts(d0, cnt);
-            const unsigned long long mine = (unsigned long long)cnt[0] + cnt[1] + cnt[2] + cnt[3];
-            unsigned long long tot;
-            unsigned long long acc = before + block_excl_scan_u64(mine, h.red, tot);
-            if (acc < (unsigned long long)k && (unsigned long long)k <= acc + mine) {
-#pragma unroll
-              for (int e = 0; e < kPer; ++e) {
-                if (acc + cnt[e] >= (unsigned long long)k) {
-                  h.sel_aux = d0 + tid * kPer + e;
-                  h.sel_before = acc;
-                  h.sel_val = cnt[e];
-                  break;
-                }
-                acc += cnt[e];
-              }
-            }
-            __syncthreads();
-            if (before + tot >= (unsigned long long)k) {
-              kth = kmax - (uint32_t)h.sel_aux;
-              need_eq = k - (long long)h.sel_before;
-              cnt_eq = (long long)h.sel_val;
-              topk_done = true;
-            }
-            before += tot;
-            __syncthreads();
-          }
-        }
-        if (nucleus_on && topk_done) {
-          const int dk = topk_on ? (int)(kmax - kth) : kWinTop;   // bins past the k-th key are out
-          const unsigned long long tie_mass = topk_on ? (unsigned long long)need_eq * wfix(K::value_of_key(kth)) : 0ull;
-          auto bin_mass = [&](int d, unsigned int cnt) -> unsigned long long {
-            if (d > dk) return 0ull;
-            if (topk_on && d == dk) return tie_mass;
-            return cnt ? (unsigned long long)cnt * wfix(K::value_of_key(kmax - (uint32_t)d)) : 0ull;
-          };
-          unsigned long long Z = zrow;
-          if (topk_on) {          // Z of the top-k set: its bins all lie in the window
-            Z = 0;
-            for (int d0 = 0; d0 <= dk; d0 += kWinBlock) {
-              unsigned int cnt[kPer];
-              row_counts(d0, cnt);
-              unsigned long long mine = 0;
-#pragma unroll
-              for (int e = 0; e < kPer; ++e) mine += bin_mass(d0 + tid * kPer + e, cnt[e]);
-              Z += block_sum_u64(mine, h.red);
-            }
-          }
-          const unsigned long long P = (unsigned long long)((double)p * (double)Z);
-          unsigned long long before = 0;
-          for (int d0 = 0; d0 < kWinTop && d0 <= dk && !nucleus_done; d0 += kWinBlock) {
-            unsigned int cnt[kPer];
-            row_counts(d0, cnt);
-            unsigned long long mb[kPer], mine = 0;
-#pragma unroll
-            for (int e = 0; e < kPer; ++e) {
-              mb[e] = bin_mass(d0 + tid * kPer + e, cnt[e]);
-              mine += mb[e];
-            }
-            unsigned long long tot;
-            unsigned long long acc = before + block_excl_scan_u64(mine, h.red, tot);
-            if (acc <= P && P < acc + mine) {
-#pragma unroll
-              for (int e = 0; e < kPer; ++e) {
-                if (acc + mb[e] > P) {
-                  h.sel_aux = d0 + tid * kPer + e;
-                  break;
-                }
-                acc += mb[e];
-              }
-            }
-            __syncthreads();
-            if (before + tot > P) {
-              tau = kmax - (uint32_t)h.sel_aux;
-              nucleus_done = true;
-            }
-            before += tot;
-            __syncthreads();
-          }
-        }
-        cluster_sync();          // every peer is done reading this CTA's window
-      }
-      // cuts the window cannot answer: radix selection over the slice
-      if (!topk_done) {
-        uint32_t prefix = 0;
-        unsigned long long remaining = (unsigned long long)k;
-        for (int shift = 8; shift >= 0; shift -= 8) {
-          for (int i = tid; i < kHistCopies * 256; i += kSampThreads) (&hist[0][0])[i] = 0ull;
-          __syncthreads();
-          const uint32_t hi_mask = shift == 8 ? 0u : 0xff00u;
-          visit<T>(src, n, true, [&](int, uint32_t b) {
-            const uint32_t key = K::key(b);
-            if ((key & hi_mask) == (prefix & hi_mask))
-              atomicAdd(reinterpret_cast<unsigned int*>(&hist[copy][(key >> shift) & 255u]), 1u);
-          });
-          __syncthreads();
-          if (tid < 256) {
-            unsigned long long s2 = 0;
-            for (int cp = 0; cp < kHistCopies; ++cp) s2 += (unsigned int)(hist[cp][tid] & 0xffffffffull);
-            h.ex_arr[c.ex][tid] = s2;
-          }
-          cluster_sum_array(c);
-          select_bin<true>(h, remaining, false);
-          const int bin = h.sel_bin;
-          remaining -= h.sel_before;
-          prefix |= (uint32_t)bin << shift;
-          if (shift == 0) cnt_eq = (long long)h.tot[bin];
-          __syncthreads();
-        }
-        kth = prefix;
-        need_eq = (long long)remaining;
-        topk_done = true;
-      }
-      if (!nucleus_done) {
-        uint32_t prefix = 0;
-        unsigned long long target = 0, above = 0;
-        for (int shift = 8; shift >= 0; shift -= 8) {
-          for (int i = tid; i < kHistCopies * 256; i += kSampThreads) (&hist[0][0])[i] = 0ull;
-          __syncthreads();
-          const uint32_t hi_mask = shift == 8 ? 0u : 0xff00u;
-          visit<T>(src, n, true, [&](int, uint32_t b) {
-            const uint32_t key = K::key(b);
-            if ((key & hi_mask) != (prefix & hi_mask)) return;
-            if (topk_on && key <= kth) return;
-            atomicAdd(&hist[copy][(key >> shift) & 255u], wfix(K::value(b)));
-          });
-          __syncthreads();
-          if (tid < 256) {
-            unsigned long long s2 = 0;
-            for (int cp = 0; cp < kHistCopies; ++cp) s2 += hist[cp][tid];
-            if (crank == 0 && topk_on && need_eq > 0 && (kth & hi_mask) == (prefix & hi_mask) &&
-                (int)((kth >> shift) & 255u) == tid)
-              s2 += (unsigned long long)need_eq * wfix(K::value_of_key(kth));
-            h.ex_arr[c.ex][tid] = s2;
-          }
-          cluster_sum_array(c);
-          if (shift == 8) target = (unsigned long long)((double)p * (double)sum_tot(h));
-          select_bin<true>(h, target - above, true);
-          const int bin = h.sel_bin;
-          const unsigned long long sb = h.sel_before;
-          __syncthreads();
-          if (bin < 0) { prefix = 0; break; }
-          above += sb;
-          prefix |= (uint32_t)bin << shift;
-        }
-        tau = prefix;
-      }
-
-      // ---- F3. this CTA's share of the lowest-index ties at the k-th key
-      int tie_lim = 0x7fffffff;
-      if (topk_on && need_eq < cnt_eq) {
-        unsigned long long mine = 0;
-        visit<T>(src, n, true, [&](int, uint32_t b) { mine += K::key(b) == kth; });
-        mine = block_sum_u64(mine, h.red);
-        long long before = 0;
-        {
-          const int sl = c.ex;
-          c.ex ^= 1;
-          if (tid == 0) h.ex_sc[sl][2] = mine;
-          cluster_sync();
-          for (int r = 0; r < (int)crank; ++r) before += (long long)dsmem_ld_u64(dsmem_addr(&h.ex_sc[sl][2], r));
-        }
-        const long long want = min(max(need_eq - before, 0ll), (long long)mine);
-        if (want == 0) {
-          tie_lim = -1;
-        } else if (want < (long long)mine) {
-          uint32_t prefix = 0;
-          unsigned long long remaining = (unsigned long long)want;
-          for (int shift = 16; shift >= 0; shift -= 8) {       // 24-bit slice-local indices
-            for (int i = tid; i < kHistCopies * 256; i += kSampThreads) (&hist[0][0])[i] = 0ull;
-            __syncthreads();
-            const uint32_t hi_mask = (shift + 8 >= 24) ? 0u : ((~0u << (shift + 8)) & 0xffffffu);
-            visit<T>(src, n, true, [&](int j, uint32_t b) {
-              if (K::key(b) != kth) return;
-              const uint32_t ik = 0xffffffu - (uint32_t)j;
-              if ((ik & hi_mask) == (prefix & hi_mask))
-                atomicAdd(reinterpret_cast<unsigned int*>(&hist[copy][(ik >> shift) & 255u]), 1u);
-            });
-            __syncthreads();
-            if (tid < 256) {
-              unsigned long long s2 = 0;
-              for (int cp = 0; cp < kHistCopies; ++cp) s2 += (unsigned int)(hist[cp][tid] & 0xffffffffull);
-              h.tot[tid] = s2;
-            }
-            __syncthreads();
-            select_bin<true>(h, remaining, false);
-            remaining -= h.sel_before;
-            prefix |= (uint32_t)h.sel_bin << shift;
-            __syncthreads();
-          }
-          tie_lim = (int)(0xffffffu - prefix);
-        }
-      }
-
-      // ---- F4. Gumbel-max over the kept ids.  A packed key test (two keys per
-      // step) finds the few candidates; only they get Philox noise.
-      uint32_t thr = tau;
-      if (topk_on && kth > thr) thr = kth;
-      {
-        // ids below m - 22 T can never win: fold that into the key threshold
-        const float vmin = m - 22.f * Tr;
-        T tv;
-        if constexpr (std::is_same<T, __half>::value) tv = __float2half_rd(vmin);
-        else tv = __float2bfloat16_rd(vmin);
-        const uint32_t kp = K::key((uint32_t)(*reinterpret_cast<const unsigned short*>(&tv)));
-        if (!isinf(vmin) && kp > thr) thr = kp;
-      }
-      const uint64_t seed = a.seeds[row_id], off = a.offsets[row_id];
-      const float invT = 1.f / Tr;
-      auto keep = [&](int j, uint32_t b) -> bool {
-        const uint32_t key = K::key(b);
-        if (key < tau) return false;
-        if (topk_on && (key < kth || (key == kth && j > tie_lim))) return false;
-        return (K::value(b) - m) * invT >= -kGumbelSpan;
-      };
-      auto score_of = [&](int jg, uint32_t b) -> unsigned long long {
-        const float sc = __fdiv_rn(K::value(b), Tr) + gumbel_noise(seed, off, (uint32_t)jg);
-        return ((unsigned long long)f32_order_key(sc) << 32) | (0xffffffffu - (uint32_t)jg);
-      };
-      // per-thread candidate slots, slot-major so the stores do not collide;
-      // a thread that meets more than kSlots candidates flags the CTA, which
-      // then scores through per-warp queues instead
-      constexpr int kSlots = region_bytes<T>() / 4 / kSampThreads;
-      uint32_t* slot = reinterpret_cast<uint32_t*>(region);
-      if (tid == 0) h.cand_n = 0;                   // overflow flag
-      __syncthreads();
-      int mine = 0;
-      auto take = [&](int j, uint32_t b) {
-        if (K::key(b) < thr) return;
-        if (mine < kSlots) slot[mine * kSampThreads + tid] = (uint32_t)j;
-        ++mine;
-      };
-      // value of the threshold key (or -inf when every id passes): a packed
-      // compare of the values is the same test as comparing keys
-      uint32_t tb = thr == 0 ? (Pack2<T>::kNegInf2 & 0xffffu)
-                             : ((thr & 0x8000u) ? (thr & 0x7fffu) : (~thr & 0xffffu));
-      const T2 thr_v2 = as_t2<T>(tb | (tb << 16));
-      for (int v = tid; v < nvec; v += kSampThreads) {
-        const uint4 u = sv[v];
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-        uint32_t cb = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t ge = __hge2_mask(as_t2<T>(w[q]), thr_v2);
-          cb |= ((ge & 1u) | ((ge >> 15) & 2u)) << (2 * q);
-        }
-        while (cb) {
-          const int e = __ffs(cb) - 1;
-          cb &= cb - 1;
-          take(v * 8 + e, (w[e / 2] >> (16 * (e & 1))) & 0xffffu);
-        }
-      }
-      for (int j = rest + tid; j < n; j += kSampThreads) take(j, bits_at(j));
-      if (mine > kSlots) h.cand_n = 1;
-      __syncthreads();
-      unsigned long long bestg = 0;
-      if (!h.cand_n) {
-        for (int i = 0; i < mine; ++i) {
-          const int j = (int)slot[i * kSampThreads + tid];
-          const uint32_t b = bits_at(j);
-          if (keep(j, b)) {
-            const unsigned long long pk = score_of(lo + j, b);
-            bestg = pk > bestg ? pk : bestg;
-          }
-        }
-      } else {
-        // dense kept set: every warp queues its candidates and scores them
-        // 32 at a time (full warps)
-        __syncthreads();
-        uint32_t* qi = reinterpret_cast<uint32_t*>(region) + warp * kQueue;
-        int qh = 0, qn = 0;
-        auto drain = [&](int cnt) {
-          if (lane < cnt) {
-            const int j = (int)qi[(qh + lane) & (kQueue - 1)];
-            const unsigned long long pk = score_of(lo + j, bits_at(j));
-            bestg = pk > bestg ? pk : bestg;
-          }
-          __syncwarp();
-          qh = (qh + cnt) & (kQueue - 1);
-          qn -= cnt;
-        };
-        for (int jb = warp * 32; jb < n; jb += kSampThreads) {      // warp-uniform trip count
-          const int j = jb + lane;
-          const bool cand = j < n && keep(j, bits_at(j));
-          const unsigned mask = __ballot_sync(FULL_MASK, cand);
-          if (mask) {
-            if (cand) qi[(qh + qn + __popc(mask & ((1u << lane) - 1u))) & (kQueue - 1)] = (uint32_t)j;
-            qn += __popc(mask);
-            __syncwarp();
-            if (qn >= 32) drain(32);
-          }
-        }
-        if (qn > 0) drain(qn);
-      }
-      bestg = block_max_u64(bestg, h.red);
-      bestg = cluster_scalar<true>(c, bestg, 3);
-      // the max id always passes every filter, so bestg is never 0 here
-      if (crank == 0 && tid == 0) a.token_ids[row_id] = (int)(0xffffffffu - (uint32_t)(bestg & 0xffffffffull));
-      cluster_sync();               // peers may still read this CTA's shared memory
-      return;
-    }
-  }
-
   // ---- 1. max key and the lowest index holding it (row-wide)
   unsigned long long best = 0;
   visit<T>(src, n, vec, [&](int j, uint32_t b) {
@@ -956,7 +1186,7 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
     best = pk > best ? pk : best;
   });
   best = block_max_u64(best, h.red);
-  best = cluster_scalar<true>(c, best, 0);
+  best = cluster_scalar<true>(c, best);
   const uint32_t kmax = (uint32_t)(best >> 32);
   const int imax = (int)(0xffffffffu - (uint32_t)(best & 0xffffffffu));
   const float Tr = a.temperature[row_id];
@@ -1062,11 +1292,8 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
     mine = block_sum_u64(mine, h.red);
     long long before = 0;
     {
-      const int s = c.ex;
-      c.ex ^= 1;
-      if (tid == 0) h.ex_sc[s][2] = mine;
-      cluster_sync();
-      for (int r = 0; r < (int)crank; ++r) before += (long long)dsmem_ld_u64(dsmem_addr(&h.ex_sc[s][2], r));
+      const ulonglong2* px = cluster_push(c, crank, mine, 0ull);
+      for (int r = 0; r < (int)crank; ++r) before += (long long)px[r].x;
     }
     const long long want = min(max(need_eq - before, 0ll), (long long)mine);
     if (want == 0) {
@@ -1118,8 +1345,7 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
     if (lane < cnt) {
       const int slot = (qh + lane) & (kQueue - 1);
       const uint32_t j = qi[slot];
-      const float score = __fdiv_rn(qx[slot], Tr) + gumbel_noise(seed, off, j);
-      const unsigned long long pk = ((unsigned long long)f32_order_key(score) << 32) | (0xffffffffu - j);
+      const unsigned long long pk = race_key(seed, off, j, (m - qx[slot]) * l2t);
       bestg = pk > bestg ? pk : bestg;
     }
     __syncwarp();
@@ -1165,7 +1391,7 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
     if (qn > 0) drain(qn);
   }
   bestg = block_max_u64(bestg, h.red);
-  bestg = cluster_scalar<true>(c, bestg, 3);
+  bestg = cluster_scalar<true>(c, bestg);
   if (crank == 0 && tid == 0)
     a.token_ids[row_id] = bestg ? (int)(0xffffffffu - (uint32_t)(bestg & 0xffffffffull)) : imax;
   cluster_sync();               // peers may still read this CTA's shared memory
@@ -1218,17 +1444,24 @@ static cudaError_t launch_sample_t(const SampArgs& base, int num_rows, cudaStrea
   // the time as (waves of clusters the GPU co-schedules) x (ids per CTA)
   // and keep the cheapest, preferring the smaller cluster on a tie
   auto slice_of = [&](int c) { return ((base.V + c - 1) / c + align - 1) / align * align; };
+  auto al128 = [](size_t b) { return (b + 127) / 128 * 128; };
   const size_t budget = kMaxSmem - hdr - region;
   const size_t chunk_cap = (size_t)kMaxChunks * kChunkBytes;
   const size_t cap = budget < chunk_cap ? budget : chunk_cap;
+  // shared memory of a launch with cluster size c: the windowed 16-bit path
+  // takes all of it (the rest of the region holds candidate lists), the
+  // others header + slice + region
+  auto smem_of = [&](int c, bool res) -> size_t {
+    if (res && esz == 2) return (size_t)kMaxSmem;
+    return hdr + (res ? al128((size_t)slice_of(c) * esz) : 0) + region;
+  };
   int cs = 0;
   long long best_cost = 0;
   for (int c = 1; c <= kMaxCluster; c *= 2) {
-    const size_t sb = (size_t)slice_of(c) * esz;
+    const size_t sb = al128((size_t)slice_of(c) * esz);
     const bool res = base.vec && sb <= cap;
     if (!res && c < kMaxCluster) continue;
-    const size_t sm = hdr + region + (res ? sb : 0);
-    const int act = max_active_clusters<T>(c, sm, sms);
+    const int act = max_active_clusters<T>(c, smem_of(c, res), sms);
     const long long waves = ((long long)num_rows + act - 1) / act;
     const long long cost = waves * slice_of(c);
     if (cs == 0 || cost < best_cost) {
@@ -1238,10 +1471,11 @@ static cudaError_t launch_sample_t(const SampArgs& base, int num_rows, cudaStrea
   }
   SampArgs a = base;
   a.slice = slice_of(cs);
-  const size_t sbytes = (size_t)a.slice * esz;
+  const size_t sbytes = al128((size_t)a.slice * esz);
   a.resident = (a.vec && sbytes <= cap) ? 1 : 0;
-  a.fast = (esz == 2 && a.resident && a.slice < (1 << 24)) ? 1 : 0;
-  const size_t smem = hdr + region + (a.resident ? sbytes : 0);
+  a.fast = (esz == 2 && a.resident) ? 1 : 0;
+  const size_t smem = smem_of(cs, a.resident != 0);
+  a.list_cap = a.fast ? (int)((smem - hdr - sbytes) / 4) - win1_bins<T>() : 0;
   {
     cudaError_t e = cudaFuncSetAttribute(sample_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -1269,6 +1503,7 @@ cudaError_t launch_sample(int32_t* token_ids, const void* logits, int dtype, int
   const int esz = dtype == PKVD_F32 ? 4 : 2;
   SampArgs a;
   a.fast = 0;
+  a.list_cap = 0;
   a.token_ids = token_ids;
   a.logits = logits;
   a.V = vocab;

@@ -100,25 +100,15 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
     return cudaMemsetAsync(a.out, 0, (size_t)a.num_seqs * a.num_q_heads * a.head_dim * esz, stream);
   }
   // the merge kernel as a programmatic dependent of the partition kernel
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)a.num_seqs);
-  cfg.blockDim = dim3(256);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  const dim3 mg((unsigned)a.num_seqs), mb(256);
   if (a.dtype == PKVD_F32)
-    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<float>, static_cast<float*>(a.out), (const float*)rec,
-                              (const int32_t*)prefix, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
+    return launch_pdl(lse_merge_kernel<float>, mg, mb, 0, stream, static_cast<float*>(a.out), (const float*)rec,
+                      (const int32_t*)prefix, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
   if (a.dtype == PKVD_F16)
-    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<__half>, static_cast<__half*>(a.out), (const float*)rec,
-                              (const int32_t*)prefix, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
-  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<__nv_bfloat16>, static_cast<__nv_bfloat16*>(a.out),
-                            (const float*)rec, (const int32_t*)prefix, a.num_seqs, a.num_q_heads, a.head_dim,
-                            a.grid);
-  return cudaSuccess;
+    return launch_pdl(lse_merge_kernel<__half>, mg, mb, 0, stream, static_cast<__half*>(a.out), (const float*)rec,
+                      (const int32_t*)prefix, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
+  return launch_pdl(lse_merge_kernel<__nv_bfloat16>, mg, mb, 0, stream, static_cast<__nv_bfloat16*>(a.out),
+                    (const float*)rec, (const int32_t*)prefix, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
 }
 
 }  // namespace pkvd

@@ -409,6 +409,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cta = blockIdx.x, grid = gridDim.x;
+  pdl_wait();                       // the cache rows stored by the previous kernel
 
   // ---- scan the chunk counts: total, this CTA's slice, and its first row
   long long part = 0;
@@ -451,7 +452,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
     if (cta == 0 && tid == 0) p.prefix[p.num_seqs] = (int)C;
   }
   // the merge kernel may be scheduled now; it waits for this grid to finish
-  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (tid == 0) pdl_trigger();
   if (c0 >= c1) return;
 
   if (tid == 0) {
@@ -593,7 +594,8 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(T* __restrict__ out, con
                                                         int hq, int D, int grid) {
   __shared__ int s_rec[kMaxMergeRecords];
   __shared__ int s_n;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_wait();                       // the partition kernel's records
+  pdl_trigger();
   const int i = blockIdx.x;
   T* orow = out + (int64_t)i * hq * D;
   const long long C = prefix[num_seqs];
@@ -677,8 +679,7 @@ cudaError_t launch_partition(const PartParams& pp, int grid, size_t smem, cudaSt
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  kern<<<grid, kAttnThreads, smem, stream>>>(pp);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kAttnThreads), smem, stream, pp);
 }
 
 }  // namespace pkvd

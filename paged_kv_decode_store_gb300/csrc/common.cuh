@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pkvd.h"
 
 namespace pkvd {
@@ -67,6 +69,33 @@ template <> struct Vec16<__nv_bfloat16> {
 // --------------------------------------------------------------- errors
 __device__ __forceinline__ void flag_error(int32_t* err, int bits) {
   if (err) atomicOr(err, bits);
+}
+
+// ------------------------------------------- programmatic dependent launch
+// Every kernel of this library is launched with programmatic stream
+// serialization: it may be scheduled while its predecessor in the stream
+// still runs.  pdl_wait() returns once the predecessor grid has completed
+// and its writes are visible (at once when there is no such predecessor),
+// so each kernel calls it before touching memory another kernel may write;
+// pdl_trigger() lets the next kernel be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch with the programmatic stream serialization attribute set.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // ---------------------------------------------------------------- PTX

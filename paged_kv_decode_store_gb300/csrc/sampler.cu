@@ -564,6 +564,8 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
   uint32_t* q_idx = reinterpret_cast<uint32_t*>(region);
   float* q_x = reinterpret_cast<float*>(region + kSampWarps * kQueue * 4);
 
+  pdl_wait();                       // logits and parameters may come from the previous kernel
+  pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   Ctx c{&h, (int)cluster_size(), 0};
   const uint32_t crank = cluster_rank();
@@ -1485,13 +1487,15 @@ static cudaError_t launch_sample_t(const SampArgs& base, int num_rows, cudaStrea
   cfg.blockDim = dim3(kSampThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, sample_kernel<T>, a);
 }
 

@@ -17,6 +17,8 @@ namespace pkvd {
 __global__ void slot_mapping_kernel(int64_t* __restrict__ slots, const int32_t* __restrict__ tables,
                                     int max_blocks, const int32_t* __restrict__ ctx, int num_seqs,
                                     int block_size, int64_t num_blocks, int32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= num_seqs) return;
   const int c = ctx[i];
@@ -48,6 +50,8 @@ __global__ void kv_store_kernel(const uint8_t* __restrict__ k, const uint8_t* __
                                 int num_heads, int head_dim, int64_t block_stride,
                                 int64_t token_stride, int64_t head_stride, int elem_bytes,
                                 int32_t* err) {
+  pdl_trigger();
+  pdl_wait();                       // slots come from the slot-mapping kernel
   const int tok = blockIdx.x;
   const int64_t slot = slots[tok];
   if (slot < 0) return;
@@ -79,9 +83,8 @@ cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* tables, int max_b
                                 int64_t num_blocks, cudaStream_t stream, int32_t* err) {
   if (num_seqs == 0) return cudaSuccess;
   const int threads = 128;
-  slot_mapping_kernel<<<(num_seqs + threads - 1) / threads, threads, 0, stream>>>(
-      slots, tables, max_blocks, ctx, num_seqs, block_size, num_blocks, err);
-  return cudaGetLastError();
+  return launch_pdl(slot_mapping_kernel, dim3((num_seqs + threads - 1) / threads), dim3(threads), 0, stream, slots,
+                    tables, max_blocks, ctx, num_seqs, block_size, num_blocks, err);
 }
 
 cudaError_t launch_kv_store(const void* k, const void* v, const int64_t* slots, int num_tokens,
@@ -91,12 +94,10 @@ cudaError_t launch_kv_store(const void* k, const void* v, const int64_t* slots, 
   const int nvec = c.num_kv_heads * c.head_dim * elem_bytes / 16;
   int threads = 2 * nvec;
   threads = threads < 64 ? 64 : (threads > 256 ? 256 : threads);
-  kv_store_kernel<<<num_tokens, threads, 0, stream>>>(
-      static_cast<const uint8_t*>(k), static_cast<const uint8_t*>(v), slots,
-      static_cast<uint8_t*>(c.k_base), static_cast<uint8_t*>(c.v_base), c.num_blocks,
-      c.block_size, c.num_kv_heads, c.head_dim, c.block_stride, c.token_stride, c.head_stride,
-      elem_bytes, err);
-  return cudaGetLastError();
+  return launch_pdl(kv_store_kernel, dim3(num_tokens), dim3(threads), 0, stream, static_cast<const uint8_t*>(k),
+                    static_cast<const uint8_t*>(v), slots, static_cast<uint8_t*>(c.k_base),
+                    static_cast<uint8_t*>(c.v_base), c.num_blocks, c.block_size, c.num_kv_heads, c.head_dim,
+                    c.block_stride, c.token_stride, c.head_stride, elem_bytes, err);
 }
 
 }  // namespace pkvd

@@ -100,7 +100,8 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
     return cudaMemsetAsync(a.out, 0, (size_t)a.num_seqs * a.num_q_heads * a.head_dim * esz, stream);
   }
   // the merge kernel as a programmatic dependent of the partition kernel
-  const dim3 mg((unsigned)a.num_seqs), mb(256);
+  const int groups = (a.num_q_heads * (a.head_dim / 4) + 255) / 256;
+  const dim3 mg((unsigned)a.num_seqs, (unsigned)groups), mb(256);
   if (a.dtype == PKVD_F32)
     return launch_pdl(lse_merge_kernel<float>, mg, mb, 0, stream, static_cast<float*>(a.out), (const float*)rec,
                       (const int32_t*)prefix, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);

@@ -579,8 +579,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
 }
 
 // ------------------------------------------------------------ merge
-// One CTA per row, launched as a programmatic dependent of the partition
-// kernel: it waits for that grid, then combines the partial records of the
+// One CTA per row and group of 256 output float4 slices (blockIdx.y), so
+// rows with many heads spread over several SMs; launched as a programmatic
+// dependent of the partition kernel: it waits for that grid, then combines the partial records of the
 // CTAs whose slices cut the row (log-sum-exp identity), writes zeros for an
 // empty context, and leaves rows one CTA finished on its own untouched.
 //   M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  o = sum_s 2^(m_s - M) acc_s / L
@@ -602,7 +603,8 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(T* __restrict__ out, con
   const long long P = prefix[i];
   const long long n = prefix[i + 1] - P;
   if (n <= 0) {
-    for (int idx = threadIdx.x; idx < hq * D; idx += blockDim.x) orow[idx] = DT<T>::from_f(0.f);
+    for (int idx = blockIdx.y * blockDim.x + threadIdx.x; idx < hq * D; idx += gridDim.y * blockDim.x)
+      orow[idx] = DT<T>::from_f(0.f);
     return;
   }
   const int a = (int)(((P + 1) * grid - 1) / C);
@@ -624,7 +626,7 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(T* __restrict__ out, con
   const int nrec = s_n;
   const int Q = D / 4;
   constexpr int R = 8;
-  for (int idx = threadIdx.x; idx < hq * Q; idx += blockDim.x) {
+  for (int idx = blockIdx.y * blockDim.x + threadIdx.x; idx < hq * Q; idx += gridDim.y * blockDim.x) {
     const int h = idx / Q, d4 = (idx % Q) * 4;
     float M = -INFINITY, L = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);

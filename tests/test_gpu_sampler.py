@@ -207,3 +207,46 @@ def test_unaligned_rows_stochastic_match_oracle(dtype):
         if int(tok[i]) != ref and not _exempt(info, float(P[i])):
             bad += 1
     assert bad == 0
+
+
+def _branch_case(name):
+    """Full-width rows that steer the 16-bit windowed path into each of its
+    branches: the first-window list overflowing, a nucleus cut past the
+    first window (second counting stage), top-k with nucleus and a tie
+    group resolved from the tie list, and a tie group too large for it."""
+    rng = np.random.default_rng(17)
+    R, V = 6, 151936
+    if name == "list_overflow":            # every id within two binades of the max
+        x = 8.0 + 0.5 * rng.standard_normal((R, V))
+        return torch.from_numpy(x.astype(np.float32)).to(torch.float16), 1.0, 0, 0.9
+    if name == "second_stage":             # nearly flat weights: the cut lies ~5 binades below the max
+        x = np.exp2(rng.uniform(-7.0, 3.0, (R, V)))
+        return torch.from_numpy(x.astype(np.float32)).to(torch.float16), 50.0, 0, 0.6
+    if name == "topk_nucleus_ties":        # bf16 with many equal values near the k-th
+        x = np.round(2.0 * rng.standard_normal((R, V)), 1)
+        return torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16), 1.0, 300, 0.9
+    if name == "huge_tie_group":           # 50k ids at the k-th value
+        x = np.full((R, V), -3.0)
+        x[:, rng.choice(V, 50_000, replace=False)] = 1.0
+        for r in range(R):
+            x[r, rng.choice(V, 20, replace=False)] = 2.0
+        return torch.from_numpy(x.astype(np.float32)).to(torch.float16), 1.0, 1000, 1.0
+    raise KeyError(name)
+
+
+@pytest.mark.parametrize("name", ["list_overflow", "second_stage", "topk_nucleus_ties", "huge_tie_group"])
+def test_windowed_path_branches_match_oracle(name):
+    pk = require_gpu()
+    logits, T, k, p = _branch_case(name)
+    R = logits.shape[0]
+    seeds = torch.arange(1, R + 1, dtype=torch.int64) * 7919
+    offs = torch.arange(R, dtype=torch.int64) * 3
+    tok = pk.sample(logits.to(DEV), torch.full((R,), T, device=DEV), torch.full((R,), k, dtype=torch.int32, device=DEV),
+                    torch.full((R,), p, device=DEV), seeds.to(DEV), offs.to(DEV)).cpu().numpy()
+    bad = 0
+    for i in range(R):
+        ref, info = oracle.sampler.sample_row(logits[i].double().numpy(), float(np.float32(T)), k,
+                                              float(np.float32(p)), int(seeds[i]), int(offs[i]), return_info=True)
+        if int(tok[i]) != ref and not _exempt(info, float(np.float32(p))):
+            bad += 1
+    assert bad == 0

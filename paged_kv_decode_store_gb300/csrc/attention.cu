@@ -100,16 +100,18 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
     return cudaMemsetAsync(a.out, 0, (size_t)a.num_seqs * a.num_q_heads * a.head_dim * esz, stream);
   }
   // the merge kernel as a programmatic dependent of the partition kernel
+  const long long cap_all = (long long)a.max_blocks_per_seq * a.block_size;
+  const int ctx_cap = (int)(cap_all < a.max_context_len ? cap_all : a.max_context_len);
   const int groups = (a.num_q_heads * (a.head_dim / 4) + 255) / 256;
   const dim3 mg((unsigned)a.num_seqs, (unsigned)groups), mb(256);
   if (a.dtype == PKVD_F32)
     return launch_pdl(lse_merge_kernel<float>, mg, mb, 0, stream, static_cast<float*>(a.out), (const float*)rec,
-                      (const int32_t*)prefix, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
+                      a.context_lens, ctx_cap, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
   if (a.dtype == PKVD_F16)
     return launch_pdl(lse_merge_kernel<__half>, mg, mb, 0, stream, static_cast<__half*>(a.out), (const float*)rec,
-                      (const int32_t*)prefix, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
+                      a.context_lens, ctx_cap, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
   return launch_pdl(lse_merge_kernel<__nv_bfloat16>, mg, mb, 0, stream, static_cast<__nv_bfloat16*>(a.out),
-                    (const float*)rec, (const int32_t*)prefix, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
+                    (const float*)rec, a.context_lens, ctx_cap, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
 }
 
 }  // namespace pkvd

@@ -591,25 +591,54 @@ constexpr int kMaxMergeRecords = 1024;     // >= any partition grid (one CTA per
 
 template <typename T>
 __global__ void __launch_bounds__(256) lse_merge_kernel(T* __restrict__ out, const float* __restrict__ rec,
-                                                        const int32_t* __restrict__ prefix, int num_seqs,
-                                                        int hq, int D, int grid) {
+                                                        const int32_t* __restrict__ ctx, int ctx_cap,
+                                                        int num_seqs, int hq, int D, int grid) {
   __shared__ int s_rec[kMaxMergeRecords];
   __shared__ int s_n;
-  pdl_wait();                       // the partition kernel's records
-  pdl_trigger();
+  __shared__ long long s_part[2][8];
   const int i = blockIdx.x;
+  // Row i's chunk range [P, P + n) and the total C from the context lengths.
+  // They are inputs of the call, complete before the partition kernel (which
+  // waited for its own predecessor first) let this grid start, so this part
+  // overlaps the partition kernel; records are read after pdl_wait().
+  long long before = 0, all = 0;
+  for (int r = threadIdx.x; r < num_seqs; r += blockDim.x) {
+    const int c = chunks_of(ctx, r, ctx_cap);
+    all += c;
+    if (r < i) before += c;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    before += __shfl_xor_sync(FULL_MASK, before, o);
+    all += __shfl_xor_sync(FULL_MASK, all, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    s_part[0][threadIdx.x >> 5] = before;
+    s_part[1][threadIdx.x >> 5] = all;
+  }
+  __syncthreads();
+  long long P = 0, C = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    P += s_part[0][w];
+    C += s_part[1][w];
+  }
+  const long long n = chunks_of(ctx, i, ctx_cap);
   T* orow = out + (int64_t)i * hq * D;
-  const long long C = prefix[num_seqs];
-  const long long P = prefix[i];
-  const long long n = prefix[i + 1] - P;
   if (n <= 0) {
+    pdl_wait();
+    pdl_trigger();
     for (int idx = blockIdx.y * blockDim.x + threadIdx.x; idx < hq * D; idx += gridDim.y * blockDim.x)
       orow[idx] = DT<T>::from_f(0.f);
     return;
   }
   const int a = (int)(((P + 1) * grid - 1) / C);
   const int b = (int)(((P + n) * grid - 1) / C);
-  if (a == b) return;
+  if (a == b) {                     // written by one CTA on its own
+    pdl_wait();
+    pdl_trigger();
+    return;
+  }
   if (threadIdx.x == 0) {
     // CTA a's slice starts at or before P (its record of this row is its
     // last segment unless it starts exactly at P); later CTAs start inside
@@ -624,6 +653,8 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(T* __restrict__ out, con
   }
   __syncthreads();
   const int nrec = s_n;
+  pdl_wait();                       // the partition kernel's records
+  pdl_trigger();
   const int Q = D / 4;
   constexpr int R = 8;
   for (int idx = blockIdx.y * blockDim.x + threadIdx.x; idx < hq * Q; idx += gridDim.y * blockDim.x) {

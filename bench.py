@@ -232,25 +232,26 @@ def time_attention(step, flush, steps, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
-def time_e2e(step, host_pinned, flush, steps, stream):
-    """Public-API step with host buffers: H2D inputs, replay, D2H outputs."""
-    out_host = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
-    tok_host = torch.empty(step.token_ids.shape, dtype=torch.int32, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in host_pinned.values())
-    d2h = out_host.numel() * out_host.element_size() + tok_host.numel() * 4
+def time_e2e(step, host_inputs, flush, steps, stream):
+    """Public-API step with host buffers: one graph holds the H2D copy of the
+    step's inputs (pinned arena), the logits' H2D copy on a second stream
+    beside the store and attention kernels (which do not read them), the
+    kernels, and the D2H copy of out and token ids."""
+    h = step.host_buffers()
+    for k, t in host_inputs.items():
+        h[k].copy_(t)
+    step.capture_host()
+    h2d = h["_in"].numel() + h["logits"].numel() * h["logits"].element_size()
+    d2h = h["_out"].numel()
     times = []
     for i in range(steps):
         flush.add_(1)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for k, t in host_pinned.items():
-            getattr(step, k).copy_(t, non_blocking=True)
-        step.replay()
-        out_host.copy_(step.out, non_blocking=True)
-        tok_host.copy_(step.token_ids, non_blocking=True)
+        step.replay_host()
         torch.cuda.current_stream().synchronize()
         times.append((time.perf_counter() - t0) * 1e3)
-    return times, h2d, d2h
+    return times, h2d, d2h, h
 
 
 # ----------------------------------------------------------------- oracle arm
@@ -431,10 +432,12 @@ def main():
     attn_mean = max_over_ranks(statistics.mean(attn_ms), ws, dev)
     clocks = clk.summary()
 
-    pinned = {k: (v.cpu().pin_memory()) for k, v in host.items()}
+    pinned = {k: v.cpu() for k, v in host.items()}
     for _ in range(2):
         time_e2e(step, pinned, flush, 1, stream)
-    e2e_ms, h2d, d2h = time_e2e(step, pinned, flush, args.steps, stream)
+    e2e_ms, h2d, d2h, hb = time_e2e(step, pinned, flush, args.steps, stream)
+    if not torch.equal(hb["token_ids"], step.token_ids.cpu()):
+        raise RuntimeError("host-staged step disagrees with the device step")
     e2e_total = max_over_ranks(sum(e2e_ms), ws, dev)
     err = int(step.err.item())
 

@@ -34,20 +34,26 @@ class DecodeStep:
         self.scale = float(scale)
         self.path = path
         dt = k_cache.dtype
-        self.q = torch.zeros(B, Hq, D, dtype=dt, device=dev)
-        self.k_new = torch.zeros(B, Hkv, D, dtype=dt, device=dev)
-        self.v_new = torch.zeros(B, Hkv, D, dtype=dt, device=dev)
-        self.block_tables = torch.full((B, max_blocks_per_seq), -1, dtype=torch.int32, device=dev)
-        self.context_lens = torch.zeros(B, dtype=torch.int32, device=dev)
+        # Per-step inputs and outputs live in two byte arenas (256-byte aligned
+        # views), so a host-staged step moves each side with one copy.
+        ins = [("q", (B, Hq, D), dt), ("k_new", (B, Hkv, D), dt), ("v_new", (B, Hkv, D), dt),
+               ("block_tables", (B, max_blocks_per_seq), torch.int32), ("context_lens", (B,), torch.int32),
+               ("temperature", (B,), torch.float32), ("top_k", (B,), torch.int32),
+               ("top_p", (B,), torch.float32), ("seeds", (B,), torch.int64), ("offsets", (B,), torch.int64)]
+        outs = [("out", (B, Hq, D), dt), ("token_ids", (B,), torch.int32)]
+        self._in_layout, in_bytes = _arena_layout(ins)
+        self._out_layout, out_bytes = _arena_layout(outs)
+        self.inputs = torch.zeros(in_bytes, dtype=torch.uint8, device=dev)
+        self.outputs = torch.zeros(out_bytes, dtype=torch.uint8, device=dev)
+        for name, view in _arena_views(self.inputs, self._in_layout).items():
+            setattr(self, name, view)
+        for name, view in _arena_views(self.outputs, self._out_layout).items():
+            setattr(self, name, view)
+        self.block_tables.fill_(-1)
+        self.temperature.fill_(1.0)
+        self.top_p.fill_(1.0)
         self.slots = torch.empty(B, dtype=torch.int64, device=dev)
-        self.out = torch.empty(B, Hq, D, dtype=dt, device=dev)
         self.logits = torch.zeros(B, vocab, dtype=logits_dtype, device=dev)
-        self.temperature = torch.ones(B, dtype=torch.float32, device=dev)
-        self.top_k = torch.zeros(B, dtype=torch.int32, device=dev)
-        self.top_p = torch.ones(B, dtype=torch.float32, device=dev)
-        self.seeds = torch.zeros(B, dtype=torch.int64, device=dev)
-        self.offsets = torch.zeros(B, dtype=torch.int64, device=dev)
-        self.token_ids = torch.empty(B, dtype=torch.int32, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         nbytes = ctypes.c_size_t(0)
         _capi.check(_capi.lib().pkvd_decode_workspace_bytes(B, Hq, D, max_context_len, 0,
@@ -55,11 +61,16 @@ class DecodeStep:
         self.workspace = torch.zeros(max(int(nbytes.value), 16), dtype=torch.uint8, device=dev)
         self.cache = _capi.cache_desc(k_cache, v_cache)
         self.graph = None
+        self.host_graph = None
         self.kernels_per_step = 5     # slot, store, partition, merge, sample
 
     def enqueue(self, stream=None) -> None:
         L = _capi.lib()
         s = _capi.stream_handle(stream, self.q)
+        self._enqueue_kv_attention(L, s)
+        self._enqueue_sample(L, s)
+
+    def _enqueue_kv_attention(self, L, s) -> None:
         p = _capi.ptr
         _capi.check(L.pkvd_slot_mapping(p(self.slots), p(self.block_tables), self.block_tables.shape[1],
                                         p(self.context_lens), self.B, self.bs, self.nb, s, p(self.err)))
@@ -70,6 +81,9 @@ class DecodeStep:
             self.block_tables.shape[1], p(self.context_lens), self.max_context_len, self.B, self.Hq,
             ctypes.c_float(self.scale), p(self.workspace), self.workspace.numel(), s, p(self.err),
             self.path))
+
+    def _enqueue_sample(self, L, s) -> None:
+        p = _capi.ptr
         V = self.logits.shape[1]
         _capi.check(L.pkvd_sample(p(self.token_ids), p(self.logits), _capi.dtype_code(self.logits.dtype),
                                   self.B, V, self.logits.stride(0), p(self.temperature), p(self.top_k),
@@ -93,3 +107,73 @@ class DecodeStep:
             self.enqueue()
         else:
             self.graph.replay()
+
+    # ------------------------------------------------ host-staged steps
+    def host_buffers(self) -> dict:
+        """Pinned host tensors shaped like the step's inputs and outputs
+        (views of pinned arenas with the device arenas' layout), plus the
+        logits: fill the inputs, call replay_host(), read out / token_ids."""
+        if getattr(self, "_host", None) is None:
+            hin = torch.zeros(self.inputs.numel(), dtype=torch.uint8, pin_memory=True)
+            hout = torch.zeros(self.outputs.numel(), dtype=torch.uint8, pin_memory=True)
+            h = {"_in": hin, "_out": hout,
+                 "logits": torch.zeros(self.logits.shape, dtype=self.logits.dtype, pin_memory=True)}
+            h.update(_arena_views(hin, self._in_layout))
+            h.update(_arena_views(hout, self._out_layout))
+            self._host = h
+        return self._host
+
+    def _enqueue_host(self) -> None:
+        h = self.host_buffers()
+        cur = torch.cuda.current_stream(self.q.device)
+        self.inputs.copy_(h["_in"], non_blocking=True)
+        # the logits are read by the sampler only: their copy runs on a
+        # second stream, beside the store and attention kernels
+        side = self._side
+        side.wait_stream(cur)
+        with torch.cuda.stream(side):
+            self.logits.copy_(h["logits"], non_blocking=True)
+        L = _capi.lib()
+        s = _capi.stream_handle(None, self.q)
+        self._enqueue_kv_attention(L, s)
+        cur.wait_stream(side)
+        self._enqueue_sample(L, s)
+        h["_out"].copy_(self.outputs, non_blocking=True)
+
+    def capture_host(self) -> None:
+        """Record a host-staged step (one input copy, the logits copy on a
+        second stream, the kernels, one output copy) into a CUDA graph."""
+        self._side = torch.cuda.Stream(device=self.q.device)
+        warm = torch.cuda.Stream(device=self.q.device)
+        warm.wait_stream(torch.cuda.current_stream(self.q.device))
+        with torch.cuda.stream(warm):
+            self._enqueue_host()
+        torch.cuda.current_stream(self.q.device).wait_stream(warm)
+        torch.cuda.synchronize(self.q.device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self._enqueue_host()
+        self.host_graph = g
+
+    def replay_host(self) -> None:
+        """One host-staged step; the host outputs are valid once the
+        current stream has synchronised."""
+        if self.host_graph is None:
+            self.capture_host()
+        self.host_graph.replay()
+
+
+def _arena_layout(fields):
+    layout, off = [], 0
+    for name, shape, dtype in fields:
+        n = 1
+        for d in shape:
+            n *= d
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        layout.append((name, shape, dtype, off, nbytes))
+        off += (nbytes + 255) // 256 * 256
+    return layout, max(off, 256)
+
+
+def _arena_views(arena: torch.Tensor, layout) -> dict:
+    return {name: arena[off:off + nbytes].view(dtype).view(shape) for name, shape, dtype, off, nbytes in layout}

@@ -145,6 +145,14 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
   return c;
 }
 
+// 2^x on the special-function unit with results below 2^-126 flushed to
+// zero (each such term is under 2^-126 of the max term, which is 1)
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // E_j = -ln u_j for id j's uniform: word (j mod 4) of Philox4x32-10 at
 // counter (j / 4, offset), u = ((w >> 9) + 1/2) 2^-23, exact in f32 and
 // strictly inside (0, 1), so E_j > 0 (accurate near u = 1, where it is tiny)
@@ -163,7 +171,7 @@ __device__ __forceinline__ float exp_noise(uint64_t seed, uint64_t offset, uint3
 // that can win.  The packed key makes the smallest race time the largest
 // key, and the lowest id the winner among equal times.  d2 = (m - x) / (T ln 2).
 __device__ __forceinline__ unsigned long long race_key(uint64_t seed, uint64_t offset, uint32_t j, float d2) {
-  const float t = exp_noise(seed, offset, j) * exp2f(d2);
+  const float t = exp_noise(seed, offset, j) * ex2_ftz(d2);
   return ((unsigned long long)(uint32_t)~f32_order_key(t) << 32) | (0xffffffffu - j);
 }
 
@@ -708,7 +716,7 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const float2 f = Pack2<T>::to_float2(w[q]);
-              vs += exp2f(fmaf(f.x, l2t, -ml2t)) + exp2f(fmaf(f.y, l2t, -ml2t));
+              vs += ex2_ftz(fmaf(f.x, l2t, -ml2t)) + ex2_ftz(fmaf(f.y, l2t, -ml2t));
             }
             zadd(vs);
           }
@@ -716,7 +724,7 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
         for (int j = rest + tid; j < n; j += kSampThreads) {
           const uint32_t b = bits_at(j);
           hits += K::key(b) >= k1;
-          if (need_z) zadd(exp2f((K::value(b) - mr) * l2t));
+          if (need_z) zadd(ex2_ftz((K::value(b) - mr) * l2t));
         }
         unsigned long long tot_u;
         const int first = (int)block_excl_scan_u64((unsigned long long)hits, h.red, tot_u);
@@ -763,7 +771,7 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
         }
         __syncthreads();                                  // gap[] and zsum visible
         const unsigned long long zrow = h.zsum;
-        auto wfix = [&](float x) -> unsigned long long { return fixed_weight(exp2f((x - m) * l2t)); };
+        auto wfix = [&](float x) -> unsigned long long { return fixed_weight(ex2_ftz((x - m) * l2t)); };
         int covered = kWin1;
         // the second stage: the bins it writes were never read (they held
         // the list), so peers may still be walking the first window

@@ -22,7 +22,7 @@
 namespace pkvd {
 
 // 16 MiB: enough for every shape this library supports up to a few thousand
-// rows x 64 query heads (the largest benchmark shape needs about 10.4 MB).
+// rows x 64 query heads (the largest benchmark shape needs about 10.3 MB).
 constexpr size_t kNoAllocScratchBytes = 16u << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

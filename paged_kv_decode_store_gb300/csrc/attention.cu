@@ -7,10 +7,6 @@ namespace pkvd {
 namespace {
 constexpr int kMaxDynSmem = 232448;    // 227 KB opt-in per CTA on sm_100-family parts
 
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-size_t prefix_bytes(int num_seqs) { return align_up(sizeof(int32_t) * ((size_t)num_seqs + 1), 256); }
-
 int elem_bytes(int dtype) { return dtype == PKVD_F32 ? 4 : 2; }
 
 int stage_count(int dtype, int head_dim, int num_kv_heads) {
@@ -32,7 +28,8 @@ int attention_grid(int num_seqs, int max_context_len, int sm_count) {
 }
 
 size_t attention_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int grid) {
-  return prefix_bytes(num_seqs) + (size_t)grid * 2 * num_q_heads * (head_dim + 4) * sizeof(float);
+  (void)num_seqs;
+  return (size_t)grid * 2 * num_q_heads * (head_dim + 4) * sizeof(float);
 }
 
 bool attention_path_supported(int path, int dtype, int head_dim, int num_kv_heads, int group) {
@@ -54,8 +51,7 @@ int attention_default_path(int dtype, int head_dim, int num_kv_heads, int group)
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   const int esz = elem_bytes(a.dtype);
   const int G = a.num_q_heads / a.num_kv_heads;
-  int32_t* prefix = static_cast<int32_t*>(a.workspace);
-  float* rec = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + prefix_bytes(a.num_seqs));
+  float* rec = static_cast<float*>(a.workspace);
   if (a.grid > 0) {
     PartParams pp;
     pp.out = a.out;
@@ -78,7 +74,6 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
     pp.num_seqs = a.num_seqs;
     pp.scale_log2 = a.scale * 1.4426950408889634f;
     pp.rec = rec;
-    pp.prefix = prefix;
     pp.err = a.err;
     pp.stages = stage_count(a.dtype, a.head_dim, a.num_kv_heads);
     pp.row_bytes = a.num_kv_heads * a.head_dim * esz;

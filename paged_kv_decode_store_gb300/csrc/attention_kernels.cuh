@@ -59,8 +59,7 @@ struct PartParams {
   int ctx_cap;
   int num_seqs;
   float scale_log2;
-  float* rec;          // partial records [grid][2][hq][D + 4]: acc[D], m, l, pad
-  int32_t* prefix;     // [num_seqs + 1] chunk prefix sums (written by CTA 0)
+  float* rec;          // partial records [grid][2][hq][D + 4]: acc[D], m, l, pad (the workspace)
   int32_t* err;
   int stages;
   int rowb;            // padded smem bytes of one token row (all heads)
@@ -412,23 +411,46 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
   pdl_wait();                       // the cache rows stored by the previous kernel
 
   // ---- scan the chunk counts: total, this CTA's slice, and its first row
-  long long part = 0;
-  for (int i = tid; i < p.num_seqs; i += kAttnThreads) part += chunks_of(p.ctx, i, p.ctx_cap);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(FULL_MASK, part, o);
+  // (every CTA computes the same scan; CTA 0 flags bad lengths)
   if (tid == 0) {
-    hdr.total = 0;
     hdr.found_seq = -1;
     hdr.found_off = 0;
     hdr.abort_flag = 0;
   }
-  __syncthreads();
-  if (lane == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&hdr.total), (unsigned long long)part);
-  __syncthreads();
-  const long long C = hdr.total;
-  const long long c0 = slice_begin(C, cta, grid), c1 = slice_begin(C, cta + 1, grid);
-  if (c0 >= c1 && cta != 0) return;
-  {
+  long long C, c0, c1;
+  if (p.num_seqs <= kAttnThreads) {
+    // one row per thread: a single block scan gives the total and the row offsets
+    const int i = tid;
+    const int n = i < p.num_seqs ? chunks_of(p.ctx, i, p.ctx_cap) : 0;
+    if (cta == 0 && i < p.num_seqs) {
+      const int raw = p.ctx[i];
+      if (raw < 0 || raw > p.ctx_cap) flag_error(p.err, PKVD_ERR_CONTEXT);
+    }
+    int total;
+    const int incl = block_incl_scan(n, hdr.scan_warp, total);   // also orders the header writes
+    C = total;
+    c0 = slice_begin(C, cta, grid);
+    c1 = slice_begin(C, cta + 1, grid);
+    if (c0 >= c1 && cta != 0) return;
+    const int excl = incl - n;
+    if (n > 0 && excl <= c0 && c0 < excl + n) {
+      hdr.found_seq = i;
+      hdr.found_off = (int)(c0 - excl);
+    }
+    __syncthreads();
+  } else {
+    long long part = 0;
+    for (int i = tid; i < p.num_seqs; i += kAttnThreads) part += chunks_of(p.ctx, i, p.ctx_cap);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(FULL_MASK, part, o);
+    if (tid == 0) hdr.total = 0;
+    __syncthreads();
+    if (lane == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&hdr.total), (unsigned long long)part);
+    __syncthreads();
+    C = hdr.total;
+    c0 = slice_begin(C, cta, grid);
+    c1 = slice_begin(C, cta + 1, grid);
+    if (c0 >= c1 && cta != 0) return;
     int running = 0;
     for (int base = 0; base < p.num_seqs; base += kAttnThreads) {
       const int i = base + tid;
@@ -437,7 +459,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
       const int incl = block_incl_scan(n, hdr.scan_warp, total);
       const int excl = running + incl - n;
       if (cta == 0 && i < p.num_seqs) {
-        p.prefix[i] = excl;
         const int raw = p.ctx[i];
         if (raw < 0 || raw > p.ctx_cap) flag_error(p.err, PKVD_ERR_CONTEXT);
       }
@@ -449,7 +470,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
       __syncthreads();
       if (cta != 0 && hdr.found_seq >= 0) break;
     }
-    if (cta == 0 && tid == 0) p.prefix[p.num_seqs] = (int)C;
   }
   // the merge kernel may be scheduled now; it waits for this grid to finish
   if (tid == 0) pdl_trigger();

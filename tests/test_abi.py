@@ -78,12 +78,11 @@ def test_workspace_query_is_host_only(L):
     n = ctypes.c_size_t(0)
     assert L.pkvd_decode_workspace_bytes(32, 48, 128, 2048, 152, ctypes.byref(n)) == 0
     grid = min(152, 32 * 128)
-    prefix = ((33 * 4 + 255) // 256) * 256
-    assert n.value == prefix + grid * 2 * 48 * 132 * 4
+    assert n.value == grid * 2 * 48 * 132 * 4                # partial records [grid][2][Hq][D + 4] fp32
     assert L.pkvd_decode_workspace_bytes(4, 4, 64, 50, 152, ctypes.byref(n)) == 0
-    assert n.value == 256 + min(152, 4 * 4) * 2 * 4 * 68 * 4          # prefix 5 x 4 B -> 256
+    assert n.value == min(152, 4 * 4) * 2 * 4 * 68 * 4
     assert L.pkvd_decode_workspace_bytes(4, 4, 64, 0, 152, ctypes.byref(n)) == 0
-    assert n.value == 256
+    assert n.value == 0                                      # no context: nothing to combine
     assert L.pkvd_decode_workspace_bytes(-1, 4, 64, 50, 152, ctypes.byref(n)) == 1
 
 

@@ -65,10 +65,10 @@ def test_noalloc_matches_workspace_entry_point_twice(cfg):
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     pk, w, lay, kc, vc, tables, ctx = _inputs(configs.GROK1.scaled(num_seqs=2, ctx_args=(64,), vocab=2048))
-    big_seqs = 1 << 23                             # its row table alone exceeds the built-in scratch
+    big_seqs, big_heads = 4096, 128                # 128 query heads: records beyond the scratch
     from paged_kv_decode_store_gb300 import _capi
     c = _capi.cache_desc(kc, vc)
-    assert pk.decode_workspace_bytes(big_seqs, 48, 128, 64) > 16 << 20
+    assert pk.decode_workspace_bytes(big_seqs, big_heads, 128, 64) > 16 << 20
     st = pk.lib().pkvd_paged_decode_attention_noalloc(
-        0, 0, ctypes.byref(c), 0, 1, 0, 64, big_seqs, 48, ctypes.c_float(0.1), None, None)
+        0, 0, ctypes.byref(c), 0, 1, 0, 64, big_seqs, big_heads, ctypes.c_float(0.1), None, None)
     assert st == 4                                 # PKVD_WORKSPACE_TOO_SMALL, nothing enqueued

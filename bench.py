@@ -59,7 +59,6 @@ class L2Flush:
     def add_(self, _):
         self.wbuf.add_(1)
         torch.sum(self.rbuf, dim=0, out=self.sink)
-KERNELS_PER_STEP = 5            # slot mapping, kv store, partition, merge, sampler
 
 
 # ----------------------------------------------------------------- bytes
@@ -465,7 +464,7 @@ def main():
                      "peak_source": peak_src, "traffic": recorded_traffic(cfg.name)},
         "e2e": {"value": ws * nbytes["step"] / (e2e_total / args.steps * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_total / args.steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": KERNELS_PER_STEP * args.steps + 2 * args.steps,
+        "gpu_launches": step.kernels_per_step * args.steps + 2 * args.steps,
         "clocks": clocks, "device_err_flag": err,
     }
     if not args.no_cpu_baseline and ws == 1:

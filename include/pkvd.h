@@ -134,6 +134,25 @@ pkvd_status pkvd_kv_store(const void* k, const void* v, const int64_t* slot_mapp
                           int32_t* err_flag);
 
 /*
+ * pkvd_kv_store_paged -- pkvd_slot_mapping and pkvd_kv_store in one kernel
+ * (same passages as those two): row i's new K and V rows go to the slot of
+ * its newest token, found from block_tables and context_lens as in
+ * pkvd_slot_mapping, and the slot is also written to slot_mapping[i] when
+ * slot_mapping is not NULL.  Rows with context_lens[i] == 0 are skipped
+ * (slot -1).  One launch instead of two for a decode step that needs the
+ * slots nowhere else.
+ * Inputs: k, v [num_seqs, num_kv_heads, head_dim] contiguous, cache dtype,
+ *         16-byte aligned; block_tables int32 [num_seqs, max_blocks_per_seq];
+ *         context_lens int32 [num_seqs] (include the new token).
+ * Output: the cache rows; slot_mapping int64 [num_seqs] or NULL.
+ * Device errors: as pkvd_slot_mapping (bad block id or length: row skipped).
+ */
+pkvd_status pkvd_kv_store_paged(const void* k, const void* v, const int32_t* block_tables,
+                                int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                int32_t num_seqs, int64_t* slot_mapping, const pkvd_cache* cache,
+                                void* stream, int32_t* err_flag);
+
+/*
  * Workspace bytes pkvd_paged_decode_attention needs for these sizes on a
  * GPU with `sm_count` SMs (sm_count <= 0: query the current device).
  * Host only; returns PKVD_CUDA_ERROR if the device query fails.

@@ -23,7 +23,7 @@ from ._capi import (LIB_PATH, PATH_AUTO, PATH_FMA, PATH_MMA, ERR_BLOCK_ID, ERR_S
                     stream_handle, cache_desc, ptr)
 from .step import DecodeStep  # noqa: F401
 
-__all__ = ["slot_mapping", "kv_store", "paged_decode_attention", "decode_workspace_bytes",
+__all__ = ["slot_mapping", "kv_store", "kv_store_paged", "paged_decode_attention", "decode_workspace_bytes",
            "sample", "DecodeStep", "PkvdError", "lib"]
 
 
@@ -52,6 +52,18 @@ def kv_store(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
     c = cache_desc(k_cache, v_cache)
     check(lib().pkvd_kv_store(ptr(k), ptr(v), ptr(slot_mapping), k.shape[0], ctypes.byref(c),
                               stream_handle(stream, k), _err_ptr(err)))
+
+
+def kv_store_paged(k: torch.Tensor, v: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                   k_cache: torch.Tensor, v_cache: torch.Tensor, slot_mapping: torch.Tensor | None = None,
+                   err: torch.Tensor | None = None, stream=None) -> None:
+    """Slot mapping and store in one kernel: row i's k[i], v[i] go to the slot of
+    its newest token (context_lens[i] - 1 through block_tables[i]); the slots are
+    also written to slot_mapping (int64 [B]) when it is given."""
+    c = cache_desc(k_cache, v_cache)
+    check(lib().pkvd_kv_store_paged(ptr(k), ptr(v), ptr(block_tables), block_tables.shape[1],
+                                    ptr(context_lens), k.shape[0], ptr(slot_mapping), ctypes.byref(c),
+                                    stream_handle(stream, k), _err_ptr(err)))
 
 
 def decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int, max_context_len: int,

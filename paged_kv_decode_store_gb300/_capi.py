@@ -37,6 +37,8 @@ SIGNATURES = {
                                     c_void_p, c_void_p]),
     "pkvd_kv_store": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, ctypes.POINTER(PkvdCache),
                                 c_void_p, c_void_p]),
+    "pkvd_kv_store_paged": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_int32, c_void_p,
+                                      ctypes.POINTER(PkvdCache), c_void_p, c_void_p]),
     "pkvd_decode_workspace_bytes": (c_int32, [c_int32, c_int32, c_int32, c_int32, c_int32,
                                               ctypes.POINTER(c_size_t)]),
     "pkvd_paged_decode_attention": (c_int32, [c_void_p, c_void_p, ctypes.POINTER(PkvdCache), c_void_p,

@@ -93,6 +93,21 @@ pkvd_status pkvd_kv_store(const void* k, const void* v, const int64_t* slot_mapp
                                    static_cast<cudaStream_t>(stream), err_flag));
 }
 
+pkvd_status pkvd_kv_store_paged(const void* k, const void* v, const int32_t* block_tables,
+                                int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                                int64_t* slot_mapping, const pkvd_cache* cache, void* stream,
+                                int32_t* err_flag) {
+  if (num_seqs < 0) return PKVD_INVALID_ARG;
+  const pkvd_status cs = check_cache(cache, false);
+  if (cs != PKVD_OK) return cs;
+  if (num_seqs == 0) return PKVD_OK;
+  if (!k || !v || !block_tables || !context_lens || max_blocks_per_seq <= 0) return PKVD_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v)) return PKVD_UNSUPPORTED_SHAPE;
+  return from_cuda(launch_kv_store_paged(k, v, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                                         slot_mapping, *cache, esize(cache->dtype),
+                                         static_cast<cudaStream_t>(stream), err_flag));
+}
+
 pkvd_status pkvd_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                         int32_t max_context_len, int32_t sm_count, size_t* bytes) {
   if (!bytes || num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0) return PKVD_INVALID_ARG;

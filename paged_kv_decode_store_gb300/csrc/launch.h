@@ -54,6 +54,9 @@ cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* tables, int max_b
 cudaError_t launch_kv_store(const void* k, const void* v, const int64_t* slots, int num_tokens,
                             const pkvd_cache& c, int elem_bytes, cudaStream_t stream,
                             int32_t* err);
+cudaError_t launch_kv_store_paged(const void* k, const void* v, const int32_t* tables, int max_blocks,
+                                  const int32_t* ctx, int num_seqs, int64_t* slots_out, const pkvd_cache& c,
+                                  int elem_bytes, cudaStream_t stream, int32_t* err);
 
 cudaError_t launch_sample(int32_t* token_ids, const void* logits, int dtype, int num_rows,
                           int vocab, int64_t row_stride, const float* temperature,

@@ -1,4 +1,5 @@
-// Slot mapping and the paged KV-cache store.
+// Slot mapping and the paged KV-cache store (separately, or fused into one
+// kernel for callers that need no slot mapping in between).
 //
 // nano-vllm "Model Runner" notes, sections "prefill and decode" and
 // "allocated kv cache": the token decoded now is position context_len - 1;
@@ -14,6 +15,31 @@
 
 namespace pkvd {
 
+// Slot of row i's newest token, or -1 (empty row or a bad length / block id,
+// which is flagged).
+__device__ __forceinline__ int64_t decode_slot(const int32_t* __restrict__ tables, int max_blocks,
+                                               const int32_t* __restrict__ ctx, int i, int block_size,
+                                               int64_t num_blocks, int32_t* err) {
+  const int c = ctx[i];
+  if (c < 0) {
+    flag_error(err, PKVD_ERR_CONTEXT);
+    return -1;
+  }
+  if (c == 0) return -1;
+  const int pos = c - 1;
+  const int logical = pos / block_size;
+  if (logical >= max_blocks) {
+    flag_error(err, PKVD_ERR_CONTEXT);
+    return -1;
+  }
+  const int phys = tables[(int64_t)i * max_blocks + logical];
+  if (phys < 0 || phys >= num_blocks) {
+    flag_error(err, PKVD_ERR_BLOCK_ID);
+    return -1;
+  }
+  return (int64_t)phys * block_size + pos % block_size;
+}
+
 __global__ void slot_mapping_kernel(int64_t* __restrict__ slots, const int32_t* __restrict__ tables,
                                     int max_blocks, const int32_t* __restrict__ ctx, int num_seqs,
                                     int block_size, int64_t num_blocks, int32_t* err) {
@@ -21,44 +47,16 @@ __global__ void slot_mapping_kernel(int64_t* __restrict__ slots, const int32_t* 
   pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= num_seqs) return;
-  const int c = ctx[i];
-  int64_t slot = -1;
-  if (c < 0) {
-    flag_error(err, PKVD_ERR_CONTEXT);
-  } else if (c > 0) {
-    const int pos = c - 1;
-    const int logical = pos / block_size;
-    if (logical >= max_blocks) {
-      flag_error(err, PKVD_ERR_CONTEXT);
-    } else {
-      const int phys = tables[(int64_t)i * max_blocks + logical];
-      if (phys < 0 || phys >= num_blocks) {
-        flag_error(err, PKVD_ERR_BLOCK_ID);
-      } else {
-        slot = (int64_t)phys * block_size + pos % block_size;
-      }
-    }
-  }
-  slots[i] = slot;
+  slots[i] = decode_slot(tables, max_blocks, ctx, i, block_size, num_blocks, err);
 }
 
-// One CTA per token row; threads stride over the 16-byte vectors of the K
-// row and then the V row.  Element e of a row is (head e / D, dim e % D).
-__global__ void kv_store_kernel(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v,
-                                const int64_t* __restrict__ slots, uint8_t* __restrict__ kc,
-                                uint8_t* __restrict__ vc, int64_t num_blocks, int block_size,
-                                int num_heads, int head_dim, int64_t block_stride,
-                                int64_t token_stride, int64_t head_stride, int elem_bytes,
-                                int32_t* err) {
-  pdl_trigger();
-  pdl_wait();                       // slots come from the slot-mapping kernel
-  const int tok = blockIdx.x;
-  const int64_t slot = slots[tok];
-  if (slot < 0) return;
-  if (slot >= num_blocks * block_size) {
-    if (threadIdx.x == 0) flag_error(err, PKVD_ERR_SLOT);
-    return;
-  }
+// Copy token tok's K and V rows (num_heads x head_dim each, 16-byte
+// vectors, threads striding) to cache slot `slot`.  Element e of a row is
+// (head e / D, dim e % D).
+__device__ __forceinline__ void store_rows(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v, int tok,
+                                           int64_t slot, uint8_t* __restrict__ kc, uint8_t* __restrict__ vc,
+                                           int block_size, int num_heads, int head_dim, int64_t block_stride,
+                                           int64_t token_stride, int64_t head_stride, int elem_bytes) {
   const int64_t blk = slot / block_size;
   const int64_t row = slot % block_size;
   const int64_t base = blk * block_stride + row * token_stride;   // elements
@@ -76,6 +74,46 @@ __global__ void kv_store_kernel(const uint8_t* __restrict__ k, const uint8_t* __
     const uint4 val = which ? __ldg(vsrc + vi) : __ldg(ksrc + vi);
     *reinterpret_cast<uint4*>((which ? vc : kc) + off) = val;
   }
+}
+
+// One CTA per token row, the slot from a slot mapping.
+__global__ void kv_store_kernel(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v,
+                                const int64_t* __restrict__ slots, uint8_t* __restrict__ kc,
+                                uint8_t* __restrict__ vc, int64_t num_blocks, int block_size,
+                                int num_heads, int head_dim, int64_t block_stride,
+                                int64_t token_stride, int64_t head_stride, int elem_bytes,
+                                int32_t* err) {
+  pdl_trigger();
+  pdl_wait();                       // slots come from the slot-mapping kernel
+  const int tok = blockIdx.x;
+  const int64_t slot = slots[tok];
+  if (slot < 0) return;
+  if (slot >= num_blocks * block_size) {
+    if (threadIdx.x == 0) flag_error(err, PKVD_ERR_SLOT);
+    return;
+  }
+  store_rows(k, v, tok, slot, kc, vc, block_size, num_heads, head_dim, block_stride, token_stride, head_stride,
+             elem_bytes);
+}
+
+// Slot mapping and store in one kernel: one CTA per row computes its slot
+// from the block table (every thread, the same two loads), optionally
+// records it, and copies the rows.
+__global__ void kv_store_paged_kernel(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v,
+                                      const int32_t* __restrict__ tables, int max_blocks,
+                                      const int32_t* __restrict__ ctx, int64_t* __restrict__ slots_out,
+                                      uint8_t* __restrict__ kc, uint8_t* __restrict__ vc, int64_t num_blocks,
+                                      int block_size, int num_heads, int head_dim, int64_t block_stride,
+                                      int64_t token_stride, int64_t head_stride, int elem_bytes, int32_t* err) {
+  pdl_wait();
+  pdl_trigger();
+  const int tok = blockIdx.x;
+  const int64_t slot = decode_slot(tables, max_blocks, ctx, tok, block_size, num_blocks,
+                                   threadIdx.x == 0 ? err : nullptr);
+  if (slots_out && threadIdx.x == 0) slots_out[tok] = slot;
+  if (slot < 0) return;
+  store_rows(k, v, tok, slot, kc, vc, block_size, num_heads, head_dim, block_stride, token_stride, head_stride,
+             elem_bytes);
 }
 
 cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* tables, int max_blocks,
@@ -98,6 +136,19 @@ cudaError_t launch_kv_store(const void* k, const void* v, const int64_t* slots, 
                     static_cast<const uint8_t*>(v), slots, static_cast<uint8_t*>(c.k_base),
                     static_cast<uint8_t*>(c.v_base), c.num_blocks, c.block_size, c.num_kv_heads, c.head_dim,
                     c.block_stride, c.token_stride, c.head_stride, elem_bytes, err);
+}
+
+cudaError_t launch_kv_store_paged(const void* k, const void* v, const int32_t* tables, int max_blocks,
+                                  const int32_t* ctx, int num_seqs, int64_t* slots_out, const pkvd_cache& c,
+                                  int elem_bytes, cudaStream_t stream, int32_t* err) {
+  if (num_seqs == 0) return cudaSuccess;
+  const int nvec = c.num_kv_heads * c.head_dim * elem_bytes / 16;
+  int threads = 2 * nvec;
+  threads = threads < 64 ? 64 : (threads > 256 ? 256 : threads);
+  return launch_pdl(kv_store_paged_kernel, dim3(num_seqs), dim3(threads), 0, stream, static_cast<const uint8_t*>(k),
+                    static_cast<const uint8_t*>(v), tables, max_blocks, ctx, slots_out,
+                    static_cast<uint8_t*>(c.k_base), static_cast<uint8_t*>(c.v_base), c.num_blocks, c.block_size,
+                    c.num_kv_heads, c.head_dim, c.block_stride, c.token_stride, c.head_stride, elem_bytes, err);
 }
 
 }  // namespace pkvd

@@ -9,7 +9,7 @@ device buffer owned by this object; a step is: write the inputs into those
 buffers, replay.
 
 Step order (all library kernels):
-    slot_mapping -> kv_store -> paged_decode_attention (partition + merge) -> sample
+    kv_store_paged (slot mapping + store) -> paged_decode_attention (partition + merge) -> sample
 """
 from __future__ import annotations
 
@@ -62,7 +62,7 @@ class DecodeStep:
         self.cache = _capi.cache_desc(k_cache, v_cache)
         self.graph = None
         self.host_graph = None
-        self.kernels_per_step = 5     # slot, store, partition, merge, sample
+        self.kernels_per_step = 4     # slot mapping + store, partition, merge, sample
 
     def enqueue(self, stream=None) -> None:
         L = _capi.lib()
@@ -72,10 +72,10 @@ class DecodeStep:
 
     def _enqueue_kv_attention(self, L, s) -> None:
         p = _capi.ptr
-        _capi.check(L.pkvd_slot_mapping(p(self.slots), p(self.block_tables), self.block_tables.shape[1],
-                                        p(self.context_lens), self.B, self.bs, self.nb, s, p(self.err)))
-        _capi.check(L.pkvd_kv_store(p(self.k_new), p(self.v_new), p(self.slots), self.B,
-                                    ctypes.byref(self.cache), s, p(self.err)))
+        # slot mapping and store in one kernel; the slots are kept for the caller
+        _capi.check(L.pkvd_kv_store_paged(p(self.k_new), p(self.v_new), p(self.block_tables),
+                                          self.block_tables.shape[1], p(self.context_lens), self.B,
+                                          p(self.slots), ctypes.byref(self.cache), s, p(self.err)))
         _capi.check(L.pkvd_paged_decode_attention_ex(
             p(self.out), p(self.q), ctypes.byref(self.cache), p(self.block_tables),
             self.block_tables.shape[1], p(self.context_lens), self.max_context_len, self.B, self.Hq,

@@ -92,6 +92,13 @@ def test_store_slot_and_sample_host_checks(L):
     assert L.pkvd_kv_store(1 << 20, 1 << 21, 1 << 22, 0, ctypes.byref(c), None, None) == 0
     assert L.pkvd_kv_store(1 << 20, (1 << 21) + 8, 1 << 22, 3, ctypes.byref(c), None, None) == 3
     assert L.pkvd_kv_store(1 << 20, 1 << 21, 1 << 22, 3, ctypes.byref(_cache(head_dim=32)), None, None) == 3
+    paged = lambda k, v, tab, nmax, ctx, n, cc: L.pkvd_kv_store_paged(k, v, tab, nmax, ctx, n, None, ctypes.byref(cc),
+                                                                    None, None)
+    assert paged(1 << 20, 1 << 21, 1 << 22, 4, 1 << 23, -1, c) == 1
+    assert paged(1 << 20, 1 << 21, 1 << 22, 4, 1 << 23, 0, c) == 0
+    assert paged(1 << 20, 1 << 21, None, 4, 1 << 23, 3, c) == 1
+    assert paged(1 << 20, 1 << 21, 1 << 22, 0, 1 << 23, 3, c) == 1
+    assert paged(1 << 20, (1 << 21) + 8, 1 << 22, 4, 1 << 23, 3, c) == 3
     assert L.pkvd_slot_mapping(1 << 20, 1 << 21, 4, 1 << 22, 0, 16, 64, None, None) == 0
     assert L.pkvd_slot_mapping(1 << 20, 1 << 21, 4, 1 << 22, 2, 0, 64, None, None) == 1
     args = [1 << 20, 1 << 21]

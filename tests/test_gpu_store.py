@@ -91,3 +91,58 @@ def test_kv_store_skips_negative_and_flags_out_of_range():
     mask[1, 1] = False
     assert torch.all(kc[mask].view(torch.int16) == 0)
     assert err.item() == pk.ERR_SLOT
+
+
+@pytest.mark.parametrize("name", list(_small_variants()) + ["qwen3_full"])
+def test_kv_store_paged_matches_the_two_step_store(name):
+    """The fused slot-mapping + store kernel writes the same cache bits and
+    slots as pkvd_slot_mapping followed by pkvd_kv_store (and the oracle)."""
+    pk = require_gpu()
+    cfg = configs.QWEN3 if name == "qwen3_full" else _small_variants()[name]
+    w = workloads.make_workload(cfg, device=DEV if name == "qwen3_full" else "cpu")
+    lay = w.layout
+    base = w.cache.to(DEV)
+    tables = torch.from_numpy(lay.block_tables).to(DEV)
+    ctx = torch.from_numpy(lay.context_lens).to(DEV)
+    k_new, v_new = w.k_new.to(DEV), w.v_new.to(DEV)
+    two = base.clone()
+    err2 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    slots2 = pk.slot_mapping(tables, ctx, cfg.block_size, lay.num_blocks, err=err2)
+    pk.kv_store(k_new, v_new, slots2, two[0, lay.layer], two[1, lay.layer], err=err2)
+    one = base
+    err1 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    slots1 = torch.full_like(slots2, 12345)
+    pk.kv_store_paged(k_new, v_new, tables, ctx, one[0, lay.layer], one[1, lay.layer], slot_mapping=slots1, err=err1)
+    torch.cuda.synchronize()
+    assert torch.equal(slots1, slots2)
+    assert torch.equal(one.view(torch.int16) if one.dtype != torch.float32 else one.view(torch.int32),
+                       two.view(torch.int16) if two.dtype != torch.float32 else two.view(torch.int32))
+    assert err1.item() == 0 and err2.item() == 0
+    ref = oracle.paging.decode_slot_mapping(lay.block_tables, lay.context_lens, cfg.block_size)
+    assert np.array_equal(slots1.cpu().numpy(), ref)
+
+
+def test_kv_store_paged_flags_and_skips_like_slot_mapping():
+    pk = require_gpu()
+    tables = torch.tensor([[5, 10, -1], [7, -1, -1], [3, 99, 2], [2, 0, 1], [4, 6, 8]],
+                          dtype=torch.int32, device=DEV)
+    ctx = torch.tensor([300, 0, 400, 769, 1], dtype=torch.int32, device=DEV)
+    nb, bs, H, D = 64, 256, 1, 64
+    kc = torch.zeros(nb, bs, H, D, dtype=torch.float16, device=DEV)
+    vc = torch.zeros_like(kc)
+    k = torch.randn(5, H, D, device=DEV).to(torch.float16)
+    v = torch.randn(5, H, D, device=DEV).to(torch.float16)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    slots = torch.empty(5, dtype=torch.int64, device=DEV)
+    pk.kv_store_paged(k, v, tables, ctx, kc, vc, slot_mapping=slots, err=err)
+    assert slots.cpu().tolist() == [10 * 256 + 43, -1, -1, -1, 4 * 256]
+    assert err.item() == (pk.ERR_BLOCK_ID | pk.ERR_CONTEXT)
+    assert torch.equal(kc[10, 43, 0], k[0, 0]) and torch.equal(vc[4, 0, 0], v[4, 0])
+    written = torch.zeros(nb, bs, dtype=torch.bool, device=DEV)
+    written[10, 43] = True
+    written[4, 0] = True
+    assert torch.all(kc[~written] == 0) and torch.all(vc[~written] == 0)
+    # no slot output requested: same cache writes
+    kc2, vc2 = torch.zeros_like(kc), torch.zeros_like(vc)
+    pk.kv_store_paged(k, v, tables, ctx, kc2, vc2)
+    assert torch.equal(kc2, kc) and torch.equal(vc2, vc)

@@ -16,8 +16,15 @@ What is computed, and where the pages say so:
 * Grok-1 section 8.2.3 (``hk_forward``): a row whose step is reset to 0
   attends to the empty set and its attention output is the zero vector.
 
+* nanochat "04 · Engine 推理与工具调用", section "推理基准 infer_bench.py":
+  a sliding-window layer reads only min(context, window) K/V rows.  The
+  plainest reading, taken here: with a window W > 0 the query attends to the
+  newest W positions of its context, [context_len - W, context_len) clipped
+  at 0 (the new token included); W <= 0 means no window.
+
 For each row i and query head h:
-    s_j = scale * <q_{i,h}, K_j>        j < context_len_i
+    s_j = scale * <q_{i,h}, K_j>        start_i <= j < context_len_i
+    start_i = max(0, context_len_i - W) with a window W > 0, else 0
     p   = softmax(s)                    (max subtracted first)
     o   = sum_j p_j V_j
 All arithmetic is float64 on exactly upcast inputs.
@@ -55,13 +62,19 @@ def attend(q_vec: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.
     return p @ V
 
 
+def window_start(context_len: int, window: int) -> int:
+    """First attended position: the newest ``window`` of ``context_len`` (0 if no window)."""
+    return max(0, int(context_len) - int(window)) if window and window > 0 else 0
+
+
 def decode_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
                      block_tables: np.ndarray, context_lens: np.ndarray,
-                     scale: float, pairs=None) -> np.ndarray:
+                     scale: float, pairs=None, window: int = 0) -> np.ndarray:
     """Output [B, Hq, D] in float64 (or only the (row, head) ``pairs``).
 
     q: [B, Hq, D]; caches: [num_blocks, block_size, Hkv, D] (any float dtype,
-    upcast exactly); block_tables: [B, max_blocks]; context_lens: [B].
+    upcast exactly); block_tables: [B, max_blocks]; context_lens: [B];
+    window > 0: attend to the newest ``window`` positions only.
     """
     B, Hq, D = q.shape
     Hkv = k_cache.shape[2]
@@ -77,6 +90,8 @@ def decode_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
             cached[key] = gather_context(k_cache, v_cache, block_tables[i],
                                          int(context_lens[i]), hk)
         K, V = cached[key]
+        st = window_start(context_lens[i], window)
+        K, V = K[st:], V[st:]
         out[i, h] = attend(q[i, h], K, V, scale) if K.shape[0] else 0.0
     return out
 

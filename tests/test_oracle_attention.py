@@ -132,3 +132,67 @@ def test_lse_merge_of_split_context_equals_full(cuts):
     edges = [0] + cuts + [ctx]
     parts = [attention.partial_state(q, K[a:b], V[a:b], 0.7) for a, b in zip(edges[:-1], edges[1:])]
     np.testing.assert_allclose(attention.lse_merge(parts), full, rtol=1e-12, atol=1e-13)
+
+
+# ---- sliding window (newest W positions of the context)
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2)])
+def test_window_matches_sdpa_with_a_window_mask(Hq, Hkv):
+    """SDPA over the whole contiguous context with a boolean mask that allows
+    only positions >= ctx - W: the window as a library routine computes it."""
+    rng = np.random.default_rng(40 + Hq)
+    B, D, bs = 5, 16, 4
+    ctx = [1, 7, 12, 9, 20]
+    q, kc, vc, tables, ctx = _random_paged(rng, B, Hq, Hkv, D, bs, ctx)
+    scale = 0.41
+    for W in (1, 3, 8, 50):
+        out = attention.decode_attention(q, kc, vc, tables, ctx, scale, window=W)
+        for i in range(B):
+            K, V = _contiguous(kc, vc, tables[i], ctx[i])
+            c = ctx[i]
+            qt = torch.from_numpy(q[i]).unsqueeze(0).unsqueeze(2)
+            Kt = torch.from_numpy(K).permute(1, 0, 2).unsqueeze(0)
+            Vt = torch.from_numpy(V).permute(1, 0, 2).unsqueeze(0)
+            allow = torch.from_numpy(np.arange(c) >= c - W).view(1, 1, 1, c)
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                qt, Kt, Vt, attn_mask=allow, scale=scale, enable_gqa=True)[0, :, 0].numpy()
+            np.testing.assert_allclose(out[i], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_window_equals_full_attention_on_the_last_w_tokens_relaid():
+    """The windowed row equals the unwindowed oracle on a fresh cache that
+    holds only the newest W tokens, laid out from position 0 in new blocks."""
+    rng = np.random.default_rng(44)
+    B, Hq, Hkv, D, bs = 3, 4, 2, 8, 4
+    ctx = [30, 9, 17]
+    q, kc, vc, tables, ctx = _random_paged(rng, B, Hq, Hkv, D, bs, ctx)
+    W = 10
+    out = attention.decode_attention(q, kc, vc, tables, ctx, 0.3, window=W)
+    for i in range(B):
+        K, V = _contiguous(kc, vc, tables[i], ctx[i])
+        K, V = K[-W:], V[-W:]
+        n = K.shape[0]
+        nb = -(-n // bs)
+        kc2 = np.zeros((nb, bs, Hkv, D))
+        vc2 = np.zeros((nb, bs, Hkv, D))
+        for j in range(n):
+            kc2[j // bs, j % bs] = K[j]
+            vc2[j // bs, j % bs] = V[j]
+        ref = attention.decode_attention(q[i:i + 1], kc2, vc2, np.arange(nb)[None, :], np.array([n]), 0.3)
+        np.testing.assert_allclose(out[i], ref[0], rtol=1e-13, atol=1e-13)
+
+
+def test_window_closed_forms():
+    rng = np.random.default_rng(45)
+    q, kc, vc, tables, ctx = _random_paged(rng, 3, 4, 2, 8, 4, [6, 13, 1])
+    full = attention.decode_attention(q, kc, vc, tables, ctx, 0.5)
+    # a window at least the context is no window; W <= 0 is no window
+    for W in (13, 100, 0, -1):
+        np.testing.assert_array_equal(attention.decode_attention(q, kc, vc, tables, ctx, 0.5, window=W), full)
+    # a window of one returns the newest token's V row exactly
+    one = attention.decode_attention(q, kc, vc, tables, ctx, 0.5, window=1)
+    for i in range(3):
+        c = ctx[i]
+        blk, row = tables[i][(c - 1) // 4], (c - 1) % 4
+        for h in range(4):
+            np.testing.assert_array_equal(one[i, h], vc[blk, row, h // 2])

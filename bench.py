@@ -62,13 +62,18 @@ class L2Flush:
 
 
 # ----------------------------------------------------------------- bytes
-def algorithmic_bytes(cfg, layout):
-    """Bytes the method must move per step (each unique byte once)."""
+def algorithmic_bytes(cfg, layout, window=0):
+    """Bytes the method must move per step (each unique byte once); with a
+    sliding window each row reads min(ctx, window) K/V rows."""
     s = cfg.itemsize
     B, Hq, Hkv, D, bs = layout.num_seqs, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size
     ctx = layout.context_lens.astype(np.int64)
     nblk = -(-ctx // bs)
-    if cfg.table_kind == "shared_prefix":
+    if window > 0:
+        start = np.maximum(ctx - window, 0)
+        kv_tokens = int(np.sum(ctx - start))
+        nblk = -(-ctx // bs) - start // bs          # table entries of the blocks the window touches
+    elif cfg.table_kind == "shared_prefix":
         prefix = cfg.ctx_args[0]
         kv_tokens = prefix + int(np.sum(ctx - prefix))
     else:
@@ -162,13 +167,13 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- setup
-def build_step(cfg, device, path):
+def build_step(cfg, device, path, window=0):
     import paged_kv_decode_store_gb300 as pk
     w = workloads.make_workload(cfg, device=device)
     lay = w.layout
     kc, vc = w.cache[0, lay.layer], w.cache[1, lay.layer]
     step = pk.DecodeStep(kc, vc, lay.num_seqs, cfg.num_q_heads, lay.max_blocks_per_seq, lay.max_context_len,
-                         cfg.vocab, w.logits.dtype, w.scale, path=path)
+                         cfg.vocab, w.logits.dtype, w.scale, path=path, window=window)
     host = {
         "q": w.q, "k_new": w.k_new, "v_new": w.v_new,
         "block_tables": torch.from_numpy(lay.block_tables).to(device),
@@ -206,7 +211,7 @@ def time_attention(step, flush, steps, stream):
     def call():
         pk.paged_decode_attention(step.q, step.k_cache, step.v_cache, step.block_tables, step.context_lens,
                                   step.max_context_len, step.scale, out=step.out, workspace=step.workspace,
-                                  err=step.err, path=step.path)
+                                  err=step.err, path=step.path, window=step.window)
 
     g = getattr(step, "_attn_graph", None)
     if g is None:
@@ -375,9 +380,10 @@ def run_reference(args, cfg, ws, rank, local):
     print(json.dumps(line))
 
 
-def config_block(cfg, lay):
+def config_block(cfg, lay, window=0):
     ctx = lay.context_lens
-    return {"workload": cfg.description, "name": cfg.name, "batch": int(lay.num_seqs),
+    desc = cfg.description + (f"; sliding window {window}" if window > 0 else "")
+    return {"workload": desc, "name": cfg.name, "batch": int(lay.num_seqs),
             "ctx_mean": float(ctx.mean()), "ctx_max": int(ctx.max()), "q_heads": cfg.num_q_heads,
             "kv_heads": cfg.num_kv_heads, "head_dim": cfg.head_dim, "block_size": cfg.block_size,
             "vocab": cfg.vocab,
@@ -394,6 +400,8 @@ def main():
     ap.add_argument("--path", default="auto", choices=["auto", "fma", "mma"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding-window attention over the newest W positions (0: none)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     cfg = configs.get(args.config)
@@ -407,9 +415,9 @@ def main():
     path = {"auto": pk.PATH_AUTO, "fma": pk.PATH_FMA, "mma": pk.PATH_MMA}[args.path]
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
-    w, step, host = build_step(cfg, dev, path)
+    w, step, host = build_step(cfg, dev, path, window=args.window)
     lay = w.layout
-    nbytes = algorithmic_bytes(cfg, lay)
+    nbytes = algorithmic_bytes(cfg, lay, window=args.window)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
@@ -455,7 +463,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic", "config": config_block(cfg, lay),
+        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic", "config": config_block(cfg, lay, args.window),
         "tokens_per_s": ws * lay.num_seqs / (ms_per_step * 1e-3),
         "step_bytes": nbytes["step"], "attention_bytes": nbytes["attention"],
         "attention_ms": attn_mean, "attention_path": args.path,

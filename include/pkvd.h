@@ -200,6 +200,24 @@ pkvd_status pkvd_paged_decode_attention_ex(void* out, const void* q, const pkvd_
                                            void* stream, int32_t* err_flag, int32_t path);
 
 /*
+ * pkvd_paged_decode_attention_window -- the same attention over a sliding
+ * window: with window > 0 row i attends to its newest `window` positions,
+ * j in [max(0, context_lens[i] - window), context_lens[i]) (nanochat
+ * "04 · Engine 推理与工具调用", section "推理基准 infer_bench.py": a window
+ * layer reads min(context, window) K/V rows; the newest positions, the new
+ * token included, is the reading taken).  window == 0: no window (same as
+ * _ex); window < 0: PKVD_INVALID_ARG.  Cache rows before the window are never
+ * read.  The workspace of pkvd_decode_workspace_bytes for max_context_len is
+ * always large enough.
+ */
+pkvd_status pkvd_paged_decode_attention_window(void* out, const void* q, const pkvd_cache* cache,
+                                               const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                               const int32_t* context_lens, int32_t max_context_len,
+                                               int32_t num_seqs, int32_t num_q_heads, float scale,
+                                               int32_t window, void* workspace, size_t workspace_bytes,
+                                               void* stream, int32_t* err_flag, int32_t path);
+
+/*
  * pkvd_paged_decode_attention_noalloc -- the same attention as
  * pkvd_paged_decode_attention (same arguments, results and errors), for
  * callers that cannot allocate device memory where they call it: code that

@@ -78,8 +78,9 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                            block_tables: torch.Tensor, context_lens: torch.Tensor,
                            max_context_len: int, scale: float, out: torch.Tensor | None = None,
                            workspace: torch.Tensor | None = None, err: torch.Tensor | None = None,
-                           stream=None, path: int = PATH_AUTO) -> torch.Tensor:
-    """out[i, h] = softmax(scale * q[i, h] . K_i^T) V_i over row i's paged context."""
+                           stream=None, path: int = PATH_AUTO, window: int = 0) -> torch.Tensor:
+    """out[i, h] = softmax(scale * q[i, h] . K_i^T) V_i over row i's paged context
+    (its newest `window` positions when window > 0)."""
     B, Hq, D = q.shape
     c = cache_desc(k_cache, v_cache)
     if out is None:
@@ -87,6 +88,12 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     if workspace is None:
         nbytes = decode_workspace_bytes(B, Hq, D, max_context_len)
         workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    if window:
+        check(lib().pkvd_paged_decode_attention_window(
+            ptr(out), ptr(q), ctypes.byref(c), ptr(block_tables), block_tables.shape[1],
+            ptr(context_lens), max_context_len, B, Hq, ctypes.c_float(scale), window, ptr(workspace),
+            workspace.numel() * workspace.element_size(), stream_handle(stream, q), _err_ptr(err), path))
+        return out
     check(lib().pkvd_paged_decode_attention_ex(
         ptr(out), ptr(q), ctypes.byref(c), ptr(block_tables), block_tables.shape[1],
         ptr(context_lens), max_context_len, B, Hq, ctypes.c_float(scale), ptr(workspace),

@@ -118,12 +118,11 @@ pkvd_status pkvd_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, i
   return PKVD_OK;
 }
 
-pkvd_status pkvd_paged_decode_attention_ex(void* out, const void* q, const pkvd_cache* cache,
-                                           const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                           const int32_t* context_lens, int32_t max_context_len,
-                                           int32_t num_seqs, int32_t num_q_heads, float scale,
-                                           void* workspace, size_t workspace_bytes, void* stream,
-                                           int32_t* err_flag, int32_t path) {
+namespace {
+pkvd_status attention_call(void* out, const void* q, const pkvd_cache* cache, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t max_context_len,
+                           int32_t num_seqs, int32_t num_q_heads, float scale, int32_t window, void* workspace,
+                           size_t workspace_bytes, void* stream, int32_t* err_flag, int32_t path) {
   if (num_seqs < 0 || num_q_heads <= 0 || max_context_len < 0 || !std::isfinite(scale)) return PKVD_INVALID_ARG;
   const pkvd_status cs = check_cache(cache, true);
   if (cs != PKVD_OK) return cs;
@@ -141,7 +140,9 @@ pkvd_status pkvd_paged_decode_attention_ex(void* out, const void* q, const pkvd_
   if (!aligned16(out) || !aligned16(q)) return PKVD_UNSUPPORTED_SHAPE;
   const int sms = device_sm_count();
   if (sms <= 0) return PKVD_CUDA_ERROR;
-  const int grid = attention_grid(num_seqs, max_context_len, sms);
+  // a window shortens every row's span: fewer units, never a larger grid
+  const int span = (window > 0 && window < max_context_len) ? window : max_context_len;
+  const int grid = attention_grid(num_seqs, span, sms);
   const size_t need = attention_workspace_bytes(num_seqs, num_q_heads, cache->head_dim, grid);
   if (!workspace || workspace_bytes < need) return PKVD_WORKSPACE_TOO_SMALL;
   if (!aligned16(workspace)) return PKVD_UNSUPPORTED_SHAPE;
@@ -169,7 +170,30 @@ pkvd_status pkvd_paged_decode_attention_ex(void* out, const void* q, const pkvd_
   a.err = err_flag;
   a.grid = grid;
   a.path = path;
+  a.window = window > 0 ? window : 0;
   return from_cuda(launch_attention(a, static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+pkvd_status pkvd_paged_decode_attention_ex(void* out, const void* q, const pkvd_cache* cache,
+                                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                           const int32_t* context_lens, int32_t max_context_len,
+                                           int32_t num_seqs, int32_t num_q_heads, float scale,
+                                           void* workspace, size_t workspace_bytes, void* stream,
+                                           int32_t* err_flag, int32_t path) {
+  return attention_call(out, q, cache, block_tables, max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                        num_q_heads, scale, 0, workspace, workspace_bytes, stream, err_flag, path);
+}
+
+pkvd_status pkvd_paged_decode_attention_window(void* out, const void* q, const pkvd_cache* cache,
+                                               const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                               const int32_t* context_lens, int32_t max_context_len,
+                                               int32_t num_seqs, int32_t num_q_heads, float scale, int32_t window,
+                                               void* workspace, size_t workspace_bytes, void* stream,
+                                               int32_t* err_flag, int32_t path) {
+  if (window < 0) return PKVD_INVALID_ARG;
+  return attention_call(out, q, cache, block_tables, max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                        num_q_heads, scale, window, workspace, workspace_bytes, stream, err_flag, path);
 }
 
 pkvd_status pkvd_paged_decode_attention(void* out, const void* q, const pkvd_cache* cache,

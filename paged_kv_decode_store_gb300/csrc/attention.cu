@@ -71,6 +71,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
     pp.ctx = a.context_lens;
     const long long cap = (long long)a.max_blocks_per_seq * a.block_size;
     pp.ctx_cap = (int)(cap < a.max_context_len ? cap : a.max_context_len);
+    pp.window = a.window;
     pp.num_seqs = a.num_seqs;
     pp.scale_log2 = a.scale * 1.4426950408889634f;
     pp.rec = rec;
@@ -101,12 +102,12 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   const dim3 mg((unsigned)a.num_seqs, (unsigned)groups), mb(256);
   if (a.dtype == PKVD_F32)
     return launch_pdl(lse_merge_kernel<float>, mg, mb, 0, stream, static_cast<float*>(a.out), (const float*)rec,
-                      a.context_lens, ctx_cap, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
+                      a.context_lens, ctx_cap, a.window, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
   if (a.dtype == PKVD_F16)
     return launch_pdl(lse_merge_kernel<__half>, mg, mb, 0, stream, static_cast<__half*>(a.out), (const float*)rec,
-                      a.context_lens, ctx_cap, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
+                      a.context_lens, ctx_cap, a.window, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
   return launch_pdl(lse_merge_kernel<__nv_bfloat16>, mg, mb, 0, stream, static_cast<__nv_bfloat16*>(a.out),
-                    (const float*)rec, a.context_lens, ctx_cap, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
+                    (const float*)rec, a.context_lens, ctx_cap, a.window, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
 }
 
 }  // namespace pkvd

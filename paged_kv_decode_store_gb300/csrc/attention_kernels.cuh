@@ -57,6 +57,7 @@ struct PartParams {
   int max_blocks;
   const int32_t* ctx;
   int ctx_cap;
+  int window;          // > 0: attend to the newest `window` positions only
   int num_seqs;
   float scale_log2;
   float* rec;          // partial records [grid][2][hq][D + 4]: acc[D], m, l, pad (the workspace)
@@ -68,10 +69,15 @@ struct PartParams {
   int active_warps;    // consumer warps that own heads
 };
 
-__device__ __forceinline__ int chunks_of(const int32_t* ctx, int i, int cap) {
+// First attended position of a context of c tokens: the newest `window`
+// positions with a sliding window (window > 0), else 0.
+__device__ __forceinline__ int window_start(int c, int window) { return (window > 0 && c > window) ? c - window : 0; }
+
+// 16-token chunks of row i's attended span (length clamped to [0, cap]).
+__device__ __forceinline__ int chunks_of(const int32_t* ctx, int i, int cap, int window) {
   int c = ctx[i];
   c = c < 0 ? 0 : (c > cap ? cap : c);
-  return (c + kChunk - 1) / kChunk;
+  return (c - window_start(c, window) + kChunk - 1) / kChunk;
 }
 
 __device__ __forceinline__ int64_t slice_begin(int64_t C, int cta, int grid) {
@@ -421,7 +427,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
   if (p.num_seqs <= kAttnThreads) {
     // one row per thread: a single block scan gives the total and the row offsets
     const int i = tid;
-    const int n = i < p.num_seqs ? chunks_of(p.ctx, i, p.ctx_cap) : 0;
+    const int n = i < p.num_seqs ? chunks_of(p.ctx, i, p.ctx_cap, p.window) : 0;
     if (cta == 0 && i < p.num_seqs) {
       const int raw = p.ctx[i];
       if (raw < 0 || raw > p.ctx_cap) flag_error(p.err, PKVD_ERR_CONTEXT);
@@ -440,7 +446,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
     __syncthreads();
   } else {
     long long part = 0;
-    for (int i = tid; i < p.num_seqs; i += kAttnThreads) part += chunks_of(p.ctx, i, p.ctx_cap);
+    for (int i = tid; i < p.num_seqs; i += kAttnThreads) part += chunks_of(p.ctx, i, p.ctx_cap, p.window);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(FULL_MASK, part, o);
     if (tid == 0) hdr.total = 0;
@@ -454,7 +460,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
     int running = 0;
     for (int base = 0; base < p.num_seqs; base += kAttnThreads) {
       const int i = base + tid;
-      const int n = i < p.num_seqs ? chunks_of(p.ctx, i, p.ctx_cap) : 0;
+      const int n = i < p.num_seqs ? chunks_of(p.ctx, i, p.ctx_cap, p.window) : 0;
       int total;
       const int incl = block_incl_scan(n, hdr.scan_warp, total);
       const int excl = running + incl - n;
@@ -491,7 +497,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
     // =============================== producer warp
     int seq = hdr.found_seq, ch = hdr.found_off;
     int ctx_seq = min(max(p.ctx[seq], 0), p.ctx_cap);
-    int nch = (ctx_seq + kChunk - 1) / kChunk;
+    int tok_base = window_start(ctx_seq, p.window);
+    int nch = (ctx_seq - tok_base + kChunk - 1) / kChunk;
     int seg_start = ch;
     long long row_start = c0 - ch;          // flat index of the row's chunk 0
     bool first_seg = true;
@@ -502,7 +509,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
         row_start += nch;
         ++seq;
         ctx_seq = min(max(p.ctx[seq], 0), p.ctx_cap);
-        nch = (ctx_seq + kChunk - 1) / kChunk;
+        tok_base = window_start(ctx_seq, p.window);
+        nch = (ctx_seq - tok_base + kChunk - 1) / kChunk;
         ch = 0;
         seg_start = 0;
         first_seg = false;
@@ -515,17 +523,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
         break;
       }
       if (*reinterpret_cast<volatile int*>(&hdr.abort_flag)) break;
-      const int token0 = ch * kChunk;
+      const int token0 = tok_base + ch * kChunk;
       const int ntok = min(kChunk, ctx_seq - token0);
-      const int lb = token0 / p.block_size, off = token0 % p.block_size;
-      if (seq != tb_seq || lb < tb_base || lb >= tb_base + 32) {
+      // a chunk of 16 consecutive positions spans at most two blocks (it
+      // starts on a 16-token boundary unless a sliding window moved it)
+      const int lb0 = token0 / p.block_size, off0 = token0 % p.block_size;
+      const int lb1 = (token0 + max(ntok, 1) - 1) / p.block_size;
+      if (seq != tb_seq || lb0 < tb_base || lb1 >= tb_base + 32) {
         tb_seq = seq;
-        tb_base = lb;
-        const int e = lb + lane;
+        tb_base = lb0;
+        const int e = lb0 + lane;
         tb_val = e < p.max_blocks ? p.tables[(int64_t)seq * p.max_blocks + e] : -1;
       }
-      const int phys = __shfl_sync(FULL_MASK, tb_val, lb - tb_base);
-      const bool ok = phys >= 0 && phys < p.num_blocks;
+      const int phys0 = __shfl_sync(FULL_MASK, tb_val, lb0 - tb_base);
+      const int phys1 = __shfl_sync(FULL_MASK, tb_val, lb1 - tb_base);
+      const bool ok = phys0 >= 0 && phys0 < p.num_blocks && phys1 >= 0 && phys1 < p.num_blocks;
       const int ncopy = ok ? ntok : 0;
       int flags = 0;
       if (ch == seg_start) flags |= F_FIRST;
@@ -540,15 +552,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
       __syncwarp();
       if (ncopy > 0) {
         uint8_t* sdst = stage_base + stage * stage_bytes;
-        const int64_t boff = ((int64_t)phys * p.block_stride + (int64_t)off * p.token_stride) * esz;
-        const uint8_t* kb = p.k_base + boff;
-        const uint8_t* vb = p.v_base + boff;
+        // row t of the chunk: block phys0 row off0 + t before the block
+        // boundary, block phys1 row off0 + t - block_size after it
+        const int split = p.block_size - off0;
+        const int64_t b0 = ((int64_t)phys0 * p.block_stride + (int64_t)off0 * p.token_stride) * esz;
+        const int64_t b1 = ((int64_t)phys1 * p.block_stride - (int64_t)split * p.token_stride) * esz;
         if (p.rows_contig) {
           for (int r = lane; r < 2 * ncopy; r += 32) {
             const int kv = r >= ncopy;
             const int t = kv ? r - ncopy : r;
-            bulk_g2s(sdst + kv * kChunk * p.rowb + t * p.rowb,
-                     (kv ? vb : kb) + (int64_t)t * p.token_stride * esz, p.row_bytes, &hdr.full[stage]);
+            const int64_t src = (t < split ? b0 : b1) + (int64_t)t * p.token_stride * esz;
+            bulk_g2s(sdst + kv * kChunk * p.rowb + t * p.rowb, (kv ? p.v_base : p.k_base) + src, p.row_bytes,
+                     &hdr.full[stage]);
           }
         } else {
           const int per = ncopy * p.hkv;
@@ -556,8 +571,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
             const int kv = r >= per;
             const int rem = kv ? r - per : r;
             const int t = rem / p.hkv, h = rem % p.hkv;
-            bulk_g2s(sdst + kv * kChunk * p.rowb + t * p.rowb + h * D * esz,
-                     (kv ? vb : kb) + ((int64_t)t * p.token_stride + (int64_t)h * p.head_stride) * esz,
+            const int64_t src = (t < split ? b0 : b1) + ((int64_t)t * p.token_stride + (int64_t)h * p.head_stride) * esz;
+            bulk_g2s(sdst + kv * kChunk * p.rowb + t * p.rowb + h * D * esz, (kv ? p.v_base : p.k_base) + src,
                      D * esz, &hdr.full[stage]);
           }
         }
@@ -611,7 +626,7 @@ constexpr int kMaxMergeRecords = 1024;     // >= any partition grid (one CTA per
 
 template <typename T>
 __global__ void __launch_bounds__(256) lse_merge_kernel(T* __restrict__ out, const float* __restrict__ rec,
-                                                        const int32_t* __restrict__ ctx, int ctx_cap,
+                                                        const int32_t* __restrict__ ctx, int ctx_cap, int window,
                                                         int num_seqs, int hq, int D, int grid) {
   __shared__ int s_rec[kMaxMergeRecords];
   __shared__ int s_n;
@@ -623,7 +638,7 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(T* __restrict__ out, con
   // overlaps the partition kernel; records are read after pdl_wait().
   long long before = 0, all = 0;
   for (int r = threadIdx.x; r < num_seqs; r += blockDim.x) {
-    const int c = chunks_of(ctx, r, ctx_cap);
+    const int c = chunks_of(ctx, r, ctx_cap, window);
     all += c;
     if (r < i) before += c;
   }
@@ -643,7 +658,7 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(T* __restrict__ out, con
     P += s_part[0][w];
     C += s_part[1][w];
   }
-  const long long n = chunks_of(ctx, i, ctx_cap);
+  const long long n = chunks_of(ctx, i, ctx_cap, window);
   T* orow = out + (int64_t)i * hq * D;
   if (n <= 0) {
     pdl_wait();

@@ -39,6 +39,7 @@ struct AttnArgs {
   int32_t* err;
   int grid;           // partition CTAs
   int path;           // PKVD_PATH_FMA / PKVD_PATH_MMA (resolved)
+  int window;         // > 0: sliding window of the newest `window` positions
 };
 
 int attention_grid(int num_seqs, int max_context_len, int sm_count);

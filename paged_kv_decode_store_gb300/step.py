@@ -24,7 +24,7 @@ class DecodeStep:
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, num_seqs: int,
                  num_q_heads: int, max_blocks_per_seq: int, max_context_len: int,
                  vocab: int, logits_dtype: torch.dtype, scale: float,
-                 path: int = _capi.PATH_AUTO):
+                 path: int = _capi.PATH_AUTO, window: int = 0):
         dev = k_cache.device
         nb, bs, Hkv, D = k_cache.shape
         B, Hq = num_seqs, num_q_heads
@@ -33,6 +33,7 @@ class DecodeStep:
         self.max_context_len = max_context_len
         self.scale = float(scale)
         self.path = path
+        self.window = int(window)        # > 0: sliding-window attention over the newest positions
         dt = k_cache.dtype
         # Per-step inputs and outputs live in two byte arenas (256-byte aligned
         # views), so a host-staged step moves each side with one copy.
@@ -76,11 +77,11 @@ class DecodeStep:
         _capi.check(L.pkvd_kv_store_paged(p(self.k_new), p(self.v_new), p(self.block_tables),
                                           self.block_tables.shape[1], p(self.context_lens), self.B,
                                           p(self.slots), ctypes.byref(self.cache), s, p(self.err)))
-        _capi.check(L.pkvd_paged_decode_attention_ex(
+        _capi.check(L.pkvd_paged_decode_attention_window(
             p(self.out), p(self.q), ctypes.byref(self.cache), p(self.block_tables),
             self.block_tables.shape[1], p(self.context_lens), self.max_context_len, self.B, self.Hq,
-            ctypes.c_float(self.scale), p(self.workspace), self.workspace.numel(), s, p(self.err),
-            self.path))
+            ctypes.c_float(self.scale), self.window, p(self.workspace), self.workspace.numel(), s,
+            p(self.err), self.path))
 
     def _enqueue_sample(self, L, s) -> None:
         p = _capi.ptr

@@ -82,7 +82,7 @@ def gather_rows_for_oracle(w, rows):
     return raw_numpy(k), raw_numpy(v), np.array(tables, dtype=np.int64), lay.context_lens[rows]
 
 
-def oracle_sampled(w, gathered, rows, heads_per_row):
+def oracle_sampled(w, gathered, rows, heads_per_row, window=0):
     """Oracle attention for sampled (row, head) pairs of a device workload."""
     k, v, tables, ctx = gathered
     bs = w.cfg.block_size
@@ -95,4 +95,4 @@ def oracle_sampled(w, gathered, rows, heads_per_row):
     vf = from_raw(v, dt).double().numpy()
     q = w.q[rows].cpu().double().numpy()
     pairs = [(r, h) for r in range(len(rows)) for h in heads_per_row]
-    return oracle.attention.decode_attention(q, kf, vf, tables, ctx, w.scale, pairs=pairs), pairs
+    return oracle.attention.decode_attention(q, kf, vf, tables, ctx, w.scale, pairs=pairs, window=window), pairs

@@ -47,7 +47,7 @@ def paths_for(cfg, pk):
     return out
 
 
-def run_attention(pk, w, path, cache=None):
+def run_attention(pk, w, path, cache=None, window=0):
     lay = w.layout
     if cache is None:
         cache = w.cache.to(DEV)
@@ -58,7 +58,8 @@ def run_attention(pk, w, path, cache=None):
     slots = pk.slot_mapping(tables, ctx, w.cfg.block_size, lay.num_blocks, err=err)
     q = w.q.to(DEV)
     pk.kv_store(w.k_new.to(DEV), w.v_new.to(DEV), slots, kc, vc, err=err)
-    out = pk.paged_decode_attention(q, kc, vc, tables, ctx, lay.max_context_len, w.scale, err=err, path=path)
+    out = pk.paged_decode_attention(q, kc, vc, tables, ctx, lay.max_context_len, w.scale, err=err, path=path,
+                                    window=window)
     torch.cuda.synchronize()
     return out, err.item()
 
@@ -159,3 +160,65 @@ def test_workspace_is_reusable_without_clearing():
     assert torch.isfinite(outs[0]).all()
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
     assert torch.all(outs[0][2] == 0)                     # the empty row
+
+
+@pytest.mark.parametrize("name", ["qwen3_small", "grok1_ragged", "longctx_small", "short_rows", "mqa_f16", "tiny"])
+@pytest.mark.parametrize("window", [1, 17, 256, 1000])
+def test_sliding_window_matches_oracle(name, window):
+    """Newest `window` positions only; cache rows before the window hold NaN
+    in the poisoned workloads only past the context, so the window start
+    must be exact for the result to match."""
+    pk = require_gpu()
+    cfg = small_variants()[name]
+    w = workloads.make_workload(cfg)
+    kf, vf, _ = oracle_store_f64(w)
+    lay = w.layout
+    ref = oracle.attention.decode_attention(w.q.double().numpy(), kf, vf, lay.block_tables,
+                                            lay.context_lens, w.scale, window=window)
+    for path in paths_for(cfg, pk):
+        out, err = run_attention(pk, w, path, window=window)
+        assert err == 0
+        check_attention(out.double().cpu().numpy(), ref, w.q.dtype)
+
+
+def test_sliding_window_never_reads_before_the_window():
+    """Rows before each row's window are overwritten with NaN after the store:
+    the windowed output stays finite and equal to the clean run."""
+    pk = require_gpu()
+    cfg = configs.GROK1.scaled(num_seqs=4, ctx_kind="explicit", ctx_args=(300, 40, 1, 129), table_kind="perm",
+                               vocab=2048)
+    w = workloads.make_workload(cfg)
+    lay = w.layout
+    W = 33
+    cache = w.cache.to(DEV)
+    clean, err = run_attention(pk, w, pk.PATH_AUTO, cache=cache, window=W)
+    assert err == 0
+    bs = cfg.block_size
+    for i in range(lay.num_seqs):
+        c = int(lay.context_lens[i])
+        for j in range(max(0, c - W)):
+            blk = int(lay.block_tables[i, j // bs])
+            cache[:, lay.layer, blk, j % bs] = float("nan")
+    dirty, err = run_attention(pk, w, pk.PATH_AUTO, cache=cache, window=W)
+    assert err == 0
+    assert torch.isfinite(dirty).all() and torch.equal(dirty, clean)
+
+
+@pytest.mark.parametrize("name", ["qwen3", "longctx"])
+def test_sliding_window_full_size_sampled_rows(name):
+    pk = require_gpu()
+    cfg = configs.CONFIGS[name]
+    w = workloads.make_workload(cfg, device=DEV)
+    lay = w.layout
+    W = 1024
+    rng = np.random.default_rng(1)
+    longest = int(np.argmax(lay.context_lens))
+    rows = sorted(set([0, longest, lay.num_seqs - 1] + rng.choice(lay.num_seqs, 3, replace=False).tolist()))
+    heads = sorted(set([0, cfg.num_q_heads - 1] + rng.choice(cfg.num_q_heads, 2, replace=False).tolist()))
+    gathered = gather_rows_for_oracle(w, rows)
+    ref, pairs = oracle_sampled(w, gathered, rows, heads, window=W)
+    for path in paths_for(cfg, pk):
+        out, err = run_attention(pk, w, path, cache=w.cache, window=W)
+        assert err == 0
+        o = out[torch.tensor(rows, device=DEV)].double().cpu().numpy()
+        check_attention(o, ref, w.q.dtype, pairs=pairs)

@@ -25,6 +25,21 @@ Steps, in the order the pages give them:
    ``x_j / T + g_j``, with g_j = -log(-log u_j) and u_j from the Philox
    stream in ``oracle.philox`` (lowest index wins an exact tie).
 
+Extras of Grok-1 section 8.3 (``sample_token``), all optional:
+
+5. Mask.  After the temperature, ``where(mask, logits, -1e10)``: a masked id
+   keeps a logit of -1e10, so it is cut by every filter and never drawn while
+   any allowed id remains (all masked: every id is equal, the draw uniform).
+   Greedy rows (T == 0) take the argmax over the allowed ids (id 0 when none
+   is allowed).
+6. ``token_prob``: the drawn id's probability under ``softmax`` of the
+   filtered logits (kept ids as they are, every other id at -1e10, so
+   probability 0); greedy rows give 1.
+7. Top-8 (``TOP_K = 8``, section 8.3.2): ``jax.lax.top_k`` of those
+   probabilities: the 8 largest, an equal pair in index order (the ids of
+   probability 0 therefore follow in index order).  Greedy rows: the drawn id
+   with probability 1, then the lowest other ids with 0.
+
 All arithmetic is float64 on the exactly upcast logits.
 """
 from __future__ import annotations
@@ -79,8 +94,30 @@ def nucleus_cut(xs: np.ndarray, kept: np.ndarray, p: float):
                              "cut_all": False}
 
 
+NEG = -1e10          # the masked / filtered logit of sample_token
+
+
+def masked_scaled(x: np.ndarray, temperature: float, mask=None) -> np.ndarray:
+    """x / T with masked ids at -1e10 (mask: bool per id, True = allowed)."""
+    xs = np.asarray(x, dtype=np.float64) / float(temperature)
+    if mask is not None:
+        xs = np.where(np.asarray(mask, dtype=bool), xs, NEG)
+    return xs
+
+
+def kept_set(x: np.ndarray, temperature: float, top_k: int, top_p: float, mask=None):
+    """Ids that survive the mask, top-k and nucleus filters (T > 0), plus the
+    nucleus diagnostics (None when the nucleus is off)."""
+    xs = masked_scaled(x, temperature, mask)
+    kept = topk_set(xs, int(top_k))
+    ninfo = None
+    if float(top_p) < 1.0:
+        kept, ninfo = nucleus_cut(xs, kept, float(top_p))
+    return xs, kept, ninfo
+
+
 def sample_row(x: np.ndarray, temperature: float, top_k: int, top_p: float,
-               seed: int, offset: int, return_info: bool = False):
+               seed: int, offset: int, return_info: bool = False, mask=None):
     """One row's token id (and diagnostics used by the parity tests)."""
     x = np.asarray(x, dtype=np.float64)
     T = float(temperature)
@@ -89,14 +126,13 @@ def sample_row(x: np.ndarray, temperature: float, top_k: int, top_p: float,
     if T < 0:
         raise ValueError("negative temperature")
     if T == 0.0:
-        tok = greedy(x)
+        if mask is not None and np.any(mask):
+            tok = greedy(np.where(np.asarray(mask, dtype=bool), x, -np.inf))
+        else:
+            tok = greedy(x) if mask is None else 0
         info["greedy"] = True
         return (tok, info) if return_info else tok
-    xs = x / T
-    kept = topk_set(x, int(top_k))
-    if float(top_p) < 1.0:
-        kept, ninfo = nucleus_cut(xs, kept, float(top_p))
-        info["nucleus"] = ninfo
+    xs, kept, info["nucleus"] = kept_set(x, T, top_k, top_p, mask)
     kept_sorted = np.sort(kept)
     g = philox.gumbel(seed, offset, kept_sorted)
     score = xs[kept_sorted] + g
@@ -108,6 +144,46 @@ def sample_row(x: np.ndarray, temperature: float, top_k: int, top_p: float,
     info["top1_score"] = float(score[best])
     info["kept"] = kept_sorted
     return (tok, info) if return_info else tok
+
+
+def filtered_probs(x: np.ndarray, temperature: float, top_k: int, top_p: float, mask=None) -> np.ndarray:
+    """softmax of the filtered logits: kept ids as scaled, every other id at
+    -1e10 (T > 0)."""
+    xs, kept, _ = kept_set(x, temperature, top_k, top_p, mask)
+    f = np.full_like(xs, NEG)
+    f[kept] = xs[kept]
+    z = np.exp(f - f.max())
+    return z / z.sum()
+
+
+def sample_outputs(x: np.ndarray, temperature: float, top_k: int, top_p: float,
+                   seed: int, offset: int, mask=None, return_info: bool = False):
+    """(token, token_prob, top-8 probabilities, top-8 ids) of one row.
+
+    The top-8 order is the mathematical one: ids of positive probability
+    (kept and allowed) by scaled logit descending, then index; then the ids
+    of probability 0 (filtered or masked) by index.  (Float underflow of a
+    kept id's probability does not move it into the second group.)"""
+    res = sample_row(x, temperature, top_k, top_p, seed, offset, return_info=True, mask=mask)
+    tok, info = res
+    V = np.asarray(x).shape[0]
+    if float(temperature) == 0.0:
+        probs = np.zeros(V)
+        probs[tok] = 1.0
+        positive = np.array([tok])
+        xs = np.zeros(V)
+    else:
+        probs = filtered_probs(x, temperature, top_k, top_p, mask)
+        xs, kept, _ = kept_set(x, temperature, top_k, top_p, mask)
+        allowed = np.ones(V, dtype=bool) if mask is None else np.asarray(mask, dtype=bool)
+        if not allowed.any():
+            allowed = np.ones(V, dtype=bool)       # all masked: every id equal (uniform)
+        positive = np.array(sorted(set(kept.tolist()) & set(np.nonzero(allowed)[0].tolist())), dtype=np.int64)
+    pos_order = positive[np.lexsort((positive, -xs[positive]))] if positive.size else positive
+    rest = np.setdiff1d(np.arange(V), positive)
+    order = np.concatenate([pos_order, rest])[:8].astype(np.int64)
+    out = (tok, float(probs[tok]), probs[order], order)
+    return (out, info) if return_info else out
 
 
 def truncated_probs(x: np.ndarray, temperature: float, top_k: int, top_p: float) -> np.ndarray:

@@ -145,3 +145,90 @@ def test_gumbel_max_chi_square_against_truncated_softmax(T, k, p):
     if exp[-1] == 0:
         obs, exp = obs[:-1], exp[:-1]
     assert stats.chisquare(obs, exp).pvalue > 1e-3
+
+
+# ---- sample_token extras: mask, token_prob, top-8 (Grok-1 section 8.3)
+
+def _page_probs(x, T, p, mask):
+    """The page's sample_token order written out with the page-form filter:
+    x / T, masked ids to -1e10, ascending-sort nucleus, softmax."""
+    xs = np.asarray(x, dtype=np.float64) / T
+    xs = np.where(mask, xs, -1e10)
+    if p < 1.0:
+        keep = _page_top_p_filter(xs, p)
+        xs = np.where(np.isin(np.arange(xs.shape[0]), list(keep)), xs, -1e10)
+    z = np.exp(xs - xs.max())
+    return z / z.sum()
+
+
+def test_token_prob_and_top8_match_the_page_formula():
+    rng = np.random.default_rng(21)
+    checked = 0
+    for trial in range(200):
+        V = int(rng.integers(9, 300))
+        x = torch.from_numpy((rng.standard_normal(V) * rng.uniform(0.5, 3)).astype(np.float32))
+        x = x.to(torch.bfloat16).double().numpy()
+        T = float(rng.uniform(0.3, 2.0))
+        p = float(rng.choice([1.0, 0.9, 0.5]))
+        mask = rng.random(V) > 0.3
+        mask[int(rng.integers(V))] = True
+        (tok, tp, p8, i8), info = sampler.sample_outputs(x, T, 0, p, 5, trial, mask=mask, return_info=True)
+        n = info["nucleus"]
+        if n is not None and min(abs(n["mass_before"] - p), abs(n["mass_after"] - p)) < 1e-9:
+            continue
+        ref = _page_probs(x, T, p, mask)
+        assert mask[tok] and ref[tok] > 0
+        np.testing.assert_allclose(tp, ref[tok], rtol=1e-12)
+        # lax.top_k: largest first, equal values in index order
+        order = np.lexsort((np.arange(V), -ref))[:8]
+        np.testing.assert_allclose(p8, ref[order], rtol=1e-12, atol=0)
+        assert i8.tolist() == order.tolist()
+        checked += 1
+    assert checked > 150
+
+
+def test_all_allowed_mask_changes_nothing():
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal(50)
+    for T, k, p in [(1.0, 0, 1.0), (0.8, 7, 0.9), (0.0, 0, 1.0)]:
+        a = sampler.sample_outputs(x, T, k, p, 3, 4)
+        b = sampler.sample_outputs(x, T, k, p, 3, 4, mask=np.ones(50, bool))
+        assert a[0] == b[0] and a[1] == b[1]
+        assert np.array_equal(a[2], b[2]) and np.array_equal(a[3], b[3])
+
+
+def test_masked_ids_are_never_drawn_and_the_rest_keep_their_ratios():
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal(10) * 1.2
+    mask = np.array([1, 0, 1, 1, 0, 1, 1, 1, 0, 1], bool)
+    n = 20_000
+    draws = np.array([sampler.sample_row(x, 1.0, 0, 1.0, 17, off, mask=mask) for off in range(n)])
+    assert mask[draws].all()
+    w = np.exp(x - x.max()) * mask
+    expected = w / w.sum() * n
+    obs = np.array([(draws == j).sum() for j in range(10)])
+    assert stats.chisquare(obs[mask], expected[mask]).pvalue > 1e-3
+
+
+def test_all_masked_row_draws_uniformly_and_greedy_takes_id_zero():
+    n = 12_000
+    draws = np.array([sampler.sample_row(np.arange(6.0), 0.9, 0, 1.0, 8, off, mask=np.zeros(6, bool))
+                      for off in range(n)])
+    assert stats.chisquare(np.bincount(draws, minlength=6), np.full(6, n / 6)).pvalue > 1e-3
+    assert sampler.sample_row(np.arange(6.0), 0.0, 0, 1.0, 8, 0, mask=np.zeros(6, bool)) == 0
+    assert sampler.sample_row(np.arange(6.0), 0.0, 0, 1.0, 8, 0,
+                              mask=np.array([1, 1, 0, 0, 0, 0], bool)) == 1
+
+
+def test_top8_closed_forms():
+    x = np.array([0.0, 5.0, 1.0, 5.0, 3.0, -2.0, 4.0, 2.0, 6.0, -1.0])
+    # greedy: the drawn id with probability 1, then the lowest other ids
+    tok, tp, p8, i8 = sampler.sample_outputs(x, 0.0, 0, 1.0, 1, 0)
+    assert tok == 8 and tp == 1.0 and i8.tolist() == [8, 0, 1, 2, 3, 4, 5, 6]
+    assert p8.tolist() == [1.0] + [0.0] * 7
+    # top-k 3: the three kept ids by value (5.0 tie in index order), then ids 0, 2, ... at 0
+    tok, tp, p8, i8 = sampler.sample_outputs(x, 1.0, 3, 1.0, 1, 0)
+    assert i8.tolist() == [8, 1, 3, 0, 2, 4, 5, 6]
+    w = np.exp(np.array([6.0, 5.0, 5.0]) - 6.0)
+    np.testing.assert_allclose(p8[:3], w / w.sum(), rtol=1e-15)
+    assert np.all(p8[3:] == 0) and abs(p8.sum() - 1) < 1e-15

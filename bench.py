@@ -62,7 +62,7 @@ class L2Flush:
 
 
 # ----------------------------------------------------------------- bytes
-def algorithmic_bytes(cfg, layout, window=0):
+def algorithmic_bytes(cfg, layout, window=0, extras=False):
     """Bytes the method must move per step (each unique byte once); with a
     sliding window each row reads min(ctx, window) K/V rows."""
     s = cfg.itemsize
@@ -82,6 +82,8 @@ def algorithmic_bytes(cfg, layout, window=0):
     store = 4 * B * Hkv * D * s + 8 * B
     slots = B * (4 + 4 + 8)
     sample = B * cfg.vocab * cfg.logits_itemsize + B * (4 + 4 + 4 + 8 + 8 + 4)
+    if extras:                                      # mask bits in; token_prob and the top-8 out
+        sample += B * ((cfg.vocab + 31) // 32) * 4 + B * (4 + 8 * 4 + 8 * 4)
     return {"attention": attn, "kv_store": store, "slot_mapping": slots, "sampler": sample,
             "step": attn + store + slots + sample}
 
@@ -167,13 +169,13 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- setup
-def build_step(cfg, device, path, window=0):
+def build_step(cfg, device, path, window=0, extras=False):
     import paged_kv_decode_store_gb300 as pk
     w = workloads.make_workload(cfg, device=device)
     lay = w.layout
     kc, vc = w.cache[0, lay.layer], w.cache[1, lay.layer]
     step = pk.DecodeStep(kc, vc, lay.num_seqs, cfg.num_q_heads, lay.max_blocks_per_seq, lay.max_context_len,
-                         cfg.vocab, w.logits.dtype, w.scale, path=path, window=window)
+                         cfg.vocab, w.logits.dtype, w.scale, path=path, window=window, extras=extras)
     host = {
         "q": w.q, "k_new": w.k_new, "v_new": w.v_new,
         "block_tables": torch.from_numpy(lay.block_tables).to(device),
@@ -185,6 +187,11 @@ def build_step(cfg, device, path, window=0):
         "seeds": torch.from_numpy(w.seeds.view(np.int64)).to(device),
         "offsets": torch.from_numpy(w.offsets.view(np.int64)).to(device),
     }
+    if extras:
+        # a seeded 5 % of the vocabulary masked in every row
+        g = torch.Generator(device="cpu").manual_seed(4242)
+        allowed = torch.rand(lay.num_seqs, cfg.vocab, generator=g) >= 0.05
+        host["mask_words"] = pk.pack_mask(allowed).to(device)
     for k, v in host.items():
         getattr(step, k).copy_(v)
     return w, step, host
@@ -380,9 +387,10 @@ def run_reference(args, cfg, ws, rank, local):
     print(json.dumps(line))
 
 
-def config_block(cfg, lay, window=0):
+def config_block(cfg, lay, window=0, extras=False):
     ctx = lay.context_lens
     desc = cfg.description + (f"; sliding window {window}" if window > 0 else "")
+    desc += "; sampler extras (5% ids masked, token_prob, top-8)" if extras else ""
     return {"workload": desc, "name": cfg.name, "batch": int(lay.num_seqs),
             "ctx_mean": float(ctx.mean()), "ctx_max": int(ctx.max()), "q_heads": cfg.num_q_heads,
             "kv_heads": cfg.num_kv_heads, "head_dim": cfg.head_dim, "block_size": cfg.block_size,
@@ -400,6 +408,8 @@ def main():
     ap.add_argument("--path", default="auto", choices=["auto", "fma", "mma"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extras", action="store_true",
+                    help="sampler extras: a 5 %% id mask, token_prob and the top-8 probabilities and ids")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding-window attention over the newest W positions (0: none)")
     args = ap.parse_args()
@@ -415,9 +425,9 @@ def main():
     path = {"auto": pk.PATH_AUTO, "fma": pk.PATH_FMA, "mma": pk.PATH_MMA}[args.path]
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
-    w, step, host = build_step(cfg, dev, path, window=args.window)
+    w, step, host = build_step(cfg, dev, path, window=args.window, extras=args.extras)
     lay = w.layout
-    nbytes = algorithmic_bytes(cfg, lay, window=args.window)
+    nbytes = algorithmic_bytes(cfg, lay, window=args.window, extras=args.extras)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
@@ -463,7 +473,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic", "config": config_block(cfg, lay, args.window),
+        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic", "config": config_block(cfg, lay, args.window, args.extras),
         "tokens_per_s": ws * lay.num_seqs / (ms_per_step * 1e-3),
         "step_bytes": nbytes["step"], "attention_bytes": nbytes["attention"],
         "attention_ms": attn_mean, "attention_path": args.path,

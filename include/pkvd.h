@@ -241,7 +241,8 @@ pkvd_status pkvd_paged_decode_attention_noalloc(void* out, const void* q, const 
                                                 int32_t num_seqs, int32_t num_q_heads, float scale,
                                                 void* stream, int32_t* err_flag);
 
-/* Workspace bytes pkvd_sample needs (host only; currently always 0). */
+/* Workspace bytes of pkvd_sample_ex's optional outputs: 32 per row (host
+ * only).  pkvd_sample itself needs none (it may get NULL, 0). */
 pkvd_status pkvd_sample_workspace_bytes(int32_t num_rows, int32_t vocab, size_t* bytes);
 
 /*
@@ -267,6 +268,40 @@ pkvd_status pkvd_sample(int32_t* token_ids, const void* logits, int32_t dtype,
                         const float* temperature, const int32_t* top_k, const float* top_p,
                         const uint64_t* seeds, const uint64_t* offsets,
                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pkvd_sample_ex -- pkvd_sample plus the rest of Grok-1's sample_token
+ * ("第 8 章 runners.py 推理引擎", section 8.3; TOP_K = 8 in section 8.3.2),
+ * each part optional (NULL = off):
+ *   mask      allowed-id bits [num_rows, mask_words_per_row] uint32, bit
+ *             (j % 32) of word (j / 32) set = id j may be drawn.  A masked
+ *             id counts as the page's logit -1e10 after the temperature: it
+ *             is cut by every filter and never drawn while any id is allowed;
+ *             a row with no allowed id draws uniformly over all ids (greedy
+ *             rows take id 0).  Rows must be 16-byte aligned and short enough
+ *             to sit in shared memory over a cluster (else
+ *             PKVD_UNSUPPORTED_SHAPE).
+ *   token_prob f32 [num_rows]: the drawn id's probability under softmax of
+ *             the filtered logits (kept ids as scaled, all others 0); 1 for
+ *             greedy rows.
+ *   top_probs f32 [num_rows, 8], top_ids int32 [num_rows, 8]: the 8 largest
+ *             of those probabilities -- kept ids by value, index order among
+ *             equal values, then ids of probability 0 in index order (-1 and
+ *             0 past the vocabulary).  Greedy rows: the drawn id with 1, then
+ *             the lowest other ids with 0.
+ * workspace: at least pkvd_sample_workspace_bytes(num_rows, vocab) bytes
+ *             (4-byte aligned) when any of token_prob / top_probs / top_ids
+ *             is requested (the sampler leaves each row's cut there for a
+ *             second kernel); otherwise unused.
+ * The token ids are those pkvd_sample gives for the same inputs.
+ */
+pkvd_status pkvd_sample_ex(int32_t* token_ids, const void* logits, int32_t dtype,
+                           int32_t num_rows, int32_t vocab, int64_t row_stride,
+                           const float* temperature, const int32_t* top_k, const float* top_p,
+                           const uint64_t* seeds, const uint64_t* offsets,
+                           const uint32_t* mask, int64_t mask_words_per_row,
+                           float* token_prob, float* top_probs, int32_t* top_ids,
+                           void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -23,7 +23,7 @@ from ._capi import (LIB_PATH, PATH_AUTO, PATH_FMA, PATH_MMA, ERR_BLOCK_ID, ERR_S
                     stream_handle, cache_desc, ptr)
 from .step import DecodeStep  # noqa: F401
 
-__all__ = ["slot_mapping", "kv_store", "kv_store_paged", "paged_decode_attention", "decode_workspace_bytes",
+__all__ = ["slot_mapping", "kv_store", "kv_store_paged", "sample_ex", "pack_mask", "paged_decode_attention", "decode_workspace_bytes",
            "sample", "DecodeStep", "PkvdError", "lib"]
 
 
@@ -114,3 +114,41 @@ def sample(logits: torch.Tensor, temperature: torch.Tensor, top_k: torch.Tensor,
                             ptr(temperature), ptr(top_k), ptr(top_p), ptr(seeds), ptr(offsets),
                             None, 0, stream_handle(stream, logits)))
     return out
+
+
+
+def pack_mask(allowed: torch.Tensor) -> torch.Tensor:
+    """Bool [R, V] (True = may be drawn) -> the int32 [R, ceil(V/32)] bit words
+    pkvd_sample_ex takes (bit j % 32 of word j / 32)."""
+    R, V = allowed.shape
+    W = (V + 31) // 32
+    bits = torch.zeros(R, W * 32, dtype=torch.int64, device=allowed.device)
+    bits[:, :V] = allowed.to(torch.int64)
+    weights = torch.pow(2, torch.arange(32, device=allowed.device, dtype=torch.int64))
+    words = (bits.view(R, W, 32) * weights).sum(-1)
+    return torch.where(words >= 2**31, words - 2**32, words).to(torch.int32)
+
+
+def sample_ex(logits: torch.Tensor, temperature: torch.Tensor, top_k: torch.Tensor, top_p: torch.Tensor,
+              seeds: torch.Tensor, offsets: torch.Tensor, mask_words: torch.Tensor | None = None,
+              with_probs: bool = True, stream=None):
+    """sample() plus Grok's extras: an optional allowed-id bit mask (pack_mask),
+    and (with_probs) the drawn token's probability and the top-8 probabilities
+    and ids.  Returns (token_ids, token_prob, top_probs, top_ids)."""
+    R, V = logits.shape
+    if logits.stride(1) != 1:
+        raise ValueError("logits rows must be contiguous")
+    dev = logits.device
+    out = torch.empty(R, dtype=torch.int32, device=dev)
+    tp = torch.empty(R, dtype=torch.float32, device=dev) if with_probs else None
+    p8 = torch.empty(R, 8, dtype=torch.float32, device=dev) if with_probs else None
+    i8 = torch.empty(R, 8, dtype=torch.int32, device=dev) if with_probs else None
+    n = ctypes.c_size_t(0)
+    check(lib().pkvd_sample_workspace_bytes(R, V, ctypes.byref(n)))
+    ws = torch.empty(max(int(n.value), 16), dtype=torch.uint8, device=dev)
+    mw = mask_words.shape[1] if mask_words is not None else 0
+    check(lib().pkvd_sample_ex(ptr(out), ptr(logits), dtype_code(logits.dtype), R, V, logits.stride(0),
+                               ptr(temperature), ptr(top_k), ptr(top_p), ptr(seeds), ptr(offsets),
+                               ptr(mask_words), mw, ptr(tp), ptr(p8), ptr(i8), ptr(ws), ws.numel(),
+                               stream_handle(stream, logits)))
+    return out, tp, p8, i8

@@ -208,24 +208,48 @@ pkvd_status pkvd_paged_decode_attention(void* out, const void* q, const pkvd_cac
 
 pkvd_status pkvd_sample_workspace_bytes(int32_t num_rows, int32_t vocab, size_t* bytes) {
   if (!bytes || num_rows < 0 || vocab <= 0) return PKVD_INVALID_ARG;
-  *bytes = 0;
+  *bytes = (size_t)num_rows * kRowInfo * sizeof(int32_t);     // per-row cut parameters (extras only)
   return PKVD_OK;
+}
+
+pkvd_status pkvd_sample_ex(int32_t* token_ids, const void* logits, int32_t dtype, int32_t num_rows, int32_t vocab,
+                           int64_t row_stride, const float* temperature, const int32_t* top_k, const float* top_p,
+                           const uint64_t* seeds, const uint64_t* offsets, const uint32_t* mask,
+                           int64_t mask_words_per_row, float* token_prob, float* top_probs, int32_t* top_ids,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  if (!valid_dtype(dtype)) return PKVD_UNSUPPORTED_DTYPE;
+  if (num_rows < 0 || vocab <= 0 || row_stride < vocab) return PKVD_INVALID_ARG;
+  if (vocab > (1 << 23)) return PKVD_UNSUPPORTED_SHAPE;
+  if (mask && mask_words_per_row < ((int64_t)vocab + 31) / 32) return PKVD_INVALID_ARG;
+  if (num_rows == 0) return PKVD_OK;
+  if (!token_ids || !logits || !temperature || !top_k || !top_p || !seeds || !offsets) return PKVD_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(logits) % esize(dtype)) return PKVD_UNSUPPORTED_SHAPE;
+  if (mask && (reinterpret_cast<uintptr_t>(mask) % 4 || !sample_mask_supported(dtype, vocab, row_stride, logits)))
+    return PKVD_UNSUPPORTED_SHAPE;
+  const bool extras = token_prob || top_probs || top_ids;
+  int32_t* row_info = nullptr;
+  if (extras) {
+    size_t need = 0;
+    pkvd_sample_workspace_bytes(num_rows, vocab, &need);
+    if (!workspace || workspace_bytes < need) return PKVD_WORKSPACE_TOO_SMALL;
+    if (reinterpret_cast<uintptr_t>(workspace) % 4) return PKVD_UNSUPPORTED_SHAPE;
+    row_info = static_cast<int32_t*>(workspace);
+  }
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_sample(token_ids, logits, dtype, num_rows, vocab, row_stride, temperature, top_k, top_p,
+                                seeds, offsets, mask, mask_words_per_row, row_info, st);
+  if (e != cudaSuccess || !extras) return from_cuda(e);
+  return from_cuda(launch_sample_extras(logits, dtype, num_rows, vocab, row_stride, temperature, mask,
+                                        mask_words_per_row, row_info, token_ids, token_prob, top_probs, top_ids,
+                                        st));
 }
 
 pkvd_status pkvd_sample(int32_t* token_ids, const void* logits, int32_t dtype, int32_t num_rows, int32_t vocab,
                         int64_t row_stride, const float* temperature, const int32_t* top_k, const float* top_p,
                         const uint64_t* seeds, const uint64_t* offsets, void* workspace, size_t workspace_bytes,
                         void* stream) {
-  (void)workspace;
-  (void)workspace_bytes;
-  if (!valid_dtype(dtype)) return PKVD_UNSUPPORTED_DTYPE;
-  if (num_rows < 0 || vocab <= 0 || row_stride < vocab) return PKVD_INVALID_ARG;
-  if (vocab > (1 << 23)) return PKVD_UNSUPPORTED_SHAPE;
-  if (num_rows == 0) return PKVD_OK;
-  if (!token_ids || !logits || !temperature || !top_k || !top_p || !seeds || !offsets) return PKVD_INVALID_ARG;
-  if (reinterpret_cast<uintptr_t>(logits) % esize(dtype)) return PKVD_UNSUPPORTED_SHAPE;
-  return from_cuda(launch_sample(token_ids, logits, dtype, num_rows, vocab, row_stride, temperature, top_k, top_p,
-                                 seeds, offsets, static_cast<cudaStream_t>(stream)));
+  return pkvd_sample_ex(token_ids, logits, dtype, num_rows, vocab, row_stride, temperature, top_k, top_p, seeds,
+                        offsets, nullptr, 0, nullptr, nullptr, nullptr, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -59,10 +59,23 @@ cudaError_t launch_kv_store_paged(const void* k, const void* v, const int32_t* t
                                   const int32_t* ctx, int num_seqs, int64_t* slots_out, const pkvd_cache& c,
                                   int elem_bytes, cudaStream_t stream, int32_t* err);
 
+// Per-row cut parameters the sampler leaves for the extras kernel:
+// [0] flags (kRowGreedy, kRowUniform, kRowTopK), [1] nucleus threshold key
+// (0 = off), [2] k-th key, [3] index of the last kept id at the k-th key
+// (INT_MAX: every one), [4] the row max value (f32 bits), [5..7] unused.
+constexpr int kRowInfo = 8;
+constexpr int kRowGreedy = 1, kRowUniform = 2, kRowTopK = 4;
+
 cudaError_t launch_sample(int32_t* token_ids, const void* logits, int dtype, int num_rows,
                           int vocab, int64_t row_stride, const float* temperature,
                           const int32_t* top_k, const float* top_p, const uint64_t* seeds,
-                          const uint64_t* offsets, cudaStream_t stream);
+                          const uint64_t* offsets, const uint32_t* mask, int64_t mask_stride,
+                          int32_t* row_info, cudaStream_t stream);
+bool sample_mask_supported(int dtype, int vocab, int64_t row_stride, const void* logits);
+cudaError_t launch_sample_extras(const void* logits, int dtype, int num_rows, int vocab, int64_t row_stride,
+                                 const float* temperature, const uint32_t* mask, int64_t mask_stride,
+                                 const int32_t* row_info, const int32_t* token_ids, float* token_prob,
+                                 float* top_probs, int32_t* top_ids, cudaStream_t stream);
 
 int device_sm_count();   // current device, cached; <= 0 on failure
 

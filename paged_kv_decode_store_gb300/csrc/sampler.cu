@@ -467,6 +467,9 @@ struct SampArgs {
   const float* top_p;
   const uint64_t* seeds;
   const uint64_t* offsets;
+  const uint32_t* mask;   // optional allowed-id bits [rows, mask_stride words] (bit j % 32 of word j / 32)
+  int64_t mask_stride;
+  int32_t* row_info;      // optional per-row cut parameters for the extras kernel (kRowInfo ints)
 };
 
 template <typename T>
@@ -507,6 +510,32 @@ __device__ __forceinline__ uint32_t keys2(uint32_t w) {
   w &= nz | 0x7fff7fffu;
   const uint32_t s = (w >> 15) & 0x00010001u;
   return w ^ ((s * 0x7fffu) | 0x80008000u);
+}
+
+// Masked ids become -inf: weight 0 in every sum, below every allowed id in
+// every cut, never a candidate while an allowed id remains.  `bits` holds
+// the 8 allowed bits of the word's 8 logits (bit e for logit e).
+template <typename T>
+__device__ __forceinline__ uint4 apply_mask16(uint4 u, uint32_t bits) {
+  constexpr uint32_t ninf = Pack2<T>::kNegInf2;
+  auto one = [&](uint32_t w, uint32_t b2) {
+    const uint32_t keep = ((b2 & 1u) ? 0x0000ffffu : 0u) | ((b2 & 2u) ? 0xffff0000u : 0u);
+    return (w & keep) | (ninf & ~keep);
+  };
+  u.x = one(u.x, bits);
+  u.y = one(u.y, bits >> 2);
+  u.z = one(u.z, bits >> 4);
+  u.w = one(u.w, bits >> 6);
+  return u;
+}
+__device__ __forceinline__ bool allowed_bit(const uint32_t* bits, int64_t j) {
+  return (bits[j >> 5] >> (j & 31)) & 1u;
+}
+template <typename T> __device__ __forceinline__ T neg_inf_value();
+template <> __device__ __forceinline__ float neg_inf_value<float>() { return __uint_as_float(0xff800000u); }
+template <> __device__ __forceinline__ __half neg_inf_value<__half>() { return __ushort_as_half((unsigned short)0xfc00u); }
+template <> __device__ __forceinline__ __nv_bfloat16 neg_inf_value<__nv_bfloat16>() {
+  return __ushort_as_bfloat16((unsigned short)0xff80u);
 }
 
 // Eight bits, one per logit of a 16-byte word of 16-bit floats (bit e for
@@ -582,6 +611,33 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
   const int lo = (int)crank * a.slice;
   const int n = max(0, min(a.V, lo + a.slice) - lo);
   const int copy = warp & (kHistCopies - 1);
+  const uint32_t* mask_row = a.mask ? a.mask + (int64_t)row_id * a.mask_stride : nullptr;
+  const uint64_t seed = a.seeds[row_id], off = a.offsets[row_id];
+  // the row's cut parameters for the extras kernel (rank 0 writes them)
+  auto put_row_info = [&](int flags, uint32_t tau_k, uint32_t kth_k, uint32_t tie_enc, float row_max) {
+    if (a.row_info && crank == 0 && tid == 0) {
+      int32_t* ri = a.row_info + (int64_t)row_id * kRowInfo;
+      ri[0] = flags;
+      ri[1] = (int32_t)tau_k;
+      ri[2] = (int32_t)kth_k;
+      ri[3] = tie_enc == 0xffffffffu ? 0x7fffffff : (int32_t)tie_enc - 1;   // last kept tie at the k-th key
+      ri[4] = __float_as_int(row_max);
+    }
+  };
+  // a tie candidate in 32 bits for a max over ranks (INT_MAX -> all ones)
+  auto tie_code = [](int cand) -> uint32_t { return cand == 0x7fffffff ? 0xffffffffu : (uint32_t)(cand + 1); };
+  // No candidate anywhere (every id masked, or no finite logit): every id
+  // counts the same, so the race is over -ln u alone.  Returns the row's best
+  // packed (race key, ~id); cluster-uniform.
+  auto uniform_draw = [&]() -> unsigned long long {
+    unsigned long long ub = 0;
+    for (int j = tid; j < n; j += kSampThreads) {
+      const unsigned long long pk = race_key(seed, off, (uint32_t)(lo + j), 0.f);
+      ub = pk > ub ? pk : ub;
+    }
+    ub = block_max_u64(ub, h.red);
+    return cluster_scalar<true>(c, ub);
+  };
 
   if constexpr (sizeof(T) == 2) {
     if (a.fast) {
@@ -615,12 +671,18 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
                      (uint32_t)sz, &h.bar[i]);
           }
         }
-        for (int j = rest + tid; j < n; j += kSampThreads) slice_smem[j] = row[lo + j];
+        for (int j = rest + tid; j < n; j += kSampThreads)
+          slice_smem[j] = (mask_row && !allowed_bit(mask_row, lo + j)) ? neg_inf_value<T>() : row[lo + j];
+        const uint8_t* mbytes = mask_row ? reinterpret_cast<const uint8_t*>(mask_row) + (lo >> 3) : nullptr;
         for (int i = 0; i < nch; ++i) {
           mbar_wait_bounded(&h.bar[i], 0);
           const int v = i * (kChunkBytes / 16) + tid;           // one 16-byte word per thread and chunk
           if (v < nvec) {
-            const uint4 u = sv[v];
+            uint4 u = sv[v];
+            if (mbytes) {                                       // masked ids become -inf in place
+              u = apply_mask16<T>(u, mbytes[v]);
+              reinterpret_cast<uint4*>(slice_smem)[v] = u;
+            }
             mx2 = __hmax2(mx2, __hmax2(__hmax2(as_t2<T>(u.x), as_t2<T>(u.y)), __hmax2(as_t2<T>(u.z), as_t2<T>(u.w))));
           }
         }
@@ -662,6 +724,7 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
           for (int r = 0; r < c.cs; ++r) best = px[r].x > best ? px[r].x : best;
           a.token_ids[row_id] = (int)(0xffffffffu - (uint32_t)(best & 0xffffffffull));
         }
+        put_row_info(kRowGreedy, 0u, 0u, 0u, 0.f);
         return;
       }
       const float l2t = 1.4426950408889634f / Tr;
@@ -948,6 +1011,7 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
       // The exchange of the tie counts is also the barrier after which no
       // peer reads this CTA's window any more.
       int tie_lim = 0x7fffffff;
+      int tie_cand = 0x7fffffff;   // index of this CTA's last kept tie, for the extras (INT_MAX: all kept)
       if (topk_on && need_eq < cnt_eq) {
         const bool hi_ok = kth < 0xffffu;
         const T2 ge_k = key_threshold2<T>(kth), ge_k1 = key_threshold2<T>(hi_ok ? kth + 1u : kth);
@@ -1026,6 +1090,7 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
           }
           tie_lim = (int)(0xffffffu - prefix);
         }
+        tie_cand = want == 0 ? -1 : (want == (long long)mine ? lo + n - 1 : lo + tie_lim);
       }
 
       // ---- F4. Gumbel-max over the kept ids
@@ -1040,7 +1105,6 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
         const uint32_t kp = K::key((uint32_t)(*reinterpret_cast<const unsigned short*>(&tv)));
         if (!isinf(vmin) && kp > thr) thr = kp;
       }
-      const uint64_t seed = a.seeds[row_id], off = a.offsets[row_id];
       const float invT = 1.f / Tr;
       auto keep = [&](int j, uint32_t b) -> bool {
         const uint32_t key = K::key(b);
@@ -1131,16 +1195,19 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
       // rank used the same bound (the row max) the packed keys compare as
       // they are; otherwise each rank's best time moves to the row max in
       // log2 units: log2 t + (max - mrow) / (T ln 2).
-      const ulonglong2* px = cluster_push(c, crank, bestg, (unsigned long long)__float_as_uint(mrow));
-      // the max id always passes every filter, so the row's best is never 0
-      if (crank == 0 && tid == 0) {
+      const ulonglong2* px = cluster_push(c, crank, bestg,
+                                          ((unsigned long long)tie_code(tie_cand) << 32) | __float_as_uint(mrow));
+      // every thread combines the ranks (the result is cluster-uniform)
+      unsigned long long best = 0;
+      uint32_t tie_enc = 0;
+      float mm = __uint_as_float((uint32_t)px[0].y);
+      {
         bool same = true;
-        float mm = __uint_as_float((uint32_t)px[0].y);
-        for (int r = 1; r < c.cs; ++r) {
-          same = same && px[r].y == px[0].y;
+        for (int r = 0; r < c.cs; ++r) {
+          same = same && (uint32_t)px[r].y == (uint32_t)px[0].y;
           mm = fmaxf(mm, __uint_as_float((uint32_t)px[r].y));
+          tie_enc = max(tie_enc, (uint32_t)(px[r].y >> 32));
         }
-        unsigned long long best = 0;
         if (same) {
           for (int r = 0; r < c.cs; ++r) best = px[r].x > best ? px[r].x : best;
         } else {
@@ -1155,8 +1222,13 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
             }
           }
         }
-        a.token_ids[row_id] = (int)(0xffffffffu - (uint32_t)(best & 0xffffffffull));
       }
+      // the max allowed id passes every filter, so best is 0 only when no id
+      // is allowed (or none is finite)
+      const bool uniform = best == 0;
+      if (uniform) best = uniform_draw();
+      if (crank == 0 && tid == 0) a.token_ids[row_id] = (int)(0xffffffffu - (uint32_t)(best & 0xffffffffull));
+      put_row_info((uniform ? kRowUniform : 0) | (topk_on ? kRowTopK : 0), tau, kth, tie_enc, mm);
       return;
     }
   }
@@ -1185,6 +1257,11 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
     for (int j = bulk / (int)sizeof(T) + tid; j < n; j += kSampThreads) slice_smem[j] = src[j];
     for (int i = 0; i < nch; ++i) mbar_wait_bounded(&h.bar[i], 0);
     __syncthreads();
+    if (mask_row) {                 // masked ids become -inf in place (masks need a resident slice)
+      for (int j = tid; j < n; j += kSampThreads)
+        if (!allowed_bit(mask_row, lo + j)) slice_smem[j] = neg_inf_value<T>();
+      __syncthreads();
+    }
     src = slice_smem;
     vec = true;
   }
@@ -1202,6 +1279,7 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
   const float Tr = a.temperature[row_id];
   if (!(Tr > 0.f)) {
     if (crank == 0 && tid == 0) a.token_ids[row_id] = imax;
+    put_row_info(kRowGreedy, 0u, 0u, 0u, 0.f);
     cluster_sync();               // peers may still read this CTA's shared memory
     return;
   }
@@ -1296,6 +1374,7 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
   // lowest-index ties (slices are ordered by index), found by a local radix
   // select over its tie indices; tie_lim = largest local index kept
   int tie_lim = 0x7fffffff;
+  int tie_cand = 0x7fffffff;     // index of this CTA's last kept tie, for the extras (INT_MAX: all kept)
   if (topk_on && need_eq < cnt_eq) {
     unsigned long long mine = 0;
     visit<T>(src, n, vec, [&](int, uint32_t b) { mine += K::key(b) == kth; });
@@ -1335,10 +1414,10 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
       }
       tie_lim = (int)(0xffffffu - prefix);
     }
+    tie_cand = want == 0 ? -1 : (want == (long long)mine ? lo + n - 1 : lo + tie_lim);
   }
 
   // ---- 6. Gumbel-max over the kept ids, candidates queued per warp
-  const uint64_t seed = a.seeds[row_id], off = a.offsets[row_id];
   const float invT = 1.f / Tr;
   unsigned long long bestg = 0;
   uint32_t* qi = q_idx + warp * kQueue;
@@ -1401,12 +1480,290 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
     if (qn > 0) drain(qn);
   }
   bestg = block_max_u64(bestg, h.red);
-  bestg = cluster_scalar<true>(c, bestg);
-  if (crank == 0 && tid == 0)
-    a.token_ids[row_id] = bestg ? (int)(0xffffffffu - (uint32_t)(bestg & 0xffffffffull)) : imax;
+  uint32_t tie_enc = 0;
+  {
+    const ulonglong2* px = cluster_push(c, crank, bestg, (unsigned long long)tie_code(tie_cand));
+    bestg = 0;
+    for (int r = 0; r < c.cs; ++r) {
+      bestg = px[r].x > bestg ? px[r].x : bestg;
+      tie_enc = max(tie_enc, (uint32_t)px[r].y);
+    }
+  }
+  // 0 only when no id is allowed (or none is finite): uniform over the row
+  const bool uniform = bestg == 0;
+  if (uniform) bestg = uniform_draw();
+  if (crank == 0 && tid == 0) a.token_ids[row_id] = (int)(0xffffffffu - (uint32_t)(bestg & 0xffffffffull));
+  put_row_info((uniform ? kRowUniform : 0) | (topk_on ? kRowTopK : 0), tau, kth, tie_enc, m);
   cluster_sync();               // peers may still read this CTA's shared memory
 }
 
+
+// ---------------------------------------------------------------- extras
+// token_prob and the top-8 of the distribution the draw used (Grok-1
+// "第 8 章 runners.py 推理引擎", section 8.3 sample_token and section 8.3.2
+// TOP_K = 8): probabilities are softmax of the filtered logits, kept ids as
+// they are and every other id at probability 0; the top-8 lists the kept
+// ids by value (index order among equal values), then the ids of
+// probability 0 in index order.  A cluster of 8 CTAs per row runs after the
+// sampler, which left the row's cut parameters (row_info: cut keys, the last
+// kept tie at the k-th key, the row max) and token; each CTA takes one slice
+// in one coalesced pass and pushes its partials to rank 0.
+struct ExtrasArgs {
+  const void* logits;
+  int V;
+  int64_t row_stride;
+  const float* temperature;
+  const uint32_t* mask;
+  int64_t mask_stride;
+  const int32_t* row_info;
+  const int32_t* token_ids;
+  float* token_prob;      // [rows] or null
+  float* top_probs;       // [rows, 8] or null
+  int32_t* top_ids;       // [rows, 8] or null
+};
+
+constexpr int kTop = 8;
+constexpr int kExThreads = 512;            // threads per extras CTA
+constexpr int kExCluster = 8;              // CTAs (slices) per row
+constexpr int kExWarps = kExThreads / 32;
+
+// 8 rounds of a warp-wide max over the heads of per-lane lists sorted in
+// descending order; the owner of each winner pops it (entries are unique).
+__device__ __forceinline__ void warp_merge8(unsigned long long* lst, unsigned long long* outl) {
+#pragma unroll
+  for (int i = 0; i < kTop; ++i) {
+    unsigned long long best = lst[0];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(FULL_MASK, best, o));
+    outl[i] = best;
+    if (best != 0ull && lst[0] == best) {
+#pragma unroll
+      for (int q = 0; q < kTop - 1; ++q) lst[q] = lst[q + 1];
+      lst[kTop - 1] = 0ull;
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kExThreads) sample_extras_kernel(const ExtrasArgs e) {
+  using K = Keys<T>;
+  // per-rank partials pushed to rank 0: [rank][0] Z (f64 bits), [1] kept
+  // count, [2..9] the rank's best 8 (key, -index)
+  __shared__ unsigned long long s_part[kExCluster][2 + kTop];
+  __shared__ unsigned long long s_top[kExWarps][kTop];
+  __shared__ double s_z[kExWarps];
+  __shared__ long long s_n[kExWarps];
+  pdl_wait();                       // the sampler's token and row_info
+  pdl_trigger();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t crank = cluster_rank();
+  const int r = blockIdx.x / kExCluster;
+  const T* row = static_cast<const T*>(e.logits) + (int64_t)r * e.row_stride;
+  const uint32_t* mrow = e.mask ? e.mask + (int64_t)r * e.mask_stride : nullptr;
+  const int32_t* info = e.row_info + (int64_t)r * kRowInfo;
+  const int flags = info[0];
+  const int tok = e.token_ids[r];
+  const int V = e.V;
+  auto bits_of = [&](int j) -> uint32_t {
+    if constexpr (sizeof(T) == 4) return __float_as_uint(reinterpret_cast<const float*>(row)[j]);
+    else return (uint32_t)reinterpret_cast<const unsigned short*>(row)[j];
+  };
+  auto allowed = [&](int j) { return !mrow || allowed_bit(mrow, j); };
+  float* tp = e.top_probs ? e.top_probs + (int64_t)r * kTop : nullptr;
+  int32_t* ti = e.top_ids ? e.top_ids + (int64_t)r * kTop : nullptr;
+  if (flags & (kRowGreedy | kRowUniform)) {
+    // a point mass on the token, or every id equal (nothing allowed); the
+    // branch is the same on every rank, so no rank waits at a barrier
+    if (crank == 0 && tid == 0) {
+      const bool uni = (flags & kRowUniform) != 0;
+      const float pu = 1.f / (float)V;
+      if (e.token_prob) e.token_prob[r] = uni ? pu : 1.f;
+      int fill = 0, next = 0;
+      if (!uni) {
+        if (tp) tp[0] = 1.f;
+        if (ti) ti[0] = tok;
+        fill = 1;
+      }
+      for (; fill < kTop; ++fill) {
+        if (!uni && next == tok) ++next;
+        const bool in = next < V;
+        if (tp) tp[fill] = in ? (uni ? pu : 0.f) : 0.f;
+        if (ti) ti[fill] = in ? next : -1;
+        ++next;
+      }
+    }
+    return;
+  }
+  const float Tr = e.temperature[r];
+  const float l2t = 1.4426950408889634f / Tr;
+  const bool topk = (flags & kRowTopK) != 0;
+  const uint32_t tau = (uint32_t)info[1], kth = (uint32_t)info[2];
+  const int tie_last = info[3];
+  const float m = __int_as_float(info[4]);
+  const uint32_t thr = topk && kth > tau ? kth : tau;
+  // kept: allowed, at or above the cut, and at the k-th key only up to the
+  // last kept tie (the sampler keeps the lowest indices)
+  auto kept = [&](int j, uint32_t key) {
+    return allowed(j) && key >= thr && !(topk && key == kth && j > tie_last);
+  };
+  // this rank's slice of the row, in 16-byte words when the row is aligned
+  constexpr int E = 16 / (int)sizeof(T);
+  const int per = ((V + kExCluster - 1) / kExCluster + E - 1) / E * E;
+  const int lo = min(V, (int)crank * per), hi = min(V, lo + per);
+  float zs = 0.f, zc = 0.f;
+  unsigned long long t8[kTop];
+#pragma unroll
+  for (int i = 0; i < kTop; ++i) t8[i] = 0ull;
+  int npos = 0;
+  auto zadd = [&](float w) {
+    const float y = w - zc;
+    const float t = zs + y;
+    zc = (t - zs) - y;
+    zs = t;
+  };
+  auto insert = [&](unsigned long long pk) {
+    if (pk > t8[kTop - 1]) {
+      t8[kTop - 1] = pk;
+#pragma unroll
+      for (int i = kTop - 1; i > 0; --i)
+        if (t8[i] > t8[i - 1]) {
+          const unsigned long long x = t8[i];
+          t8[i] = t8[i - 1];
+          t8[i - 1] = x;
+        }
+    }
+  };
+  auto take = [&](int j, uint32_t b) {
+    const uint32_t key = K::key(b);
+    if (!kept(j, key)) return;
+    ++npos;
+    zadd(ex2_ftz((K::value(b) - m) * l2t));
+    insert(((unsigned long long)key << 32) | (0xffffffffu - (uint32_t)j));
+  };
+  const bool vec = (reinterpret_cast<uintptr_t>(row) % 16) == 0;
+  const int nvec = vec ? (hi - lo) / E : 0;
+  const uint4* rv = reinterpret_cast<const uint4*>(row + lo);
+  if constexpr (sizeof(T) == 2) {
+    // a packed compare against the cut finds the few words with kept ids
+    const auto thr2 = key_threshold2<T>(thr);
+    const bool plain = !mrow && !topk;          // kept == at or above the cut
+    for (int v = tid; v < nvec; v += kExThreads) {
+      const uint4 u = rv[v];
+      uint32_t pb = pass_bits<T>(u, thr2);
+      if (plain && pb == 0xffu) {
+        // a whole word kept: its 8 weights summed as a tree, one compensated
+        // add, and the keys tested against this thread's 8th best
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        const float ml = m * l2t;
+        float ws = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = Pack2<T>::to_float2(w[q]);
+          ws += ex2_ftz(fmaf(f.x, l2t, -ml)) + ex2_ftz(fmaf(f.y, l2t, -ml));
+        }
+        zadd(ws);
+        npos += 8;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t b = (w[q / 2] >> (16 * (q & 1))) & 0xffffu;
+          insert(((unsigned long long)K::key(b) << 32) | (0xffffffffu - (uint32_t)(lo + v * E + q)));
+        }
+        continue;
+      }
+      while (pb) {
+        const int q = __ffs(pb) - 1;
+        pb &= pb - 1;
+        const uint32_t wd = q < 2 ? u.x : (q < 4 ? u.y : (q < 6 ? u.z : u.w));
+        take(lo + v * E + q, (q & 1) ? (wd >> 16) : (wd & 0xffffu));
+      }
+    }
+  } else {
+    for (int v = tid; v < nvec; v += kExThreads) {
+      const uint4 u = rv[v];
+      take(lo + v * 4 + 0, u.x);
+      take(lo + v * 4 + 1, u.y);
+      take(lo + v * 4 + 2, u.z);
+      take(lo + v * 4 + 3, u.w);
+    }
+  }
+  for (int j = lo + nvec * E + tid; j < hi; j += kExThreads) take(j, bits_of(j));
+  // block: Z, the kept count, the best 8
+  double z = (double)zs;
+  long long np = npos;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    z += __shfl_xor_sync(FULL_MASK, z, o);
+    np += __shfl_xor_sync(FULL_MASK, np, o);
+  }
+  unsigned long long wl[kTop];
+  warp_merge8(t8, wl);
+  if (lane == 0) {
+    s_z[warp] = z;
+    s_n[warp] = np;
+#pragma unroll
+    for (int i = 0; i < kTop; ++i) s_top[warp][i] = wl[i];
+  }
+  __syncthreads();
+  if (warp == 0) {
+    double zb = lane < kExWarps ? s_z[lane] : 0.0;
+    long long nb = lane < kExWarps ? s_n[lane] : 0;
+    unsigned long long ll[kTop], bl[kTop];
+#pragma unroll
+    for (int i = 0; i < kTop; ++i) ll[i] = lane < kExWarps ? s_top[lane][i] : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      zb += __shfl_xor_sync(FULL_MASK, zb, o);
+      nb += __shfl_xor_sync(FULL_MASK, nb, o);
+    }
+    warp_merge8(ll, bl);
+    // push this rank's partials into rank 0's table
+    if (lane < 2 + kTop) {
+      const unsigned long long val = lane == 0 ? (unsigned long long)__double_as_longlong(zb)
+                                   : lane == 1 ? (unsigned long long)nb : bl[0];
+      unsigned long long vv = val;
+#pragma unroll
+      for (int i = 0; i < kTop; ++i)
+        if (lane == 2 + i) vv = bl[i];
+      const uint32_t addr = dsmem_addr(&s_part[crank][lane], 0u);
+      asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(vv) : "memory");
+    }
+  }
+  cluster_sync();
+  if (crank != 0 || warp != 0) return;
+  // rank 0: the row's Z, count and best 8 over the ranks
+  double Z = lane < kExCluster ? __longlong_as_double((long long)s_part[lane][0]) : 0.0;
+  long long NP = lane < kExCluster ? (long long)s_part[lane][1] : 0;
+  unsigned long long ll[kTop], fl[kTop];
+#pragma unroll
+  for (int i = 0; i < kTop; ++i) ll[i] = lane < kExCluster ? s_part[lane][2 + i] : 0ull;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Z += __shfl_xor_sync(FULL_MASK, Z, o);
+    NP += __shfl_xor_sync(FULL_MASK, NP, o);
+  }
+  warp_merge8(ll, fl);
+  if (lane != 0) return;
+  const float inv = (float)(1.0 / Z);
+  if (e.token_prob) e.token_prob[r] = ex2_ftz((K::value(bits_of(tok)) - m) * l2t) * inv;
+  int fill = 0;
+  for (; fill < kTop && fl[fill] != 0ull; ++fill) {
+    const uint32_t key = (uint32_t)(fl[fill] >> 32);
+    if (tp) tp[fill] = ex2_ftz((K::value_of_key(key) - m) * l2t) * inv;
+    if (ti) ti[fill] = (int32_t)(0xffffffffu - (uint32_t)(fl[fill] & 0xffffffffull));
+  }
+  // fewer than 8 kept: the lowest ids of probability 0, in index order
+  for (int j = 0; fill < kTop && j < V; ++j) {
+    if (kept(j, K::key(bits_of(j)))) continue;
+    if (tp) tp[fill] = 0.f;
+    if (ti) ti[fill] = j;
+    ++fill;
+  }
+  for (; fill < kTop; ++fill) {
+    if (tp) tp[fill] = 0.f;
+    if (ti) ti[fill] = -1;
+  }
+  (void)NP;
+}
 
 // Clusters of `cs` CTAs with `smem` bytes each that the GPU runs at once
 // (cached per size; a failed query falls back to an SM-count estimate).
@@ -1510,7 +1867,7 @@ static cudaError_t launch_sample_t(const SampArgs& base, int num_rows, cudaStrea
 cudaError_t launch_sample(int32_t* token_ids, const void* logits, int dtype, int num_rows, int vocab,
                           int64_t row_stride, const float* temperature, const int32_t* top_k,
                           const float* top_p, const uint64_t* seeds, const uint64_t* offsets,
-                          cudaStream_t stream) {
+                          const uint32_t* mask, int64_t mask_stride, int32_t* row_info, cudaStream_t stream) {
   if (num_rows == 0) return cudaSuccess;
   const int esz = dtype == PKVD_F32 ? 4 : 2;
   SampArgs a;
@@ -1528,12 +1885,65 @@ cudaError_t launch_sample(int32_t* token_ids, const void* logits, int dtype, int
   a.top_p = top_p;
   a.seeds = seeds;
   a.offsets = offsets;
+  a.mask = mask;
+  a.mask_stride = mask_stride;
+  a.row_info = row_info;
   cudaError_t e;
   if (dtype == PKVD_F32) e = launch_sample_t<float>(a, num_rows, stream);
   else if (dtype == PKVD_F16) e = launch_sample_t<__half>(a, num_rows, stream);
   else e = launch_sample_t<__nv_bfloat16>(a, num_rows, stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+bool sample_mask_supported(int dtype, int vocab, int64_t row_stride, const void* logits) {
+  // a mask is applied to the shared-memory copy of the row: rows must be
+  // 16-byte aligned and fit on chip over a cluster of kMaxCluster CTAs
+  const int esz = dtype == PKVD_F32 ? 4 : 2;
+  if ((reinterpret_cast<uintptr_t>(logits) % 16) || ((row_stride * esz) % 16)) return false;
+  const size_t hdr = ((sizeof(SampHdr) + 127) / 128) * 128;
+  const size_t region = esz == 4 ? (size_t)region_bytes<float>() : (size_t)region_bytes<__half>();
+  const int align = 16 / esz;
+  const long long slice = (((long long)vocab + kMaxCluster - 1) / kMaxCluster + align - 1) / align * align;
+  const size_t sb = ((size_t)slice * esz + 127) / 128 * 128;
+  const size_t budget = 232448 - hdr - region;
+  const size_t cap = budget < (size_t)kMaxChunks * kChunkBytes ? budget : (size_t)kMaxChunks * kChunkBytes;
+  return sb <= cap;
+}
+
+cudaError_t launch_sample_extras(const void* logits, int dtype, int num_rows, int vocab, int64_t row_stride,
+                                 const float* temperature, const uint32_t* mask, int64_t mask_stride,
+                                 const int32_t* row_info, const int32_t* token_ids, float* token_prob,
+                                 float* top_probs, int32_t* top_ids, cudaStream_t stream) {
+  if (num_rows == 0) return cudaSuccess;
+  ExtrasArgs x;
+  x.logits = logits;
+  x.V = vocab;
+  x.row_stride = row_stride;
+  x.temperature = temperature;
+  x.mask = mask;
+  x.mask_stride = mask_stride;
+  x.row_info = row_info;
+  x.token_ids = token_ids;
+  x.token_prob = token_prob;
+  x.top_probs = top_probs;
+  x.top_ids = top_ids;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(num_rows * kExCluster));
+  cfg.blockDim = dim3(kExThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)kExCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (dtype == PKVD_F32) return cudaLaunchKernelEx(&cfg, sample_extras_kernel<float>, x);
+  if (dtype == PKVD_F16) return cudaLaunchKernelEx(&cfg, sample_extras_kernel<__half>, x);
+  return cudaLaunchKernelEx(&cfg, sample_extras_kernel<__nv_bfloat16>, x);
 }
 
 }  // namespace pkvd

@@ -24,7 +24,7 @@ class DecodeStep:
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, num_seqs: int,
                  num_q_heads: int, max_blocks_per_seq: int, max_context_len: int,
                  vocab: int, logits_dtype: torch.dtype, scale: float,
-                 path: int = _capi.PATH_AUTO, window: int = 0):
+                 path: int = _capi.PATH_AUTO, window: int = 0, extras: bool = False):
         dev = k_cache.device
         nb, bs, Hkv, D = k_cache.shape
         B, Hq = num_seqs, num_q_heads
@@ -42,6 +42,12 @@ class DecodeStep:
                ("temperature", (B,), torch.float32), ("top_k", (B,), torch.int32),
                ("top_p", (B,), torch.float32), ("seeds", (B,), torch.int64), ("offsets", (B,), torch.int64)]
         outs = [("out", (B, Hq, D), dt), ("token_ids", (B,), torch.int32)]
+        # sampler extras: an allowed-id bit mask in, token_prob and the top-8 out
+        self.extras = bool(extras)
+        if self.extras:
+            ins.append(("mask_words", (B, (vocab + 31) // 32), torch.int32))
+            outs += [("token_prob", (B,), torch.float32), ("top_probs", (B, 8), torch.float32),
+                     ("top_ids", (B, 8), torch.int32)]
         self._in_layout, in_bytes = _arena_layout(ins)
         self._out_layout, out_bytes = _arena_layout(outs)
         self.inputs = torch.zeros(in_bytes, dtype=torch.uint8, device=dev)
@@ -51,6 +57,11 @@ class DecodeStep:
         for name, view in _arena_views(self.outputs, self._out_layout).items():
             setattr(self, name, view)
         self.block_tables.fill_(-1)
+        if self.extras:
+            self.mask_words.fill_(-1)                  # every id allowed until the caller says otherwise
+            n = ctypes.c_size_t(0)
+            _capi.check(_capi.lib().pkvd_sample_workspace_bytes(B, vocab, ctypes.byref(n)))
+            self.sample_workspace = torch.zeros(max(int(n.value), 16), dtype=torch.uint8, device=dev)
         self.temperature.fill_(1.0)
         self.top_p.fill_(1.0)
         self.slots = torch.empty(B, dtype=torch.int64, device=dev)
@@ -63,7 +74,7 @@ class DecodeStep:
         self.cache = _capi.cache_desc(k_cache, v_cache)
         self.graph = None
         self.host_graph = None
-        self.kernels_per_step = 4     # slot mapping + store, partition, merge, sample
+        self.kernels_per_step = 5 if self.extras else 4   # store, partition, merge, sample (+ extras)
 
     def enqueue(self, stream=None) -> None:
         L = _capi.lib()
@@ -86,6 +97,13 @@ class DecodeStep:
     def _enqueue_sample(self, L, s) -> None:
         p = _capi.ptr
         V = self.logits.shape[1]
+        if self.extras:
+            _capi.check(L.pkvd_sample_ex(p(self.token_ids), p(self.logits), _capi.dtype_code(self.logits.dtype),
+                                         self.B, V, self.logits.stride(0), p(self.temperature), p(self.top_k),
+                                         p(self.top_p), p(self.seeds), p(self.offsets), p(self.mask_words),
+                                         self.mask_words.shape[1], p(self.token_prob), p(self.top_probs),
+                                         p(self.top_ids), p(self.sample_workspace), self.sample_workspace.numel(), s))
+            return
         _capi.check(L.pkvd_sample(p(self.token_ids), p(self.logits), _capi.dtype_code(self.logits.dtype),
                                   self.B, V, self.logits.stride(0), p(self.temperature), p(self.top_k),
                                   p(self.top_p), p(self.seeds), p(self.offsets), None, 0, s))

@@ -250,3 +250,108 @@ def test_windowed_path_branches_match_oracle(name):
         if int(tok[i]) != ref and not _exempt(info, float(np.float32(p))):
             bad += 1
     assert bad == 0
+
+
+# ---- sample_token extras (NEXT f2): mask, token_prob, top-8
+
+def _extras_rows(name, R, V, dtype, rng):
+    if name == "normal":
+        x = rng.standard_normal((R, V)) * 2.0
+    elif name == "bf16_ties":
+        x = np.round(rng.standard_normal((R, V)) * 2.0, 1)
+    else:
+        raise KeyError(name)
+    return torch.from_numpy(x.astype(np.float32)).to(dtype)
+
+
+@pytest.mark.parametrize("dtype,V,case", [(torch.float16, 151936, "normal"), (torch.bfloat16, 65536, "bf16_ties"),
+                                          (torch.float32, 5000, "normal"), (torch.bfloat16, 2048, "normal")])
+def test_sample_ex_matches_oracle(dtype, V, case):
+    pk = require_gpu()
+    rng = np.random.default_rng(31)
+    R = 12
+    logits = _extras_rows(case, R, V, dtype, rng)
+    T = rng.choice([0.0, 0.6, 1.0, 1.4], R).astype(np.float32)
+    K = rng.choice([0, 5, 50, 300], R).astype(np.int32)
+    P = rng.choice([1.0, 0.9, 0.5], R).astype(np.float32)
+    allowed = rng.random((R, V)) > rng.choice([0.0, 0.3, 0.9], R)[:, None]
+    allowed[3] = False                                     # a row with nothing allowed
+    T[3] = 0.8
+    T[4] = 0.0
+    allowed[4] = rng.random(V) > 0.5                        # a greedy row with a mask
+    S = rng.integers(0, 2**62, R, dtype=np.int64)
+    O = rng.integers(0, 2**30, R, dtype=np.int64)
+    mask_words = pk.pack_mask(torch.from_numpy(allowed)).to(DEV)
+    tok, tp, p8, i8 = pk.sample_ex(logits.to(DEV), torch.from_numpy(T).to(DEV), torch.from_numpy(K).to(DEV),
+                                   torch.from_numpy(P).to(DEV), torch.from_numpy(S).to(DEV),
+                                   torch.from_numpy(O).to(DEV), mask_words=mask_words)
+    tok, tp, p8, i8 = tok.cpu().numpy(), tp.cpu().numpy(), p8.cpu().numpy(), i8.cpu().numpy()
+    # the ids equal plain sampling on the same inputs with masked logits at -inf
+    x = logits.double().numpy()
+    checked = 0
+    for r in range(R):
+        (rt, rp, r8p, r8i), info = oracle.sampler.sample_outputs(x[r], float(T[r]), int(K[r]), float(P[r]), int(S[r]),
+                                                                  int(O[r]), mask=allowed[r], return_info=True)
+        if r == 3:                                          # nothing allowed: uniform draw
+            assert 0 <= tok[r] < V and abs(tp[r] - 1.0 / V) < 1e-9 and i8[r].tolist() == list(range(8))
+            continue
+        if int(tok[r]) != rt:
+            assert _exempt(info, float(P[r]))
+            continue
+        assert allowed[r, tok[r]]
+        np.testing.assert_allclose(tp[r], rp, rtol=1e-5, atol=1e-30)
+        assert i8[r].tolist() == r8i.tolist()
+        np.testing.assert_allclose(p8[r], r8p, rtol=1e-5, atol=1e-30)
+        checked += 1
+    assert checked >= R - 3
+
+
+def test_all_allowed_mask_gives_the_same_ids_as_plain_sampling():
+    pk = require_gpu()
+    si = workloads.make_sampler_inputs(configs.QWEN3)
+    T, k, p, s, o = _dev_params(si)
+    L = si.logits.to(DEV)
+    plain = pk.sample(L, T, k, p, s, o)
+    words = pk.pack_mask(torch.ones(L.shape, dtype=torch.bool)).to(DEV)
+    masked, _, _, _ = pk.sample_ex(L, T, k, p, s, o, mask_words=words, with_probs=False)
+    assert torch.equal(plain, masked)
+
+
+def test_masked_ids_are_never_drawn_chi_square():
+    pk = require_gpu()
+    rng = np.random.default_rng(32)
+    V, R = 40, 100_000
+    row = torch.from_numpy((rng.standard_normal(V) * 1.5).astype(np.float32)).to(torch.bfloat16)
+    allowed = torch.from_numpy(rng.random(V) > 0.4)
+    logits = row.unsqueeze(0).repeat(R, 1).to(DEV)
+    words = pk.pack_mask(allowed.unsqueeze(0).repeat(R, 1)).to(DEV)
+    tok, _, _, _ = pk.sample_ex(logits, torch.full((R,), 0.9, device=DEV), torch.zeros(R, dtype=torch.int32, device=DEV),
+                                torch.full((R,), 0.95, device=DEV), torch.full((R,), 5, dtype=torch.int64, device=DEV),
+                                torch.arange(R, dtype=torch.int64, device=DEV), mask_words=words, with_probs=False)
+    tok = tok.cpu().numpy()
+    probs = oracle.sampler.filtered_probs(row.double().numpy(), float(np.float32(0.9)), 0, float(np.float32(0.95)),
+                                          allowed.numpy())
+    assert np.all(allowed.numpy()[tok]) and np.all(probs[tok] > 0)
+    support = np.nonzero(probs > 0)[0]
+    counts = np.bincount(tok, minlength=V)[support]
+    expected = probs[support] * R
+    keep = expected >= 5
+    obs = np.append(counts[keep], counts[~keep].sum())
+    exp = np.append(expected[keep], expected[~keep].sum())
+    if exp[-1] == 0:
+        obs, exp = obs[:-1], exp[:-1]
+    assert stats.chisquare(obs, exp).pvalue > 1e-3
+
+
+def test_nothing_allowed_draws_uniformly():
+    pk = require_gpu()
+    V, R = 24, 60_000
+    logits = torch.randn(R, V, device=DEV).to(torch.float16)
+    words = pk.pack_mask(torch.zeros(R, V, dtype=torch.bool)).to(DEV)
+    tok, tp, _, i8 = pk.sample_ex(logits, torch.ones(R, device=DEV), torch.zeros(R, dtype=torch.int32, device=DEV),
+                                  torch.ones(R, device=DEV), torch.full((R,), 9, dtype=torch.int64, device=DEV),
+                                  torch.arange(R, dtype=torch.int64, device=DEV), mask_words=words)
+    counts = np.bincount(tok.cpu().numpy(), minlength=V)
+    assert stats.chisquare(counts, np.full(V, R / V)).pvalue > 1e-3
+    assert torch.allclose(tp, torch.full_like(tp, 1.0 / V))
+    assert torch.equal(i8[0].cpu(), torch.arange(8, dtype=torch.int32))

@@ -96,3 +96,34 @@ def test_host_staged_step_matches_device_step():
     torch.cuda.synchronize()
     assert torch.equal(h["token_ids"], tok_ref.cpu())
     assert step.err.item() == 0
+
+
+def test_step_with_sampler_extras_matches_the_eager_calls():
+    pk = require_gpu()
+    cfg = configs.NANOCHAT
+    w = workloads.make_workload(cfg, device=DEV)
+    lay = w.layout
+    kc, vc = w.cache[0, lay.layer], w.cache[1, lay.layer]
+    step = pk.DecodeStep(kc, vc, lay.num_seqs, cfg.num_q_heads, lay.max_blocks_per_seq,
+                         lay.max_context_len, cfg.vocab, w.logits.dtype, w.scale, extras=True)
+    step.q.copy_(w.q)
+    step.k_new.copy_(w.k_new)
+    step.v_new.copy_(w.v_new)
+    step.block_tables.copy_(torch.from_numpy(lay.block_tables))
+    step.context_lens.copy_(torch.from_numpy(lay.context_lens))
+    step.logits.copy_(w.logits)
+    step.temperature.copy_(torch.from_numpy(w.temperature))
+    step.top_k.copy_(torch.from_numpy(w.top_k))
+    step.top_p.copy_(torch.from_numpy(w.top_p))
+    step.seeds.copy_(torch.from_numpy(w.seeds.view(np.int64)))
+    g = torch.Generator().manual_seed(3)
+    step.mask_words.copy_(pk.pack_mask(torch.rand(lay.num_seqs, cfg.vocab, generator=g) > 0.2))
+    step.capture()
+    step.replay()
+    torch.cuda.synchronize()
+    tok, tp, p8, i8 = pk.sample_ex(step.logits, step.temperature, step.top_k, step.top_p, step.seeds,
+                                   step.offsets, mask_words=step.mask_words)
+    torch.cuda.synchronize()
+    assert torch.equal(step.token_ids, tok) and torch.equal(step.token_prob, tp)
+    assert torch.equal(step.top_probs, p8) and torch.equal(step.top_ids, i8)
+    assert step.kernels_per_step == 5 and step.err.item() == 0

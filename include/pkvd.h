@@ -28,7 +28,9 @@
  *     (NULL = legacy default stream).  Every call only enqueues work on
  *     `stream` and returns; nothing synchronises, nothing allocates, no
  *     state is kept between calls.  The caller owns every buffer, including
- *     workspaces, and may capture the calls in a CUDA graph.
+ *     workspaces, and may capture the calls in a CUDA graph.  (The one
+ *     exception is the host block manager below: an object the caller
+ *     creates and destroys, touched by host calls only.)
  *   - Argument checks run on the host before anything is enqueued and return
  *     a status code; the library never aborts, exits or traps.
  *   - `err_flag`, where present, is an optional device int32.  Kernels OR
@@ -54,7 +56,8 @@ typedef enum {
   PKVD_UNSUPPORTED_DTYPE = 2,
   PKVD_UNSUPPORTED_SHAPE = 3,    /* head_dim, group size, block size, alignment */
   PKVD_WORKSPACE_TOO_SMALL = 4,
-  PKVD_CUDA_ERROR = 5            /* a CUDA runtime call failed (launch, query) */
+  PKVD_CUDA_ERROR = 5,           /* a CUDA runtime call failed (launch, query) */
+  PKVD_NO_SPACE = 6              /* block manager: not enough free blocks (nothing changed) */
 } pkvd_status;
 
 typedef enum { PKVD_F32 = 0, PKVD_F16 = 1, PKVD_BF16 = 2 } pkvd_dtype;
@@ -302,6 +305,66 @@ pkvd_status pkvd_sample_ex(int32_t* token_ids, const void* logits, int32_t dtype
                            const uint32_t* mask, int64_t mask_words_per_row,
                            float* token_prob, float* top_probs, int32_t* top_ids,
                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Host block manager -- the allocation side of the paged cache (nano-vllm
+ * "Model Runner" notes, section "prepare Prefill": schedule-time CPU
+ * bookkeeping that fills each sequence's block table and counts its
+ * prefix-cached tokens; nanochat "04 · Engine 推理与工具调用", sections 2-3:
+ * one prefill cloned N ways, here by sharing blocks).  Host memory and host
+ * calls only; one object per cache, not thread-safe.
+ *   - free blocks form a FIFO (0 .. num_blocks-1 at the start): allocation
+ *     takes the front, a block whose reference count drops to 0 goes to the
+ *     back and keeps its content key until it is handed out again;
+ *   - a full block is keyed by (the block before it in the table, or -1, and
+ *     its block_size token ids); a prompt reuses its registered full blocks
+ *     in order up to the first miss, never the block holding its last token;
+ *   - a token written into a shared last block first gets a fresh copy of it
+ *     (copy-on-write: the caller copies the rows with pkvd_copy_blocks);
+ *   - a request that needs more free blocks than there are returns
+ *     PKVD_NO_SPACE and changes nothing.
+ */
+typedef struct pkvd_block_manager pkvd_block_manager;
+
+pkvd_status pkvd_bm_create(int32_t num_blocks, int32_t block_size, pkvd_block_manager** out);
+void pkvd_bm_destroy(pkvd_block_manager* bm);
+/* Free blocks; -1 for a NULL manager. */
+int32_t pkvd_bm_num_free(const pkvd_block_manager* bm);
+/* Reference count of one block; -1 if out of range. */
+int32_t pkvd_bm_ref_count(const pkvd_block_manager* bm, int32_t block);
+
+/* A new prompt of num_tokens token ids (host array): writes its block table
+ * (host, at most max_blocks entries), the block count and the number of
+ * leading tokens already cached (a multiple of block_size). */
+pkvd_status pkvd_bm_allocate(pkvd_block_manager* bm, const int32_t* tokens, int32_t num_tokens,
+                             int32_t* block_table, int32_t max_blocks, int32_t* num_blocks,
+                             int32_t* cached_tokens);
+
+/* The sequence grew by one token: tokens holds all num_tokens ids, the table
+ * the blocks of the first num_tokens - 1 (*num_blocks of them; updated in
+ * place).  When the new token lands in a shared block, *copy_src / *copy_dst
+ * / *copy_rows name the copy-on-write copy to run before the store (else
+ * -1, -1, 0). */
+pkvd_status pkvd_bm_append(pkvd_block_manager* bm, const int32_t* tokens, int32_t num_tokens,
+                           int32_t* block_table, int32_t* num_blocks, int32_t max_blocks,
+                           int32_t* copy_src, int32_t* copy_dst, int32_t* copy_rows);
+
+/* A clone of a sequence: every block of the table gains a reference (the
+ * caller keeps a copy of the table for the clone). */
+pkvd_status pkvd_bm_fork(pkvd_block_manager* bm, const int32_t* block_table, int32_t num_blocks);
+
+/* A sequence ends: every block of its table loses a reference (last first). */
+pkvd_status pkvd_bm_release(pkvd_block_manager* bm, const int32_t* block_table, int32_t num_blocks);
+
+/*
+ * pkvd_copy_blocks -- the device side of copy-on-write: for each i < count,
+ * the first rows[i] token rows of block src[i] (K and V, every head) are
+ * copied to block dst[i].  src, dst, rows: device int32 [count].
+ * Device errors: a block id outside the pool or rows outside [0, block_size]
+ * sets PKVD_ERR_BLOCK_ID and that copy is skipped.
+ */
+pkvd_status pkvd_copy_blocks(const pkvd_cache* cache, const int32_t* src, const int32_t* dst,
+                             const int32_t* rows, int32_t count, void* stream, int32_t* err_flag);
 
 #ifdef __cplusplus
 }

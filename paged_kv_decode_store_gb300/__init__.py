@@ -22,8 +22,9 @@ from ._capi import (LIB_PATH, PATH_AUTO, PATH_FMA, PATH_MMA, ERR_BLOCK_ID, ERR_S
                     ERR_CONTEXT, ERR_TIMEOUT, PkvdCache, PkvdError, lib, check, dtype_code,
                     stream_handle, cache_desc, ptr)
 from .step import DecodeStep  # noqa: F401
+from .block_manager import BlockManager  # noqa: F401
 
-__all__ = ["slot_mapping", "kv_store", "kv_store_paged", "sample_ex", "pack_mask", "paged_decode_attention", "decode_workspace_bytes",
+__all__ = ["BlockManager", "copy_blocks", "slot_mapping", "kv_store", "kv_store_paged", "sample_ex", "pack_mask", "paged_decode_attention", "decode_workspace_bytes",
            "sample", "DecodeStep", "PkvdError", "lib"]
 
 
@@ -64,6 +65,15 @@ def kv_store_paged(k: torch.Tensor, v: torch.Tensor, block_tables: torch.Tensor,
     check(lib().pkvd_kv_store_paged(ptr(k), ptr(v), ptr(block_tables), block_tables.shape[1],
                                     ptr(context_lens), k.shape[0], ptr(slot_mapping), ctypes.byref(c),
                                     stream_handle(stream, k), _err_ptr(err)))
+
+
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src: torch.Tensor, dst: torch.Tensor,
+                rows: torch.Tensor, err: torch.Tensor | None = None, stream=None) -> None:
+    """Copy-on-write: the first rows[i] token rows of block src[i] -> block dst[i]
+    (K and V; src, dst, rows: int32 device tensors)."""
+    c = cache_desc(k_cache, v_cache)
+    check(lib().pkvd_copy_blocks(ctypes.byref(c), ptr(src), ptr(dst), ptr(rows), src.numel(),
+                                 stream_handle(stream, k_cache), _err_ptr(err)))
 
 
 def decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int, max_context_len: int,

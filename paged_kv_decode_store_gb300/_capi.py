@@ -10,6 +10,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkvd.so"
 
 PATH_AUTO, PATH_FMA, PATH_MMA = 0, 1, 2
 ERR_BLOCK_ID, ERR_SLOT, ERR_CONTEXT, ERR_TIMEOUT = 1, 2, 4, 8
+NO_SPACE = 6
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 c_void_p, c_int32, c_int64, c_size_t, c_float = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
@@ -39,6 +40,18 @@ SIGNATURES = {
                                 c_void_p, c_void_p]),
     "pkvd_kv_store_paged": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_int32, c_void_p,
                                       ctypes.POINTER(PkvdCache), c_void_p, c_void_p]),
+    "pkvd_bm_create": (c_int32, [c_int32, c_int32, ctypes.POINTER(c_void_p)]),
+    "pkvd_bm_destroy": (None, [c_void_p]),
+    "pkvd_bm_num_free": (c_int32, [c_void_p]),
+    "pkvd_bm_ref_count": (c_int32, [c_void_p, c_int32]),
+    "pkvd_bm_allocate": (c_int32, [c_void_p, c_void_p, c_int32, c_void_p, c_int32, ctypes.POINTER(c_int32),
+                                   ctypes.POINTER(c_int32)]),
+    "pkvd_bm_append": (c_int32, [c_void_p, c_void_p, c_int32, c_void_p, ctypes.POINTER(c_int32), c_int32,
+                                 ctypes.POINTER(c_int32), ctypes.POINTER(c_int32), ctypes.POINTER(c_int32)]),
+    "pkvd_bm_fork": (c_int32, [c_void_p, c_void_p, c_int32]),
+    "pkvd_bm_release": (c_int32, [c_void_p, c_void_p, c_int32]),
+    "pkvd_copy_blocks": (c_int32, [ctypes.POINTER(PkvdCache), c_void_p, c_void_p, c_void_p, c_int32, c_void_p,
+                                   c_void_p]),
     "pkvd_decode_workspace_bytes": (c_int32, [c_int32, c_int32, c_int32, c_int32, c_int32,
                                               ctypes.POINTER(c_size_t)]),
     "pkvd_paged_decode_attention": (c_int32, [c_void_p, c_void_p, ctypes.POINTER(PkvdCache), c_void_p,

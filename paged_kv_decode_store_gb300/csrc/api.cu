@@ -65,6 +65,7 @@ const char* pkvd_status_string(pkvd_status s) {
     case PKVD_UNSUPPORTED_SHAPE: return "unsupported shape or alignment";
     case PKVD_WORKSPACE_TOO_SMALL: return "workspace too small";
     case PKVD_CUDA_ERROR: return "CUDA runtime error";
+    case PKVD_NO_SPACE: return "no free block";
   }
   return "unknown status";
 }
@@ -106,6 +107,17 @@ pkvd_status pkvd_kv_store_paged(const void* k, const void* v, const int32_t* blo
   return from_cuda(launch_kv_store_paged(k, v, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                                          slot_mapping, *cache, esize(cache->dtype),
                                          static_cast<cudaStream_t>(stream), err_flag));
+}
+
+pkvd_status pkvd_copy_blocks(const pkvd_cache* cache, const int32_t* src, const int32_t* dst, const int32_t* rows,
+                             int32_t count, void* stream, int32_t* err_flag) {
+  if (count < 0) return PKVD_INVALID_ARG;
+  const pkvd_status cs = check_cache(cache, false);
+  if (cs != PKVD_OK) return cs;
+  if (count == 0) return PKVD_OK;
+  if (!src || !dst || !rows) return PKVD_INVALID_ARG;
+  return from_cuda(launch_copy_blocks(*cache, esize(cache->dtype), src, dst, rows, count,
+                                      static_cast<cudaStream_t>(stream), err_flag));
 }
 
 pkvd_status pkvd_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,

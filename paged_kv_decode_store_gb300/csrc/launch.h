@@ -58,6 +58,8 @@ cudaError_t launch_kv_store(const void* k, const void* v, const int64_t* slots, 
 cudaError_t launch_kv_store_paged(const void* k, const void* v, const int32_t* tables, int max_blocks,
                                   const int32_t* ctx, int num_seqs, int64_t* slots_out, const pkvd_cache& c,
                                   int elem_bytes, cudaStream_t stream, int32_t* err);
+cudaError_t launch_copy_blocks(const pkvd_cache& c, int elem_bytes, const int32_t* src, const int32_t* dst,
+                               const int32_t* rows, int count, cudaStream_t stream, int32_t* err);
 
 // Per-row cut parameters the sampler leaves for the extras kernel:
 // [0] flags (kRowGreedy, kRowUniform, kRowTopK), [1] nucleus threshold key

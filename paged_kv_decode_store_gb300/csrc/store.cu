@@ -138,6 +138,43 @@ cudaError_t launch_kv_store(const void* k, const void* v, const int64_t* slots, 
                     c.block_stride, c.token_stride, c.head_stride, elem_bytes, err);
 }
 
+// Copy-on-write of shared blocks: CTA (i, kv) copies the first rows[i]
+// token rows of block src[i] to block dst[i] in the K (kv = 0) or V cache,
+// 16-byte vectors over every head of each row.
+__global__ void copy_blocks_kernel(uint8_t* __restrict__ kc, uint8_t* __restrict__ vc, const int32_t* __restrict__ src,
+                                   const int32_t* __restrict__ dst, const int32_t* __restrict__ rows,
+                                   int64_t num_blocks, int block_size, int num_heads, int head_dim,
+                                   int64_t block_stride, int64_t token_stride, int64_t head_stride, int elem_bytes,
+                                   int32_t* err) {
+  pdl_wait();
+  pdl_trigger();
+  const int i = blockIdx.x;
+  const int s = src[i], d = dst[i], n = rows[i];
+  if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks || n < 0 || n > block_size) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) flag_error(err, PKVD_ERR_BLOCK_ID);
+    return;
+  }
+  uint8_t* base = blockIdx.y ? vc : kc;
+  const int vec_elems = 16 / elem_bytes;
+  const int per_head = head_dim / vec_elems;
+  const int per_row = num_heads * per_head;
+  for (int idx = threadIdx.x; idx < n * per_row; idx += blockDim.x) {
+    const int t = idx / per_row, rem = idx % per_row;
+    const int h = rem / per_head, c = rem % per_head;
+    const int64_t off = ((int64_t)t * token_stride + (int64_t)h * head_stride + (int64_t)c * vec_elems) * elem_bytes;
+    const uint4 val = *reinterpret_cast<const uint4*>(base + (int64_t)s * block_stride * elem_bytes + off);
+    *reinterpret_cast<uint4*>(base + (int64_t)d * block_stride * elem_bytes + off) = val;
+  }
+}
+
+cudaError_t launch_copy_blocks(const pkvd_cache& c, int elem_bytes, const int32_t* src, const int32_t* dst,
+                               const int32_t* rows, int count, cudaStream_t stream, int32_t* err) {
+  if (count == 0) return cudaSuccess;
+  return launch_pdl(copy_blocks_kernel, dim3(count, 2), dim3(256), 0, stream, static_cast<uint8_t*>(c.k_base),
+                    static_cast<uint8_t*>(c.v_base), src, dst, rows, c.num_blocks, c.block_size, c.num_kv_heads,
+                    c.head_dim, c.block_stride, c.token_stride, c.head_stride, elem_bytes, err);
+}
+
 cudaError_t launch_kv_store_paged(const void* k, const void* v, const int32_t* tables, int max_blocks,
                                   const int32_t* ctx, int num_seqs, int64_t* slots_out, const pkvd_cache& c,
                                   int elem_bytes, cudaStream_t stream, int32_t* err) {

@@ -146,3 +146,77 @@ def test_kv_store_paged_flags_and_skips_like_slot_mapping():
     kc2, vc2 = torch.zeros_like(kc), torch.zeros_like(vc)
     pk.kv_store_paged(k, v, tables, ctx, kc2, vc2)
     assert torch.equal(kc2, kc) and torch.equal(vc2, vc)
+
+
+@pytest.mark.parametrize("dtype,H,D,bs", [(torch.float16, 16, 64, 256), (torch.bfloat16, 8, 128, 16),
+                                          (torch.float32, 2, 64, 16)])
+def test_copy_blocks_copies_the_leading_rows_bit_exactly(dtype, H, D, bs):
+    pk = require_gpu()
+    nb = 40
+    g = torch.Generator(device="cpu").manual_seed(8)
+    kc = torch.randn(nb, bs, H, D, generator=g).to(dtype).to(DEV)
+    vc = torch.randn(nb, bs, H, D, generator=g).to(dtype).to(DEV)
+    src = torch.tensor([3, 7, 11, 0], dtype=torch.int32)
+    dst = torch.tensor([20, 21, 22, 23], dtype=torch.int32)
+    rows = torch.tensor([bs - 1, 1, 0, bs], dtype=torch.int32)
+    k0, v0 = kc.clone(), vc.clone()
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pk.copy_blocks(kc, vc, src.to(DEV), dst.to(DEV), rows.to(DEV), err=err)
+    torch.cuda.synchronize()
+    ek, ev = k0.clone(), v0.clone()
+    for s_, d_, r_ in zip(src.tolist(), dst.tolist(), rows.tolist()):
+        ek[d_, :r_] = k0[s_, :r_]
+        ev[d_, :r_] = v0[s_, :r_]
+    assert torch.equal(kc, ek) and torch.equal(vc, ev) and err.item() == 0
+    bad = torch.tensor([nb], dtype=torch.int32, device=DEV)
+    pk.copy_blocks(kc, vc, bad, dst[:1].to(DEV), rows[:1].to(DEV), err=err)
+    torch.cuda.synchronize()
+    assert err.item() == pk.ERR_BLOCK_ID and torch.equal(kc, ek)
+
+
+def test_block_manager_fork_and_copy_on_write_on_the_device():
+    """Two clones of a prompt share its blocks; each decodes its own token into
+    the shared partial block after the copy-on-write copy, and attention over
+    either sequence equals the oracle over that sequence's own K/V."""
+    pk = require_gpu()
+    import oracle as orc
+    nb, bs, H, D, G = 16, 16, 2, 64, 2
+    g = torch.Generator(device="cpu").manual_seed(9)
+    kc = torch.full((nb, bs, H, D), float("nan"), dtype=torch.float16, device=DEV)
+    vc = torch.full_like(kc, float("nan"))
+    bm = pk.BlockManager(nb, bs)
+    prompt = list(range(100, 137))                            # 37 tokens: blocks 0, 1 full, 2 partial
+    table, cached = bm.allocate(prompt)
+    assert cached == 0
+    kv = {p: (torch.randn(H, D, generator=g).half(), torch.randn(H, D, generator=g).half()) for p in range(40)}
+    for p in range(len(prompt)):                              # the prompt's K/V rows, through the store kernel
+        t_ = torch.tensor([table + [-1] * 2], dtype=torch.int32, device=DEV)
+        pk.kv_store_paged(kv[p][0].unsqueeze(0).to(DEV), kv[p][1].unsqueeze(0).to(DEV), t_,
+                          torch.tensor([p + 1], dtype=torch.int32, device=DEV), kc, vc)
+    clone = bm.fork(table)
+    seqs = {"a": (prompt + [1], table), "b": (prompt + [2], clone)}
+    own = {"a": torch.randn(H, D, generator=g).half(), "b": torch.randn(H, D, generator=g).half()}
+    q = torch.randn(2, H * G, D, generator=g).half()
+    outs, tabs = {}, {}
+    for name, (toks, tab) in seqs.items():
+        t2, cp = bm.append(toks, tab)
+        if cp is not None:
+            pk.copy_blocks(kc, vc, *(torch.tensor([x], dtype=torch.int32, device=DEV) for x in cp))
+        tabs[name] = t2
+        tt = torch.tensor([t2 + [-1] * 2], dtype=torch.int32, device=DEV)
+        ctx = torch.tensor([len(toks)], dtype=torch.int32, device=DEV)
+        pk.kv_store_paged(own[name].unsqueeze(0).to(DEV), own[name].unsqueeze(0).to(DEV), tt, ctx, kc, vc)
+    # the first clone copied the shared partial block; the second then owned the original alone
+    assert tabs["a"][:2] == table[:2] and tabs["a"][2] != table[2] and tabs["b"] == table
+    for i, name in enumerate(["a", "b"]):
+        toks, _ = seqs[name]
+        tt = torch.tensor([tabs[name] + [-1] * 2], dtype=torch.int32, device=DEV)
+        ctx = torch.tensor([len(toks)], dtype=torch.int32, device=DEV)
+        out = pk.paged_decode_attention(q[i:i + 1].to(DEV), kc, vc, tt, ctx, len(toks), 0.125)
+        K = torch.stack([kv[p][0] for p in range(len(prompt))] + [own[name]]).double().numpy()
+        V = torch.stack([kv[p][1] for p in range(len(prompt))] + [own[name]]).double().numpy()
+        kc_ref = K[:, None]                                   # [ctx, 1(row), H, D] as one-row blocks
+        ref = orc.attention.decode_attention(q[i:i + 1].double().numpy(), kc_ref, V[:, None],
+                                             np.arange(len(toks))[None, :], np.array([len(toks)]), 0.125)
+        rel = (out.double().cpu().numpy() - ref).__abs__().max() / np.abs(ref).max()
+        assert rel < 2e-2 and torch.isfinite(out).all()

@@ -38,9 +38,13 @@ def _check(bm, live, content):
             refs[b] += 1
         assert content.read(table, len(toks)) == toks          # every sequence reads its own tokens
         assert len(table) == -(-len(toks) // bm.bs)
-    assert refs == bm.ref
-    assert sorted(bm.free) == [b for b in range(bm.nb) if refs[b] == 0]
-    assert len(set(bm.free)) == len(bm.free)
+    if hasattr(bm, "ref"):                                    # the oracle: its lists directly
+        assert refs == bm.ref
+        assert sorted(bm.free) == [b for b in range(bm.nb) if refs[b] == 0]
+        assert len(set(bm.free)) == len(bm.free)
+    else:                                                      # the native manager: its queries
+        assert refs == [bm.ref_count(b) for b in range(bm.nb)]
+        assert bm.num_free() == sum(1 for r in refs if r == 0)
 
 
 def run_random_workload(make_bm, seed, steps=400, nb=48, bs=4, check=True):
@@ -145,3 +149,28 @@ def test_no_space_changes_nothing():
     toks += [10, 11, 12]
     assert bm.append(toks[:11], t2)[0] == t2 and bm.append(toks[:12], t2)[0] == t2
     assert bm.append(toks[:13], t2) == (None, None)   # a 4th block: none free
+
+
+# ---- the native manager against the oracle (host code: no GPU needed)
+
+def test_native_block_manager_matches_the_oracle_step_by_step():
+    import paged_kv_decode_store_gb300 as pk
+    for seed in range(8):
+        for nb, bs in [(48, 4), (20, 2), (96, 16)]:
+            want = run_random_workload(BlockManager, seed, nb=nb, bs=bs, check=False)
+            got = run_random_workload(pk.BlockManager, seed, nb=nb, bs=bs, check=True)
+            assert got == want
+
+
+def test_native_block_manager_rejects_bad_tables():
+    import paged_kv_decode_store_gb300 as pk
+    from paged_kv_decode_store_gb300 import _capi
+    bm = pk.BlockManager(4, 2)
+    t, _ = bm.allocate([1, 2, 3])
+    import pytest
+    with pytest.raises(_capi.PkvdError):
+        bm.release([t[0], 9])                      # a block outside the pool: nothing released
+    assert bm.ref_count(t[0]) == 1
+    with pytest.raises(_capi.PkvdError):
+        bm.fork([3])                               # an unreferenced block cannot be cloned
+    assert bm.allocate([1] * 20) is None and bm.num_free() == 2

@@ -398,6 +398,81 @@ def config_block(cfg, lay, window=0, extras=False):
             "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MB write, then {FLUSH_BYTES >> 20} MB read)"}
 
 
+def peak_hbm():
+    """(HBM copy peak in GB/s, "measured" or "fallback")."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peak = json.load(open(path)).get("hbm_gbs") if os.path.exists(path) else None
+    return (peak, "measured") if peak else (6800.0, "fallback")
+
+
+def run_block_manager_bench(args):
+    """The nanochat clone scenario on the host block manager (a 1024-token
+    prompt, 16 forks, 255 decode appends each with copy-on-write on the first,
+    release), timed through the Python binding, and the copy-on-write kernel
+    moving whole blocks on the GPU."""
+    import paged_kv_decode_store_gb300 as pk
+    bs, nclone, ndec = 16, 16, 255
+    rng = np.random.default_rng(7)
+    prompt = rng.integers(0, 65536, 1024 + 7).tolist()          # 64 full blocks + a partial one
+    t_alloc, t_fork, t_app, t_rel, n_app, copies = [], [], [], [], 0, 0
+    for _ in range(max(args.steps, 3)):
+        bm = pk.BlockManager(4096, bs)
+        t0 = time.perf_counter()
+        table, _ = bm.allocate(prompt)
+        t_alloc.append(time.perf_counter() - t0)
+        seqs = []
+        t0 = time.perf_counter()
+        for _ in range(nclone):
+            seqs.append(bm.fork(table))
+        t_fork.append((time.perf_counter() - t0) / nclone)
+        bufs = [np.zeros(len(prompt) + ndec, dtype=np.int32) for _ in range(nclone)]   # token buffers
+        for b in bufs:
+            b[:len(prompt)] = prompt
+        t0 = time.perf_counter()
+        for d in range(ndec):
+            n = len(prompt) + d + 1
+            for i in range(nclone):
+                bufs[i][n - 1] = d
+                seqs[i], cp = bm.append(bufs[i][:n], seqs[i])
+                copies += cp is not None
+                n_app += 1
+        t_app.append(time.perf_counter() - t0)
+        t0 = time.perf_counter()
+        for tab in seqs:
+            bm.release(tab)
+        bm.release(table)
+        t_rel.append((time.perf_counter() - t0) / (nclone + 1))
+        bm.close()
+    # the copy kernel: 4096 whole blocks of the nanochat cache shape (bf16, 8 heads x 128)
+    dev = "cuda"
+    nb = 8192
+    kc = torch.zeros(nb, bs, 8, 128, dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    n = 4096
+    src = torch.arange(n, dtype=torch.int32, device=dev)
+    dst = src + n
+    rows = torch.full((n,), bs, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        pk.copy_blocks(kc, vc, src, dst, rows)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(10):
+        pk.copy_blocks(kc, vc, src, dst, rows)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / 10
+    moved = 2 * n * 2 * kc[0].numel() * kc.element_size()       # K and V, read + write
+    line = {"metric": "block manager op rates (host) and copy-on-write bandwidth (GPU)",
+            "scenario": f"1031-token prompt, {nclone} forks, {ndec} appends each, block_size {bs}, 4096 blocks",
+            "host_us": {"allocate": 1e6 * statistics.median(t_alloc), "fork": 1e6 * statistics.median(t_fork),
+                        "append": 1e6 * sum(t_app) / n_app, "release": 1e6 * statistics.median(t_rel)},
+            "copy_on_write_copies": copies, "timing": "through the Python binding (ctypes)",
+            "copy_blocks": {"blocks": n, "ms": ms, "GB/s": moved / (ms * 1e-3) / 1e9,
+                            "frac_of_copy_peak": moved / (ms * 1e-3) / 1e9 / peak_hbm()[0]}}
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -410,6 +485,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extras", action="store_true",
                     help="sampler extras: a 5 %% id mask, token_prob and the top-8 probabilities and ids")
+    ap.add_argument("--block-manager", action="store_true",
+                    help="host block manager op rates and the copy-on-write kernel's bandwidth (one JSON line)")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding-window attention over the newest W positions (0: none)")
     args = ap.parse_args()
@@ -419,6 +496,10 @@ def main():
 
     if args.impl == "reference":
         run_reference(args, cfg, ws, rank, local)
+        return
+    if args.block_manager:
+        if rank == 0:
+            run_block_manager_bench(args)
         return
 
     import paged_kv_decode_store_gb300 as pk
@@ -462,13 +543,7 @@ def main():
         return
     ms_per_step = total_ms / args.steps
     value = ws * nbytes["step"] / (ms_per_step * 1e-3) / 1e9
-    peaks = {}
-    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(pk_path):
-        peaks = json.load(open(pk_path))
-    peak = peaks.get("hbm_gbs")
-    peak_src = "measured" if peak else "fallback"
-    peak = peak or 6800.0
+    peak, peak_src = peak_hbm()
     attn_gbs = nbytes["attention"] / (attn_mean * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,

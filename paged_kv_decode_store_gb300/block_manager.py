@@ -13,7 +13,11 @@ from . import _capi
 
 
 def _arr(values, extra=0):
-    """int32 host array (numpy) with `extra` spare slots; returns (array, pointer)."""
+    """int32 host array (numpy) with `extra` spare slots; returns (array, pointer).
+    A contiguous int32 numpy array with no spare slots is passed as it is."""
+    if extra == 0 and isinstance(values, np.ndarray) and values.dtype == np.int32 and values.flags.c_contiguous \
+            and values.size > 0:
+        return values, values.ctypes.data_as(ctypes.c_void_p)
     a = np.zeros(len(values) + extra + 1, dtype=np.int32)
     a[:len(values)] = np.asarray(values, dtype=np.int64)
     return a, a.ctypes.data_as(ctypes.c_void_p)

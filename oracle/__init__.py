@@ -17,10 +17,15 @@ Every function restates, in the plainest form, what the pages define:
   Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11).
 * ``sampler``   -- temperature, top-k, nucleus cut (Grok-1 section 8.3.1
   ``top_p_filter``, restated in descending order), Gumbel-max draw.
+* ``prefill``   -- varlen prefill: slots of the scheduled tokens and causal
+  attention over cached prefix plus new rows (nano-vllm "Model Runner",
+  sections "prefix cache", "prepare Prefill", "prefill and decode").
+* ``block_manager`` -- block allocation with prefix sharing, forks and
+  copy-on-write (imported on its own by its tests).
 
 Pins: every function is checked by ``tests/test_oracle_*.py`` against
 worked examples the pages print, closed forms, brute force on tiny inputs,
 library routines and published known-answer vectors.  No function is left
 "parity unpinned".
 """
-from . import paging, store, attention, philox, sampler  # noqa: F401
+from . import paging, store, attention, philox, sampler, prefill  # noqa: F401

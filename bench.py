@@ -473,6 +473,194 @@ def run_block_manager_bench(args):
     print(json.dumps(line))
 
 
+# ----------------------------------------------------------------- prefill
+PREFILL_METRIC = "varlen paged prefill attention TFLOP/s (causal, prefix-cache hits)"
+
+PREFILL_ORACLE_SCRIPT = r"""
+import json, sys, time
+sys.path.insert(0, sys.argv[1])
+import numpy as np
+import oracle
+d = np.load(sys.argv[2])
+budget = float(sys.argv[3])
+cu_q, cu_k, tab, bs = d["cu_q"], d["cu_k"], d["tab"], int(d["bs"])
+kc, vc = d["kc"], d["vc"]
+slots = oracle.prefill.prefill_slot_mapping(tab, cu_q, cu_k, bs)
+oracle.store.kv_store(d["knew"], d["vnew"], slots, kc, vc)
+pairs = [tuple(int(x) for x in p) for p in d["pairs"]]
+t0 = time.perf_counter()
+done = 0
+while done < len(pairs) and time.perf_counter() - t0 < budget:
+    oracle.prefill.prefill_attention(d["q"], kc, vc, tab, cu_q, cu_k, float(d["scale"]),
+                                     pairs=pairs[done:done + 16])
+    done = min(done + 16, len(pairs))
+print(json.dumps({"pairs": done, "seconds": time.perf_counter() - t0}))
+"""
+
+
+def prefill_keys(cu_q, cu_k, window=0):
+    """Keys each new token attends to (causal, optional window), int64 [total_q]."""
+    out = []
+    for i in range(len(cu_q) - 1):
+        qn, kn = int(cu_q[i + 1] - cu_q[i]), int(cu_k[i + 1] - cu_k[i])
+        p = np.arange(kn - qn, kn, dtype=np.int64)
+        first = np.maximum(p + 1 - window, 0) if window > 0 else np.zeros_like(p)
+        out.append(p + 1 - first)
+    return np.concatenate(out) if out else np.zeros(0, np.int64)
+
+
+def prefill_oracle_sample(b, budget_s):
+    """The float64 oracle on random (token, head) pairs of the median-length
+    sequence, single-threaded, ~budget_s: (pairs done, seconds, FLOPs)."""
+    klen = b.k_lens
+    i = int(np.argsort(klen)[len(klen) // 2])
+    bs, D = b.cfg.block_size, b.cfg.head_dim
+    n = -(-int(klen[i]) // bs)
+    ids = torch.from_numpy(b.block_tables[i, :n].astype(np.int64))
+    q0, q1 = int(b.cu_seqlens_q[i]), int(b.cu_seqlens_q[i + 1])
+    rng = np.random.default_rng(3)
+    toks = rng.integers(0, q1 - q0, 4096)
+    heads = rng.integers(0, b.cfg.num_q_heads, 4096)
+    arrays = {"cu_q": np.array([0, q1 - q0]), "cu_k": np.array([0, int(klen[i])]),
+              "tab": np.arange(n, dtype=np.int64)[None, :], "bs": np.array(bs), "scale": np.array(b.scale),
+              "kc": b.cache[0].index_select(0, ids).double().numpy(),
+              "vc": b.cache[1].index_select(0, ids).double().numpy(),
+              "knew": b.k_new[q0:q1].double().numpy(), "vnew": b.v_new[q0:q1].double().numpy(),
+              "q": b.q[q0:q1].double().numpy(), "pairs": np.stack([toks, heads], 1)}
+    fd, path = tempfile.mkstemp(suffix=".npz")
+    os.close(fd)
+    np.savez(path, **arrays)
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-c", PREFILL_ORACLE_SCRIPT, ROOT, path, str(budget_s)],
+                       capture_output=True, text=True, env=env)
+    os.unlink(path)
+    if r.returncode:
+        raise RuntimeError(r.stderr[-2000:])
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    keys = prefill_keys(arrays["cu_q"], arrays["cu_k"])
+    flops = 4.0 * D * float(keys[toks[:res["pairs"]]].sum())
+    return res["pairs"], res["seconds"], flops
+
+
+def run_prefill_bench(args):
+    """One prefill step (varlen store + causal attention over the paged cache)
+    of a seeded batch, replayed as a CUDA graph, L2 flushed before each step."""
+    import paged_kv_decode_store_gb300 as pk
+    from workloads import prefill as wp
+    cfg = wp.PREFILL_CONFIGS[args.prefill]
+    b = wp.make_prefill_batch(cfg)
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    window = args.window
+    cache = b.cache.to(dev)
+    kc, vc = cache[0], cache[1]
+    d = {"q": b.q.to(dev), "k": b.k_new.to(dev), "v": b.v_new.to(dev),
+         "tables": torch.from_numpy(b.block_tables).to(dev), "cu_q": torch.from_numpy(b.cu_seqlens_q).to(dev),
+         "cu_k": torch.from_numpy(b.cu_seqlens_k).to(dev)}
+    out = torch.empty_like(d["q"])
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    maxq = b.max_seqlen_q
+
+    def store():
+        pk.kv_store_prefill(d["k"], d["v"], d["tables"], d["cu_q"], d["cu_k"], kc, vc, err=err)
+
+    def attend():
+        pk.prefill_attention(d["q"], kc, vc, d["tables"], d["cu_q"], d["cu_k"], maxq, b.scale, window=window,
+                             out=out, err=err)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        store()
+        attend()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g_step, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        store()
+        attend()
+    with torch.cuda.graph(g_attn):
+        attend()
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(graph, n):
+        st = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        en = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for j in range(n):
+            flush.add_(1)
+            st[j].record(stream)
+            graph.replay()
+            en[j].record(stream)
+        torch.cuda.synchronize()
+        return [x.elapsed_time(y) for x, y in zip(st, en)]
+
+    timed(g_step, args.warmup)
+    timed(g_attn, 3)
+    with ClockSampler(0) as clk:
+        step_ms = timed(g_step, args.steps)
+        attn_ms = timed(g_attn, args.steps)
+    clocks = clk.summary()
+
+    # end to end: pinned host inputs -> device, the step, the output -> pinned host
+    host_in = {k: t.cpu().pin_memory() for k, t in d.items()}
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    e2e = []
+    for j in range(args.warmup + args.steps):
+        flush.add_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k, t in host_in.items():
+            d[k].copy_(t, non_blocking=True)
+        g_step.replay()
+        host_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if j >= args.warmup:
+            e2e.append(e0.elapsed_time(e1))
+    if int(err.item()):
+        raise RuntimeError(f"prefill kernels flagged device errors {int(err.item())}")
+
+    keys = prefill_keys(b.cu_seqlens_q, b.cu_seqlens_k, window)
+    flops = 4.0 * cfg.num_q_heads * cfg.head_dim * float(keys.sum())
+    ms = statistics.mean(step_ms)
+    attn = statistics.mean(attn_ms)
+    e2e_ms = statistics.mean(e2e)
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = peaks.get("bf16_tflops") or 1900.0
+    achieved = flops / (attn * 1e-3) / 1e12
+    line = {
+        "metric": PREFILL_METRIC, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+        "config": {"workload": cfg.description + (f"; sliding window {window}" if window else ""),
+                   "name": cfg.name, "batch": cfg.num_seqs, "total_q": b.total_q,
+                   "q_len_mean": float(b.q_lens.mean()), "cached_mean": float((b.k_lens - b.q_lens).mean()),
+                   "max_seqlen_q": maxq, "q_heads": cfg.num_q_heads, "kv_heads": cfg.num_kv_heads,
+                   "head_dim": cfg.head_dim, "block_size": cfg.block_size,
+                   "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MB write, then "
+                         f"{FLUSH_BYTES >> 20} MB read)"},
+        "tokens_per_s": b.total_q / (ms * 1e-3), "attention_flops": flops, "attention_ms": attn,
+        "roofline": {"kernel": "prefill_attention_kernel (mma.sync m16n8k16, fp32 accumulation)",
+                     "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak,
+                     "peak_source": "measured bf16 burst" if peaks.get("bf16_tflops") else "fallback",
+                     "traffic": None},
+        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps, "clocks": clocks, "device_err_flag": 0,
+    }
+    if not args.no_cpu_baseline:
+        done, secs, cflops = prefill_oracle_sample(b, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": cflops / secs / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{done} random (token, head) rows of the median sequence, "
+                                          f"{secs:.1f} s, single thread"}
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -489,6 +677,9 @@ def main():
                     help="host block manager op rates and the copy-on-write kernel's bandwidth (one JSON line)")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding-window attention over the newest W positions (0: none)")
+    ap.add_argument("--prefill", default=None,
+                    choices=["qwen3_prefill", "grok1_prefill", "chunked_prefill"],
+                    help="time a varlen prefill step (store + causal attention) instead (one JSON line)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     cfg = configs.get(args.config)
@@ -500,6 +691,10 @@ def main():
     if args.block_manager:
         if rank == 0:
             run_block_manager_bench(args)
+        return
+    if args.prefill:
+        if rank == 0:
+            run_prefill_bench(args)
         return
 
     import paged_kv_decode_store_gb300 as pk

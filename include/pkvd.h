@@ -244,6 +244,72 @@ pkvd_status pkvd_paged_decode_attention_noalloc(void* out, const void* q, const 
                                                 int32_t num_seqs, int32_t num_q_heads, float scale,
                                                 void* stream, int32_t* err_flag);
 
+/*
+ * pkvd_kv_store_prefill -- the store of a varlen prefill batch (nano-vllm
+ * "Model Runner" notes, sections "prepare Prefill" and "prefix cache": the
+ * block table is filled before the step, and the step writes every newly
+ * scheduled token's K and V rows to the slot its position maps to).
+ * Sequence i owns new rows [cu_seqlens_q[i], cu_seqlens_q[i+1]) and has
+ * k_len_i = cu_seqlens_k[i+1] - cu_seqlens_k[i] tokens in all, the first
+ * k_len_i - q_len_i of them already cached (a prefix-cache hit or an earlier
+ * chunk); new row t of sequence i is position p = (k_len_i - q_len_i) +
+ * (t - cu_seqlens_q[i]) and goes to slot
+ *   block_tables[i][p / bs] * bs + p % bs,
+ * also written to slot_mapping[t] when slot_mapping is not NULL.
+ * Inputs: k, v [total_q, num_kv_heads, head_dim] contiguous, cache dtype,
+ *         16-byte aligned; cu_seqlens_q, cu_seqlens_k int32 [num_seqs + 1]
+ *         device arrays, non-decreasing, starting at 0; block_tables int32
+ *         [num_seqs, max_blocks_per_seq].
+ * Output: the cache rows; slot_mapping int64 [total_q] or NULL.
+ * Device errors: rows t >= cu_seqlens_q[num_seqs] are skipped (slot -1);
+ *         q_len > k_len or a position past the table sets PKVD_ERR_CONTEXT,
+ *         a block id outside [0, num_blocks) PKVD_ERR_BLOCK_ID; such rows
+ *         are skipped.
+ */
+pkvd_status pkvd_kv_store_prefill(const void* k, const void* v, const int32_t* block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t* cu_seqlens_q,
+                                  const int32_t* cu_seqlens_k, int32_t num_seqs, int32_t total_q,
+                                  int64_t* slot_mapping, const pkvd_cache* cache, void* stream,
+                                  int32_t* err_flag);
+
+/*
+ * pkvd_prefill_attention -- varlen causal attention of a prefill batch over
+ * the paged cache (nano-vllm "Model Runner" notes, sections "prefix cache"
+ * and "prefill and decode": cu_seqlens_q / cu_seqlens_k describe the batch,
+ * cu_seqlens_k[-1] > cu_seqlens_q[-1] when prefixes are cached, and prefill
+ * runs its own dense, compute-bound kernel).  New row t of sequence i at
+ * position p (as in pkvd_kv_store_prefill), query head h, kv head
+ * hk = h / G:
+ *   s_j = scale * <q[t,h,:], K_j>,  ws(p) <= j <= p,
+ *   K_j = K[block_tables[i][j / bs], j % bs, hk, :]   (V_j likewise)
+ *   out[t,h,:] = sum_j softmax(s)_j V_j,
+ * ws(p) = max(0, p + 1 - window) for window > 0, else 0.  The cache must
+ * already hold positions 0 .. k_len_i - 1 (run pkvd_kv_store_prefill first
+ * on the same stream).  Rows of the cache outside [ws, p] of some new token
+ * are never read.
+ * Inputs: q [total_q, num_q_heads, head_dim] contiguous, cache dtype,
+ *         16-byte aligned; cu_seqlens_q, cu_seqlens_k, block_tables as in
+ *         pkvd_kv_store_prefill; max_seqlen_q >= every q_len (host bound that
+ *         sizes the grid).
+ * Output: out [total_q, num_q_heads, head_dim], cache dtype, 4-byte
+ *         aligned; rows t >= cu_seqlens_q[num_seqs] are not written.
+ *         Tensor-core products with fp32 accumulation; the softmax weights
+ *         are rounded to the cache dtype for the second product.
+ * Requirements: cache dtype f16 or bf16 (PKVD_UNSUPPORTED_DTYPE for f32),
+ *         head_dim 64 or 128, num_q_heads % num_kv_heads == 0, group size
+ *         <= 128, num_seqs <= 65535, window >= 0.
+ * Device errors: q_len > k_len, cu_seqlens_q[i+1] > total_q, k_len past the
+ *         table or q_len > max_seqlen_q set PKVD_ERR_CONTEXT (that
+ *         sequence's rows, or in the last case its earliest rows, are not
+ *         written); a bad block id sets PKVD_ERR_BLOCK_ID (its rows read as
+ *         zeros).
+ */
+pkvd_status pkvd_prefill_attention(void* out, const void* q, const pkvd_cache* cache, const int32_t* block_tables,
+                                   int32_t max_blocks_per_seq, const int32_t* cu_seqlens_q,
+                                   const int32_t* cu_seqlens_k, int32_t num_seqs, int32_t total_q,
+                                   int32_t max_seqlen_q, int32_t num_q_heads, float scale, int32_t window,
+                                   void* stream, int32_t* err_flag);
+
 /* Workspace bytes of pkvd_sample_ex's optional outputs: 32 per row (host
  * only).  pkvd_sample itself needs none (it may get NULL, 0). */
 pkvd_status pkvd_sample_workspace_bytes(int32_t num_rows, int32_t vocab, size_t* bytes);

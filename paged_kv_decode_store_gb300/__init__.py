@@ -24,7 +24,8 @@ from ._capi import (LIB_PATH, PATH_AUTO, PATH_FMA, PATH_MMA, ERR_BLOCK_ID, ERR_S
 from .step import DecodeStep  # noqa: F401
 from .block_manager import BlockManager  # noqa: F401
 
-__all__ = ["BlockManager", "copy_blocks", "slot_mapping", "kv_store", "kv_store_paged", "sample_ex", "pack_mask", "paged_decode_attention", "decode_workspace_bytes",
+__all__ = ["BlockManager", "copy_blocks", "slot_mapping", "kv_store", "kv_store_paged", "kv_store_prefill",
+           "prefill_attention", "sample_ex", "pack_mask", "paged_decode_attention", "decode_workspace_bytes",
            "sample", "DecodeStep", "PkvdError", "lib"]
 
 
@@ -65,6 +66,38 @@ def kv_store_paged(k: torch.Tensor, v: torch.Tensor, block_tables: torch.Tensor,
     check(lib().pkvd_kv_store_paged(ptr(k), ptr(v), ptr(block_tables), block_tables.shape[1],
                                     ptr(context_lens), k.shape[0], ptr(slot_mapping), ctypes.byref(c),
                                     stream_handle(stream, k), _err_ptr(err)))
+
+
+def kv_store_prefill(k: torch.Tensor, v: torch.Tensor, block_tables: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                     cu_seqlens_k: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                     slot_mapping: torch.Tensor | None = None, err: torch.Tensor | None = None,
+                     stream=None) -> None:
+    """Varlen prefill store: new row t of sequence i (rows cu_seqlens_q[i] ..
+    cu_seqlens_q[i+1]-1) goes to the slot of position (k_len_i - q_len_i) +
+    (t - cu_seqlens_q[i]); the slots are also written to slot_mapping (int64
+    [total_q]) when it is given."""
+    c = cache_desc(k_cache, v_cache)
+    check(lib().pkvd_kv_store_prefill(ptr(k), ptr(v), ptr(block_tables), block_tables.shape[1],
+                                      ptr(cu_seqlens_q), ptr(cu_seqlens_k), cu_seqlens_q.shape[0] - 1,
+                                      k.shape[0], ptr(slot_mapping), ctypes.byref(c),
+                                      stream_handle(stream, k), _err_ptr(err)))
+
+
+def prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_tables: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
+                      max_seqlen_q: int, scale: float, window: int = 0, out: torch.Tensor | None = None,
+                      err: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Causal varlen attention of the new rows q ([total_q, Hq, D]) over their
+    sequences' cached prefix and new rows, read from the paged cache."""
+    T, Hq, _ = q.shape
+    c = cache_desc(k_cache, v_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    check(lib().pkvd_prefill_attention(ptr(out), ptr(q), ctypes.byref(c), ptr(block_tables),
+                                       block_tables.shape[1], ptr(cu_seqlens_q), ptr(cu_seqlens_k),
+                                       cu_seqlens_q.shape[0] - 1, T, max_seqlen_q, Hq,
+                                       ctypes.c_float(scale), window, stream_handle(stream, q), _err_ptr(err)))
+    return out
 
 
 def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src: torch.Tensor, dst: torch.Tensor,

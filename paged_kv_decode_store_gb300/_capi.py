@@ -40,6 +40,11 @@ SIGNATURES = {
                                 c_void_p, c_void_p]),
     "pkvd_kv_store_paged": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_int32, c_void_p,
                                       ctypes.POINTER(PkvdCache), c_void_p, c_void_p]),
+    "pkvd_kv_store_prefill": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_int32,
+                                        c_int32, c_void_p, ctypes.POINTER(PkvdCache), c_void_p, c_void_p]),
+    "pkvd_prefill_attention": (c_int32, [c_void_p, c_void_p, ctypes.POINTER(PkvdCache), c_void_p, c_int32,
+                                         c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_float,
+                                         c_int32, c_void_p, c_void_p]),
     "pkvd_bm_create": (c_int32, [c_int32, c_int32, ctypes.POINTER(c_void_p)]),
     "pkvd_bm_destroy": (None, [c_void_p]),
     "pkvd_bm_num_free": (c_int32, [c_void_p]),

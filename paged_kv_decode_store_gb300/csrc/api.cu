@@ -120,6 +120,62 @@ pkvd_status pkvd_copy_blocks(const pkvd_cache* cache, const int32_t* src, const 
                                       static_cast<cudaStream_t>(stream), err_flag));
 }
 
+pkvd_status pkvd_kv_store_prefill(const void* k, const void* v, const int32_t* block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t* cu_seqlens_q,
+                                  const int32_t* cu_seqlens_k, int32_t num_seqs, int32_t total_q,
+                                  int64_t* slot_mapping, const pkvd_cache* cache, void* stream,
+                                  int32_t* err_flag) {
+  if (num_seqs < 0 || total_q < 0) return PKVD_INVALID_ARG;
+  const pkvd_status cs = check_cache(cache, false);
+  if (cs != PKVD_OK) return cs;
+  if (total_q == 0) return PKVD_OK;
+  if (!k || !v || !cu_seqlens_q || !cu_seqlens_k) return PKVD_INVALID_ARG;
+  if (num_seqs > 0 && (!block_tables || max_blocks_per_seq <= 0)) return PKVD_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v)) return PKVD_UNSUPPORTED_SHAPE;
+  return from_cuda(launch_kv_store_prefill(k, v, block_tables, max_blocks_per_seq, cu_seqlens_q, cu_seqlens_k,
+                                           num_seqs, total_q, slot_mapping, *cache, esize(cache->dtype),
+                                           static_cast<cudaStream_t>(stream), err_flag));
+}
+
+pkvd_status pkvd_prefill_attention(void* out, const void* q, const pkvd_cache* cache, const int32_t* block_tables,
+                                   int32_t max_blocks_per_seq, const int32_t* cu_seqlens_q,
+                                   const int32_t* cu_seqlens_k, int32_t num_seqs, int32_t total_q,
+                                   int32_t max_seqlen_q, int32_t num_q_heads, float scale, int32_t window,
+                                   void* stream, int32_t* err_flag) {
+  if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || window < 0) return PKVD_INVALID_ARG;
+  if (!std::isfinite(scale)) return PKVD_INVALID_ARG;
+  const pkvd_status cs = check_cache(cache, false);
+  if (cs != PKVD_OK) return cs;
+  if (num_q_heads <= 0) return PKVD_INVALID_ARG;
+  if (num_q_heads % cache->num_kv_heads) return PKVD_UNSUPPORTED_SHAPE;
+  const int group = num_q_heads / cache->num_kv_heads;
+  if (!prefill_supported(cache->dtype, cache->head_dim, group)) {
+    return cache->dtype == PKVD_F32 ? PKVD_UNSUPPORTED_DTYPE : PKVD_UNSUPPORTED_SHAPE;
+  }
+  if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return PKVD_OK;
+  if (!out || !q || !block_tables || !cu_seqlens_q || !cu_seqlens_k || max_blocks_per_seq <= 0)
+    return PKVD_INVALID_ARG;
+  if (!aligned16(q) || (reinterpret_cast<uintptr_t>(out) & 3u)) return PKVD_UNSUPPORTED_SHAPE;
+  const int tiles = (max_seqlen_q + prefill_tile_tokens(group) - 1) / prefill_tile_tokens(group);
+  if (num_seqs > 65535 || tiles > 65535) return PKVD_UNSUPPORTED_SHAPE;
+  PrefillArgs a;
+  a.out = out;
+  a.q = q;
+  a.cache = *cache;
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.cu_seqlens_k = cu_seqlens_k;
+  a.num_seqs = num_seqs;
+  a.total_q = total_q;
+  a.max_seqlen_q = max_seqlen_q;
+  a.num_q_heads = num_q_heads;
+  a.scale = scale;
+  a.window = window;
+  a.err = err_flag;
+  return from_cuda(launch_prefill_attention(a, static_cast<cudaStream_t>(stream)));
+}
+
 pkvd_status pkvd_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                         int32_t max_context_len, int32_t sm_count, size_t* bytes) {
   if (!bytes || num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0) return PKVD_INVALID_ARG;

@@ -61,6 +61,31 @@ cudaError_t launch_kv_store_paged(const void* k, const void* v, const int32_t* t
 cudaError_t launch_copy_blocks(const pkvd_cache& c, int elem_bytes, const int32_t* src, const int32_t* dst,
                                const int32_t* rows, int count, cudaStream_t stream, int32_t* err);
 
+// Varlen paged prefill (prefill.cu, store.cu).
+struct PrefillArgs {
+  void* out;
+  const void* q;
+  pkvd_cache cache;
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_k;
+  int num_seqs;
+  int total_q;
+  int max_seqlen_q;
+  int num_q_heads;
+  float scale;
+  int window;
+  int32_t* err;
+};
+bool prefill_supported(int dtype, int head_dim, int group);
+int prefill_tile_tokens(int group);
+cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_kv_store_prefill(const void* k, const void* v, const int32_t* tables, int max_blocks,
+                                    const int32_t* cu_q, const int32_t* cu_k, int num_seqs, int total_q,
+                                    int64_t* slots_out, const pkvd_cache& c, int elem_bytes, cudaStream_t stream,
+                                    int32_t* err);
+
 // Per-row cut parameters the sampler leaves for the extras kernel:
 // [0] flags (kRowGreedy, kRowUniform, kRowTopK), [1] nucleus threshold key
 // (0 = off), [2] k-th key, [3] index of the last kept id at the k-th key

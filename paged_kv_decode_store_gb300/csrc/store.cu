@@ -116,6 +116,62 @@ __global__ void kv_store_paged_kernel(const uint8_t* __restrict__ k, const uint8
              elem_bytes);
 }
 
+// Slot of new token row t of a varlen prefill batch, or -1 (a row past
+// cu_seqlens_q[num_seqs], or a bad length / block id, which is flagged).
+// nano-vllm "Model Runner" notes, section "prefix cache": sequence i owns
+// rows [cu_q[i], cu_q[i+1]) and k_len = cu_k[i+1] - cu_k[i] tokens in all,
+// so row t sits at position (k_len - q_len) + (t - cu_q[i]).
+__device__ __forceinline__ int64_t prefill_slot(const int32_t* __restrict__ tables, int max_blocks,
+                                                const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k,
+                                                int num_seqs, int t, int block_size, int64_t num_blocks,
+                                                int32_t* err) {
+  if (t >= cu_q[num_seqs]) return -1;
+  int lo = 0, hi = num_seqs - 1;   // the last i with cu_q[i] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu_q[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  const int q0 = cu_q[lo], q1 = cu_q[lo + 1];
+  const int qlen = q1 - q0, klen = cu_k[lo + 1] - cu_k[lo];
+  if (t < q0 || t >= q1 || klen < qlen) {
+    flag_error(err, PKVD_ERR_CONTEXT);
+    return -1;
+  }
+  const int pos = klen - qlen + (t - q0);
+  const int logical = pos / block_size;
+  if (logical >= max_blocks) {
+    flag_error(err, PKVD_ERR_CONTEXT);
+    return -1;
+  }
+  const int phys = tables[(int64_t)lo * max_blocks + logical];
+  if (phys < 0 || phys >= num_blocks) {
+    flag_error(err, PKVD_ERR_BLOCK_ID);
+    return -1;
+  }
+  return (int64_t)phys * block_size + pos % block_size;
+}
+
+// Prefill store: one CTA per new token row finds its sequence and position,
+// optionally records the slot and copies the K and V rows there.
+__global__ void kv_store_prefill_kernel(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v,
+                                        const int32_t* __restrict__ tables, int max_blocks,
+                                        const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k,
+                                        int num_seqs, int64_t* __restrict__ slots_out, uint8_t* __restrict__ kc,
+                                        uint8_t* __restrict__ vc, int64_t num_blocks, int block_size,
+                                        int num_heads, int head_dim, int64_t block_stride, int64_t token_stride,
+                                        int64_t head_stride, int elem_bytes, int32_t* err) {
+  pdl_wait();
+  pdl_trigger();
+  const int tok = blockIdx.x;
+  const int64_t slot = prefill_slot(tables, max_blocks, cu_q, cu_k, num_seqs, tok, block_size, num_blocks,
+                                    threadIdx.x == 0 ? err : nullptr);
+  if (slots_out && threadIdx.x == 0) slots_out[tok] = slot;
+  if (slot < 0) return;
+  store_rows(k, v, tok, slot, kc, vc, block_size, num_heads, head_dim, block_stride, token_stride, head_stride,
+             elem_bytes);
+}
+
 cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* tables, int max_blocks,
                                 const int32_t* ctx, int num_seqs, int block_size,
                                 int64_t num_blocks, cudaStream_t stream, int32_t* err) {
@@ -184,6 +240,20 @@ cudaError_t launch_kv_store_paged(const void* k, const void* v, const int32_t* t
   threads = threads < 64 ? 64 : (threads > 256 ? 256 : threads);
   return launch_pdl(kv_store_paged_kernel, dim3(num_seqs), dim3(threads), 0, stream, static_cast<const uint8_t*>(k),
                     static_cast<const uint8_t*>(v), tables, max_blocks, ctx, slots_out,
+                    static_cast<uint8_t*>(c.k_base), static_cast<uint8_t*>(c.v_base), c.num_blocks, c.block_size,
+                    c.num_kv_heads, c.head_dim, c.block_stride, c.token_stride, c.head_stride, elem_bytes, err);
+}
+
+cudaError_t launch_kv_store_prefill(const void* k, const void* v, const int32_t* tables, int max_blocks,
+                                    const int32_t* cu_q, const int32_t* cu_k, int num_seqs, int total_q,
+                                    int64_t* slots_out, const pkvd_cache& c, int elem_bytes, cudaStream_t stream,
+                                    int32_t* err) {
+  if (total_q == 0) return cudaSuccess;
+  const int nvec = c.num_kv_heads * c.head_dim * elem_bytes / 16;
+  int threads = 2 * nvec;
+  threads = threads < 64 ? 64 : (threads > 256 ? 256 : threads);
+  return launch_pdl(kv_store_prefill_kernel, dim3(total_q), dim3(threads), 0, stream, static_cast<const uint8_t*>(k),
+                    static_cast<const uint8_t*>(v), tables, max_blocks, cu_q, cu_k, num_seqs, slots_out,
                     static_cast<uint8_t*>(c.k_base), static_cast<uint8_t*>(c.v_base), c.num_blocks, c.block_size,
                     c.num_kv_heads, c.head_dim, c.block_stride, c.token_stride, c.head_stride, elem_bytes, err);
 }

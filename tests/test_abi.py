@@ -109,3 +109,29 @@ def test_store_slot_and_sample_host_checks(L):
     assert L.pkvd_sample(*args, 2, 0, 100, 100, *tail) == 0
     n = ctypes.c_size_t(7)
     assert L.pkvd_sample_workspace_bytes(4, 100, ctypes.byref(n)) == 0 and n.value == 4 * 32     # extras' row cuts
+
+
+def test_prefill_host_checks(L):
+    def attn(cache, hq=48, q=1 << 22, out=1 << 21, seqs=4, total=100, maxq=64, scale=0.088, window=0):
+        return L.pkvd_prefill_attention(out, q, ctypes.byref(cache), 1 << 23, 8, 1 << 24, 1 << 25, seqs, total,
+                                        maxq, hq, ctypes.c_float(scale), window, None, None)
+    assert attn(_cache(dtype=0)) == 2                          # no fp32 prefill kernel
+    assert attn(_cache(), hq=44) == 3                          # 44 % 8 != 0
+    assert attn(_cache(num_kv_heads=1, block_stride=16 * 128, token_stride=128), hq=129) == 3   # group > 128
+    assert attn(_cache(head_dim=96)) == 3
+    assert attn(_cache(), window=-1) == 1
+    assert attn(_cache(), scale=float("inf")) == 1
+    assert attn(_cache(), q=(1 << 22) + 8) == 3                # q must be 16-byte aligned
+    assert attn(_cache(), out=(1 << 21) + 2) == 3              # out 4-byte aligned
+    assert attn(_cache(), seqs=70000) == 3                     # grid y limit
+    assert attn(_cache(), maxq=65536 * 21 + 1) == 3            # grid z limit (21 tokens per tile at group 6)
+    assert attn(_cache(), seqs=0) == 0
+    assert attn(_cache(), total=0) == 0
+    assert attn(_cache(), seqs=-1) == 1
+    store = lambda k, v, total, cc, tab=1 << 22: L.pkvd_kv_store_prefill(k, v, tab, 8, 1 << 23, 1 << 24, 4, total,
+                                                                         None, ctypes.byref(cc), None, None)
+    assert store(1 << 20, 1 << 21, -1, _cache()) == 1
+    assert store(1 << 20, 1 << 21, 0, _cache()) == 0
+    assert store(None, 1 << 21, 5, _cache()) == 1
+    assert store(1 << 20, 1 << 21, 5, _cache(), tab=None) == 1
+    assert store(1 << 20, (1 << 21) + 8, 5, _cache()) == 3

@@ -564,9 +564,11 @@ def run_prefill_bench(args):
     def store():
         pk.kv_store_prefill(d["k"], d["v"], d["tables"], d["cu_q"], d["cu_k"], kc, vc, err=err)
 
+    path = {"auto": pk.PATH_AUTO, "tc": pk.PATH_TC, "mma": pk.PATH_MMA}[args.prefill_path]
+
     def attend():
         pk.prefill_attention(d["q"], kc, vc, d["tables"], d["cu_q"], d["cu_k"], maxq, b.scale, window=window,
-                             out=out, err=err)
+                             out=out, err=err, path=path)
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -644,7 +646,10 @@ def run_prefill_bench(args):
                    "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MB write, then "
                          f"{FLUSH_BYTES >> 20} MB read)"},
         "tokens_per_s": b.total_q / (ms * 1e-3), "attention_flops": flops, "attention_ms": attn,
-        "roofline": {"kernel": "prefill_attention_kernel (mma.sync m16n8k16, fp32 accumulation)",
+        "attention_path": args.prefill_path,
+        "roofline": {"kernel": ("prefill_attention_kernel (mma.sync m16n8k16, fp32 accumulation)"
+                                if args.prefill_path == "mma" else
+                                "prefill_tc_kernel (tcgen05.mma kind::f16, TMA 128B-swizzled K/V, TMEM accumulators)"),
                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
                      "peak_source": "measured bf16 burst" if peaks.get("bf16_tflops") else "fallback",
@@ -680,6 +685,8 @@ def main():
     ap.add_argument("--prefill", default=None,
                     choices=["qwen3_prefill", "grok1_prefill", "chunked_prefill"],
                     help="time a varlen prefill step (store + causal attention) instead (one JSON line)")
+    ap.add_argument("--prefill-path", default="auto", choices=["auto", "tc", "mma"],
+                    help="prefill attention kernel: tcgen05 (auto picks it where it runs) or mma.sync")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     cfg = configs.get(args.config)

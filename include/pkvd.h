@@ -68,11 +68,14 @@ typedef enum { PKVD_F32 = 0, PKVD_F16 = 1, PKVD_BF16 = 2 } pkvd_dtype;
 #define PKVD_ERR_CONTEXT     4   /* context_len < 0 or > the stated bound     */
 #define PKVD_ERR_TIMEOUT     8   /* a pipeline wait gave up (never expected)  */
 
-/* Attention path selector for pkvd_paged_decode_attention_ex. */
+/* Attention path selector for pkvd_paged_decode_attention_ex and
+ * pkvd_prefill_attention_ex. */
 typedef enum {
   PKVD_PATH_AUTO = 0,   /* the library's choice for the shape              */
-  PKVD_PATH_FMA = 1,    /* fp32 CUDA-core dot products                     */
-  PKVD_PATH_MMA = 2     /* tensor-core m16n8k16 over the query group       */
+  PKVD_PATH_FMA = 1,    /* fp32 CUDA-core dot products (decode only)       */
+  PKVD_PATH_MMA = 2,    /* warp-level mma.sync m16n8k16 tensor-core path   */
+  PKVD_PATH_TC = 3      /* tcgen05: TMA-fed operands, TMEM accumulators
+                           (prefill only)                                  */
 } pkvd_attn_path;
 
 /*
@@ -309,6 +312,21 @@ pkvd_status pkvd_prefill_attention(void* out, const void* q, const pkvd_cache* c
                                    const int32_t* cu_seqlens_k, int32_t num_seqs, int32_t total_q,
                                    int32_t max_seqlen_q, int32_t num_q_heads, float scale, int32_t window,
                                    void* stream, int32_t* err_flag);
+
+/* Same as pkvd_prefill_attention with an explicit compute path:
+ * PKVD_PATH_TC (tcgen05 MMAs on TMA-loaded 128-byte-swizzled tiles with TMEM
+ * accumulators; needs block_size >= 8, 16-byte aligned q and out, and a cache
+ * whose strides nest head < token < block), PKVD_PATH_MMA (mma.sync), or
+ * PKVD_PATH_AUTO (TC when it can run the call, else MMA; what
+ * pkvd_prefill_attention does).  PKVD_UNSUPPORTED_SHAPE if the path cannot
+ * run the call.  Both paths compute the same function; on the TC path cache
+ * rows of a 16-row-aligned group that meets a sequence's range may be
+ * fetched, but rows outside [ws, p] never weigh in. */
+pkvd_status pkvd_prefill_attention_ex(void* out, const void* q, const pkvd_cache* cache, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* cu_seqlens_q,
+                                      const int32_t* cu_seqlens_k, int32_t num_seqs, int32_t total_q,
+                                      int32_t max_seqlen_q, int32_t num_q_heads, float scale, int32_t window,
+                                      void* stream, int32_t* err_flag, int32_t path);
 
 /* Workspace bytes of pkvd_sample_ex's optional outputs: 32 per row (host
  * only).  pkvd_sample itself needs none (it may get NULL, 0). */

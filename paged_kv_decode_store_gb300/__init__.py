@@ -18,7 +18,7 @@ import os
 
 import torch
 
-from ._capi import (LIB_PATH, PATH_AUTO, PATH_FMA, PATH_MMA, ERR_BLOCK_ID, ERR_SLOT,  # noqa: F401
+from ._capi import (LIB_PATH, PATH_AUTO, PATH_FMA, PATH_MMA, PATH_TC, ERR_BLOCK_ID, ERR_SLOT,  # noqa: F401
                     ERR_CONTEXT, ERR_TIMEOUT, PkvdCache, PkvdError, lib, check, dtype_code,
                     stream_handle, cache_desc, ptr)
 from .step import DecodeStep  # noqa: F401
@@ -86,17 +86,19 @@ def kv_store_prefill(k: torch.Tensor, v: torch.Tensor, block_tables: torch.Tenso
 def prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                       block_tables: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
                       max_seqlen_q: int, scale: float, window: int = 0, out: torch.Tensor | None = None,
-                      err: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                      err: torch.Tensor | None = None, stream=None, path: int = PATH_AUTO) -> torch.Tensor:
     """Causal varlen attention of the new rows q ([total_q, Hq, D]) over their
-    sequences' cached prefix and new rows, read from the paged cache."""
+    sequences' cached prefix and new rows, read from the paged cache
+    (path: PATH_AUTO, PATH_TC for tcgen05, PATH_MMA for mma.sync)."""
     T, Hq, _ = q.shape
     c = cache_desc(k_cache, v_cache)
     if out is None:
         out = torch.empty_like(q)
-    check(lib().pkvd_prefill_attention(ptr(out), ptr(q), ctypes.byref(c), ptr(block_tables),
-                                       block_tables.shape[1], ptr(cu_seqlens_q), ptr(cu_seqlens_k),
-                                       cu_seqlens_q.shape[0] - 1, T, max_seqlen_q, Hq,
-                                       ctypes.c_float(scale), window, stream_handle(stream, q), _err_ptr(err)))
+    check(lib().pkvd_prefill_attention_ex(ptr(out), ptr(q), ctypes.byref(c), ptr(block_tables),
+                                          block_tables.shape[1], ptr(cu_seqlens_q), ptr(cu_seqlens_k),
+                                          cu_seqlens_q.shape[0] - 1, T, max_seqlen_q, Hq,
+                                          ctypes.c_float(scale), window, stream_handle(stream, q), _err_ptr(err),
+                                          path))
     return out
 
 

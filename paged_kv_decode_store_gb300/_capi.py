@@ -8,7 +8,7 @@ import torch
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkvd.so")
 
-PATH_AUTO, PATH_FMA, PATH_MMA = 0, 1, 2
+PATH_AUTO, PATH_FMA, PATH_MMA, PATH_TC = 0, 1, 2, 3
 ERR_BLOCK_ID, ERR_SLOT, ERR_CONTEXT, ERR_TIMEOUT = 1, 2, 4, 8
 NO_SPACE = 6
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
@@ -45,6 +45,9 @@ SIGNATURES = {
     "pkvd_prefill_attention": (c_int32, [c_void_p, c_void_p, ctypes.POINTER(PkvdCache), c_void_p, c_int32,
                                          c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_float,
                                          c_int32, c_void_p, c_void_p]),
+    "pkvd_prefill_attention_ex": (c_int32, [c_void_p, c_void_p, ctypes.POINTER(PkvdCache), c_void_p, c_int32,
+                                            c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_float,
+                                            c_int32, c_void_p, c_void_p, c_int32]),
     "pkvd_bm_create": (c_int32, [c_int32, c_int32, ctypes.POINTER(c_void_p)]),
     "pkvd_bm_destroy": (None, [c_void_p]),
     "pkvd_bm_num_free": (c_int32, [c_void_p]),

@@ -137,11 +137,13 @@ pkvd_status pkvd_kv_store_prefill(const void* k, const void* v, const int32_t* b
                                            static_cast<cudaStream_t>(stream), err_flag));
 }
 
-pkvd_status pkvd_prefill_attention(void* out, const void* q, const pkvd_cache* cache, const int32_t* block_tables,
-                                   int32_t max_blocks_per_seq, const int32_t* cu_seqlens_q,
-                                   const int32_t* cu_seqlens_k, int32_t num_seqs, int32_t total_q,
-                                   int32_t max_seqlen_q, int32_t num_q_heads, float scale, int32_t window,
-                                   void* stream, int32_t* err_flag) {
+pkvd_status pkvd_prefill_attention_ex(void* out, const void* q, const pkvd_cache* cache, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* cu_seqlens_q,
+                                      const int32_t* cu_seqlens_k, int32_t num_seqs, int32_t total_q,
+                                      int32_t max_seqlen_q, int32_t num_q_heads, float scale, int32_t window,
+                                      void* stream, int32_t* err_flag, int32_t path) {
+  if (path != PKVD_PATH_AUTO && path != PKVD_PATH_MMA && path != PKVD_PATH_TC)
+    return path == PKVD_PATH_FMA ? PKVD_UNSUPPORTED_SHAPE : PKVD_INVALID_ARG;
   if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || window < 0) return PKVD_INVALID_ARG;
   if (!std::isfinite(scale)) return PKVD_INVALID_ARG;
   const pkvd_status cs = check_cache(cache, false);
@@ -173,7 +175,21 @@ pkvd_status pkvd_prefill_attention(void* out, const void* q, const pkvd_cache* c
   a.scale = scale;
   a.window = window;
   a.err = err_flag;
+  const bool tc = prefill_tc_supported(a);
+  if (path == PKVD_PATH_TC && !tc) return PKVD_UNSUPPORTED_SHAPE;
+  if (path == PKVD_PATH_TC || (path == PKVD_PATH_AUTO && tc))
+    return from_cuda(launch_prefill_tc(a, static_cast<cudaStream_t>(stream)));
   return from_cuda(launch_prefill_attention(a, static_cast<cudaStream_t>(stream)));
+}
+
+pkvd_status pkvd_prefill_attention(void* out, const void* q, const pkvd_cache* cache, const int32_t* block_tables,
+                                   int32_t max_blocks_per_seq, const int32_t* cu_seqlens_q,
+                                   const int32_t* cu_seqlens_k, int32_t num_seqs, int32_t total_q,
+                                   int32_t max_seqlen_q, int32_t num_q_heads, float scale, int32_t window,
+                                   void* stream, int32_t* err_flag) {
+  return pkvd_prefill_attention_ex(out, q, cache, block_tables, max_blocks_per_seq, cu_seqlens_q, cu_seqlens_k,
+                                   num_seqs, total_q, max_seqlen_q, num_q_heads, scale, window, stream, err_flag,
+                                   PKVD_PATH_AUTO);
 }
 
 pkvd_status pkvd_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
@@ -198,7 +214,7 @@ pkvd_status attention_call(void* out, const void* q, const pkvd_cache* cache, co
   const int G = num_q_heads / cache->num_kv_heads;
   if (path == PKVD_PATH_AUTO) path = attention_default_path(cache->dtype, cache->head_dim, cache->num_kv_heads, G);
   if (path != PKVD_PATH_FMA && path != PKVD_PATH_MMA) {
-    if (path == 0) return PKVD_UNSUPPORTED_SHAPE;
+    if (path == 0 || path == PKVD_PATH_TC) return PKVD_UNSUPPORTED_SHAPE;
     return PKVD_INVALID_ARG;
   }
   if (!attention_path_supported(path, cache->dtype, cache->head_dim, cache->num_kv_heads, G))

@@ -79,6 +79,8 @@ struct PrefillArgs {
   int32_t* err;
 };
 bool prefill_supported(int dtype, int head_dim, int group);
+bool prefill_tc_supported(const PrefillArgs& a);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
 int prefill_tile_tokens(int group);
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_kv_store_prefill(const void* k, const void* v, const int32_t* tables, int max_blocks,

@@ -1,0 +1,661 @@
+// Varlen paged prefill attention on the 5th-generation tensor cores
+// (tcgen05: operands in shared memory, accumulators in tensor memory).
+//
+// Same operation as prefill.cu (nano-vllm "Model Runner" notes, sections
+// "prefix cache" and "prefill and decode": cu_seqlens_q / cu_seqlens_k
+// describe the batch, new token j of sequence i sits at position
+// (k_len_i - q_len_i) + j and attends causally to positions 0..p of its
+// sequence through the block table).
+//
+// One CTA per (KV head, sequence, tile of 128 query rows); row = token * G +
+// query head of the group, so every K/V tile serves the whole GQA group.
+// Six warps with fixed roles:
+//   warps 0-3  softmax: thread t owns query row t = TMEM lane t.  Loads its Q
+//              row into shared memory, then per 128-key tile reads its row of
+//              S from TMEM, masks, keeps a running max (re-based only when it
+//              grows by more than 2^8, so O is rarely rescaled), writes
+//              P = 2^(S - max) as 16-bit values into shared memory, and at the
+//              end reads O from TMEM, divides by the row sum and stores it.
+//   warp 4     producer: TMA (cp.async.bulk.tensor, 128-byte swizzle) of the
+//              K and V rows of each tile, one box per (cache block segment,
+//              64-column half), into two stages each.
+//   warp 5     MMA: allocates 512 TMEM columns; one thread issues
+//              S = Q K^T (M 128, N 128 keys, K = head_dim) into one of two S
+//              buffers and O += P V (M 128, N = head_dim, K 128 keys) with
+//              tcgen05.mma kind::f16 (fp32 accumulate), and signals mbarriers
+//              with tcgen05.commit.
+// S(j+1) and PV(j-1) run on the tensor cores while the softmax of tile j
+// runs.  Keys outside [first window start, last position] of the tile, and
+// segments whose block id is bad, are masked in S; their V rows are zeroed
+// in shared memory before PV, so poisoned rows never weigh in.
+//
+// Shared-memory operand layout (K-major, 128-byte swizzle): a 128-row tile of
+// 64 16-bit columns is 128 rows of 128 bytes, 16-byte chunk c of row r at
+// r*128 + ((c ^ (r % 8)) * 16); head_dim 128 uses two such halves.  Q, K and
+// P are read K-major (stride between 8-row groups 1024 B); V is read
+// MN-major (head_dim contiguous: 1024 B between 8-key groups, one half-tile
+// between 64-column halves).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace pkvd {
+
+namespace {
+
+constexpr int kTcRows = 128;          // M: query rows per CTA
+constexpr int kTcKeys = 128;          // keys per tile
+constexpr int kTcThreads = 320;       // 8 softmax warps, producer, MMA
+constexpr int kSoftmax = 256;         // softmax threads: two per query row
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr uint32_t kHalf = 128u * 128u;   // one 128-row x 64-column 16-bit half tile
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;         // S buffers at columns [0,128) and [128,256)
+constexpr uint32_t kColO = 256;       // O at [256, 256 + head_dim)
+constexpr float kRebase = 8.f;        // re-base the running max when it grows by > 2^8
+
+template <int D>
+struct TcLayout {
+  static constexpr int kHalves = D / 64;
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kK = kQ + kHalves * kHalf;          // kKStages stages
+  static constexpr uint32_t kV = kK + 3 * kHalves * kHalf;      // kVStages stages
+  static constexpr uint32_t kP = kV + 2 * kHalves * kHalf;      // 2 halves (128 keys)
+  static constexpr uint32_t kBar = kP + 2 * kHalf;
+  static constexpr uint32_t kX = kBar + 256;                    // row-pair exchange: 2 x 128 floats
+  // + alignment slack; at least 120 KB so that one CTA (which holds all 512
+  // TMEM columns) is resident per SM
+  static constexpr uint32_t kBytes = kX + 1024 + 1024 > 122880u ? kX + 1024 + 1024 : 122880u;
+};
+
+// mbarrier slots (8 bytes each) after kBar
+// K runs three tiles ahead (S needs it first), V two (PV needs it after the softmax).
+constexpr int kKStages = 3, kVStages = 2;
+enum : int {
+  kKFull = 0, kKEmpty = 3, kVFull = 6, kVEmpty = 8, kSFull = 10, kPFull = 12, kPVDone = 13, kQFull = 14, kDrain = 15,
+  kNumBars = 16
+};
+constexpr uint32_t kTmemSlot = 8 * kNumBars;   // the allocated TMEM base address
+
+struct TcParams {
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
+  void* out;
+  const void* q;
+  const int32_t* tables;
+  int max_blocks;
+  int64_t num_blocks;
+  int block_size;
+  int seg_rows;          // rows per TMA box: min(block_size, 128)
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int total_q;
+  int hq;
+  int group;
+  int tile_tokens;
+  float scale_log2;
+  int window;
+  int32_t* err;
+};
+
+// Non-blocking: has the phase with this parity completed?
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ int tc_window_start(int c, int window) {
+  return (window > 0 && c > window) ? c - window : 0;
+}
+
+__device__ __forceinline__ float tc_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------------------ tcgen05 PTX
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16, one CTA.
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far completes.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  const uint32_t* r = reinterpret_cast<const uint32_t*>(v);
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+      "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+      "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: 128-byte swizzle, version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B of the same
+// 16-bit type (0 f16, 1 bf16), A K-major, B K-major (b_mn = 0) or MN-major.
+__host__ __device__ constexpr uint32_t tc_idesc(uint32_t fmt, uint32_t n, uint32_t b_mn) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | (b_mn << 16) | ((n >> 3) << 17) | ((uint32_t)(kTcRows >> 4) << 24);
+}
+
+// 4-D tiled TMA load: coordinates (column, kv head, row in block, block).
+__device__ __forceinline__ void tma_load4(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Byte offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled half tile.
+__device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
+  using L = TcLayout<D>;
+  constexpr int H = L::kHalves;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;          // 1024-byte aligned: whole swizzle atoms
+  uint8_t* gbase = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + L::kBar);
+  const int hk = blockIdx.x, seq = blockIdx.y, ztile = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  pdl_wait();      // the cache rows of this step come from the store kernel
+  pdl_trigger();
+
+  const int q0 = p.cu_q[seq], q1 = p.cu_q[seq + 1];
+  const int klen = p.cu_k[seq + 1] - p.cu_k[seq];
+  const int qlen = q1 - q0;
+  if (q0 < 0 || qlen < 0 || klen < qlen || q1 > p.total_q ||
+      (int64_t)klen > (int64_t)p.max_blocks * p.block_size) {
+    if (threadIdx.x == 0 && ztile == 0 && hk == 0) flag_error(p.err, PKVD_ERR_CONTEXT);
+    return;
+  }
+  if (ztile == 0 && hk == 0 && threadIdx.x == 0 && qlen > (int)gridDim.z * p.tile_tokens)
+    flag_error(p.err, PKVD_ERR_CONTEXT);
+  const int tok_end = qlen - ztile * p.tile_tokens;
+  if (tok_end <= 0) return;
+  const int tok_begin = max(0, tok_end - p.tile_tokens);
+  const int G = p.group;
+  const int qrows = (tok_end - tok_begin) * G;
+  const int cached = klen - qlen;
+  const int pos_first = cached + tok_begin, pos_last = cached + tok_end - 1;
+  const int lo = tc_window_start(pos_first + 1, p.window);
+  const int hi = pos_last;
+  const int kt_first = lo / kTcKeys, kt_last = hi / kTcKeys;
+  const int n = kt_last - kt_first + 1;
+  const int32_t* table = p.tables + (int64_t)seq * p.max_blocks;
+  const int nseg = kTcKeys / p.seg_rows;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], (i == kPFull || i == kQFull) ? (uint32_t)kSoftmax : 1u);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(base + L::kBar + kTmemSlot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + L::kBar + kTmemSlot);
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    // Lane 0 polls for free stages and picks the next copy: K runs up to
+    // kKStages tiles ahead but at most one tile ahead of V while V can go.
+    // Lane s looks up and copies segment s of the tile.
+    const uint32_t box = (uint32_t)p.seg_rows * 128u;
+    int kt = 0, vt = 0;
+    bool ok = true;
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_k)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_v)) : "memory");
+    }
+    uint64_t t_start = globaltimer_ns();       // the last progress
+    // Block-table entries are fetched one tile ahead (lane s: segment s);
+    // kNone marks a segment that misses [lo, hi] (nothing to load).
+    constexpr int kNone = INT_MIN;
+    auto fetch = [&](int t) -> int {
+      if (t >= n || lane >= nseg) return kNone;
+      const int ks = (kt_first + t) * kTcKeys + lane * p.seg_rows;
+      if (ks > hi || ks + p.seg_rows - 1 < lo) return kNone;
+      return __ldg(table + ks / p.block_size);
+    };
+    int k_cur = fetch(0), k_next = fetch(1), v_cur = k_cur, v_next = k_next;
+    while (kt < n || vt < n) {
+      int what = 0;   // 1: issue K(kt), 2: issue V(vt), -1: gave up
+      if (lane == 0) {
+        const bool can_k =
+            kt < n && (kt < kKStages || mbar_test(&bars[kKEmpty + kt % kKStages], ((kt / kKStages) - 1) & 1));
+        const bool can_v =
+            vt < kt && (vt < kVStages || mbar_test(&bars[kVEmpty + vt % kVStages], ((vt / kVStages) - 1) & 1));
+        // K leads V by at most one tile unless V cannot go
+        if (can_v && (vt + 1 < kt || !can_k)) what = 2;
+        else if (can_k) what = 1;
+        else if (globaltimer_ns() - t_start > 2000000000ull) what = -1;
+      }
+      what = __shfl_sync(FULL_MASK, what, 0);
+      if (what < 0) {
+        ok = false;
+        break;
+      }
+      if (what == 0) continue;
+      const int raw = what == 1 ? k_cur : v_cur;
+      const bool good = raw != kNone && raw >= 0 && raw < p.num_blocks;
+      const uint32_t loaded = __ballot_sync(FULL_MASK, good);
+      if (what == 1 && __ballot_sync(FULL_MASK, raw != kNone && !good) && lane == 0)
+        flag_error(p.err, PKVD_ERR_BLOCK_ID);
+      const int phys = raw;
+      const int j = what == 1 ? kt : vt;
+      const int stg = what == 1 ? kt % kKStages : vt % kVStages;
+      uint64_t* bar = &bars[(what == 1 ? kKFull : kVFull) + stg];
+      const uint32_t dst0 = base + (what == 1 ? L::kK : L::kV) + stg * H * kHalf;
+      const CUtensorMap* map = what == 1 ? &p.tmap_k : &p.tmap_v;
+      const int kbase = (kt_first + j) * kTcKeys;
+      // a segment with a bad block id reads as zeros (like the mma.sync path)
+      if (raw != kNone && !good) {
+        for (int h = 0; h < H; ++h)
+          for (uint32_t o = 0; o < box; o += 16) st_shared_v4(dst0 + h * kHalf + lane * box + o, make_uint4(0u, 0u, 0u, 0u));
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      // lane 0 announces the bytes, then lane s copies segment s (in parallel)
+      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(loaded) * box * H);
+      __syncwarp();
+      if ((loaded >> lane) & 1u) {
+        const int ks = kbase + lane * p.seg_rows;
+#pragma unroll
+        for (int h = 0; h < H; ++h) tma_load4(dst0 + h * kHalf + lane * box, map, h * 64, hk, ks % p.block_size, phys, bar);
+      }
+      if (what == 1) {
+        ++kt;
+        k_cur = k_next;
+        k_next = fetch(kt + 1);
+      } else {
+        ++vt;
+        v_cur = v_next;
+        v_next = fetch(vt + 1);
+      }
+      if (lane == 0) t_start = globaltimer_ns();
+    }
+    if (!ok && lane == 0) {
+      // gave up: let the copies still in flight land before the CTA leaves
+      flag_error(p.err, PKVD_ERR_TIMEOUT);
+      for (int t = max(0, kt - kKStages); t < kt; ++t) mbar_wait_bounded(&bars[kKFull + t % kKStages], (t / kKStages) & 1);
+      for (int t = max(0, vt - kVStages); t < vt; ++t) mbar_wait_bounded(&bars[kVFull + t % kVStages], (t / kVStages) & 1);
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA
+    // One thread issues whichever product is ready first: S(js) once K(js)
+    // has landed and the S buffer is free (PV(js - 2) issued), or PV(jp) once
+    // P(jp) and V(jp) are ready.
+    if (lane == 0) {
+      constexpr uint32_t fmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+      constexpr uint32_t id_s = tc_idesc(fmt, kTcKeys, 0), id_pv = tc_idesc(fmt, D, 1);
+      bool ok = mbar_wait_bounded(&bars[kQFull], 0);
+      tc_fence_after();
+      int js = 0, jp = 0;
+      uint64_t t_start = globaltimer_ns();        // the last progress
+      while (ok && jp < n) {
+        if (js < n && js <= jp + 1 && mbar_test(&bars[kKFull + js % kKStages], (js / kKStages) & 1)) {
+          tc_fence_after();
+          const int sb = js & 1;
+          const uint32_t kb = base + L::kK + (js % kKStages) * H * kHalf;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
+            tc_mma(tmem + kColS + sb * kTcKeys, smem_desc(base + L::kQ + off, 16, 1024),
+                   smem_desc(kb + off, 16, 1024), id_s, k > 0);
+          }
+          tc_commit(&bars[kSFull + sb]);
+          tc_commit(&bars[kKEmpty + js % kKStages]);
+          ++js;
+          t_start = globaltimer_ns();
+        } else if (jp < js && mbar_test(&bars[kPFull], jp & 1) &&
+                   mbar_test(&bars[kVFull + jp % kVStages], (jp / kVStages) & 1)) {
+          tc_fence_after();
+          const uint32_t vb = base + L::kV + (jp % kVStages) * H * kHalf;
+#pragma unroll
+          for (int k = 0; k < kTcKeys / 16; ++k) {
+            const uint32_t poff = (k >> 2) * kHalf + (k & 3) * 32;
+            tc_mma(tmem + kColO, smem_desc(base + L::kP + poff, 16, 1024), smem_desc(vb + k * 2048, kHalf, 1024),
+                   id_pv, (jp > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(&bars[kVEmpty + jp % kVStages]);
+          tc_commit(&bars[kPVDone]);
+          ++jp;
+          t_start = globaltimer_ns();
+        } else if (globaltimer_ns() - t_start > 2000000000ull) {
+          ok = false;
+        }
+      }
+      if (!ok) {
+        flag_error(p.err, PKVD_ERR_TIMEOUT);
+        tc_commit(&bars[kDrain]);          // wait for the tensor-core work already issued
+        mbar_wait_bounded(&bars[kDrain], 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    // Two threads per query row: thread (r, half) owns TMEM lane r, key
+    // columns [64 half, 64 half + 64) of S and P, and output columns
+    // [half D/2, half D/2 + D/2) of O.  The pair (warps w and w + 4) trades
+    // row maxima and sums through shared memory behind a 64-thread barrier.
+    const int r = threadIdx.x & 127, half = threadIdx.x >> 7;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int pair_bar = 1 + (warp & 3);
+    float* xch = reinterpret_cast<float*>(gbase + L::kX);   // [2][128]
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
+    const bool live = r < qrows;
+    const int tt = live ? r / G : 0, g = live ? r - (r / G) * G : 0;
+    const int pr = pos_first + tt;                 // padding rows mirror row 0
+    const int wr = tc_window_start(pr + 1, p.window);
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
+                                                        ((int64_t)(q0 + tok_begin + tt) * p.hq + (int64_t)hk * G + g) * D);
+#pragma unroll
+      for (int c = half * (D / 16); c < (half + 1) * (D / 16); ++c) {
+        const uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        st_shared_v4(base + L::kQ + (c >> 3) * kHalf + swz(r, c & 7), v);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars[kQFull]);
+    }
+
+    constexpr int kCols = kTcKeys / 2;            // key columns per thread
+    constexpr int kOCols = D / 2;                 // output columns per thread
+    const int c_base = half * kCols;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const int st = j & 1;
+      const int kbase = (kt_first + j) * kTcKeys;
+      // this row's usable columns of the tile, as bits of this thread's 64
+      const int c_lo = max(wr - kbase - c_base, 0), c_hi = min(pr - kbase - c_base, kCols - 1);
+      const bool row_full = c_lo == 0 && c_hi == kCols - 1;
+      uint32_t mw[2];
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        const int a = min(max(c_lo - 32 * w, 0), 32), z = min(max(c_hi + 1 - 32 * w, 0), 32);
+        mw[w] = (z == 32 ? 0xffffffffu : ((1u << z) - 1u)) & ~(a == 32 ? 0xffffffffu : ((1u << a) - 1u));
+      }
+
+      // After a timeout (ok false) the loop still runs to the end without
+      // waiting, so the two warps of a pair always meet at the same barriers.
+      if (ok) ok = __all_sync(FULL_MASK, mbar_wait_bounded(&bars[kSFull + st], (j >> 1) & 1));
+      tc_fence_after();
+      const uint32_t s_addr = tmem + lane_base + kColS + st * kTcKeys + c_base;
+      float v[kCols];
+      tmem_ld32(s_addr, v);
+      tmem_ld32(s_addr + 32, v + 32);
+      tmem_ld_wait();
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < kCols; ++c) {
+        const float x = v[c] * p.scale_log2;
+        v[c] = (row_full || ((mw[c >> 5] >> (c & 31)) & 1u)) ? x : -INFINITY;
+        mx[c & 3] = fmaxf(mx[c & 3], v[c]);
+      }
+      const float m_own = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      xch[half * 128 + r] = m_own;
+      pair_sync();
+      const float mt = fmaxf(m_own, xch[(half ^ 1) * 128 + r]);
+      pair_sync();                                 // both read before the next tile writes
+      // Re-base the running max only when it grows by more than 2^kRebase:
+      // exponents stay <= 2^8 and O is rescaled rarely (exact either way).
+      // Both threads of a row take the same decisions from the same values.
+      const bool rebase = mt > m_ref + kRebase;
+      const bool scale_o = rebase && m_ref != -INFINITY;
+      const float alpha = scale_o ? tc_ex2(m_ref - mt) : 1.f;
+      if (rebase) m_ref = mt;
+      const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+      // P = 2^(score - mu), packed to 16-bit pairs in registers
+      uint32_t pk[kCols / 2];
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < kCols; c += 2) {
+        const float e0 = tc_ex2(v[c] - mu), e1 = tc_ex2(v[c + 1] - mu);
+        rs += e0 + e1;
+        pk[c / 2] = Mma<T>::pack(e0, e1);
+      }
+      l = l * alpha + rs;                          // this thread's share of the row sum
+      if (j > 0) {
+        // PV(j-1) has finished: O may be rescaled and the P tile rewritten
+        if (ok) ok = __all_sync(FULL_MASK, mbar_wait_bounded(&bars[kPVDone], (j - 1) & 1));
+        tc_fence_after();
+        if (ok && __any_sync(FULL_MASK, scale_o)) {
+#pragma unroll 1
+          for (int c4 = 0; c4 < kOCols / 32; ++c4) {
+            float o[32];
+            const uint32_t oa = tmem + lane_base + kColO + half * kOCols + c4 * 32;
+            tmem_ld32(oa, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tmem_st32(oa, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      // this thread's 64 keys are P half `half`: 8 chunks of 16 bytes per row
+#pragma unroll
+      for (int chunk = 0; chunk < 8; ++chunk)
+        st_shared_v4(base + L::kP + half * kHalf + swz(r, chunk),
+                     make_uint4(pk[chunk * 4], pk[chunk * 4 + 1], pk[chunk * 4 + 2], pk[chunk * 4 + 3]));
+      // V rows outside [lo, hi] of an edge tile become zeros (thread (r, h)
+      // clears the h-th 64-column half of V row r)
+      if (kbase < lo || kbase + kTcKeys - 1 > hi) {
+        if (ok) ok = __all_sync(FULL_MASK, mbar_wait_bounded(&bars[kVFull + j % kVStages], (j / kVStages) & 1));
+        const int kp = kbase + r;
+        if ((kp < lo || kp > hi) && half < H) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(base + L::kV + ((j % kVStages) * H + half) * kHalf + r * 128 + c * 16,
+                         make_uint4(0u, 0u, 0u, 0u));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars[kPFull]);
+    }
+    if (ok) ok = __all_sync(FULL_MASK, mbar_wait_bounded(&bars[kPVDone], (n - 1) & 1));
+    // the row sum: this thread's share plus its partner's
+    xch[half * 128 + r] = l;
+    pair_sync();
+    const float l_row = l + xch[(half ^ 1) * 128 + r];
+    if (ok) {
+      tc_fence_after();
+      const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+      T* dst = static_cast<T*>(p.out) + ((int64_t)(q0 + tok_begin + tt) * p.hq + (int64_t)hk * G + g) * D +
+               half * kOCols;
+#pragma unroll
+      for (int c4 = 0; c4 < kOCols / 32; ++c4) {
+        float o[32];
+        tmem_ld32(tmem + lane_base + kColO + half * kOCols + c4 * 32, o);
+        tmem_ld_wait();
+        if (live) {
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            uint4 w;
+            w.x = Mma<T>::pack(o[c8 * 8 + 0] * inv, o[c8 * 8 + 1] * inv);
+            w.y = Mma<T>::pack(o[c8 * 8 + 2] * inv, o[c8 * 8 + 3] * inv);
+            w.z = Mma<T>::pack(o[c8 * 8 + 4] * inv, o[c8 * 8 + 5] * inv);
+            w.w = Mma<T>::pack(o[c8 * 8 + 6] * inv, o[c8 * 8 + 7] * inv);
+            *reinterpret_cast<uint4*>(dst + c4 * 32 + c8 * 8) = w;
+          }
+        }
+      }
+    } else if (lane == 0) {
+      flag_error(p.err, PKVD_ERR_TIMEOUT);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(f);
+    tried = true;
+  }
+  return fn;
+}
+
+// Tensor map over one cache ([num_blocks, block_size, Hkv, D] with element
+// strides), box = 64 columns x 1 head x seg_rows rows x 1 block, 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* map, const void* base, const pkvd_cache& c, int seg_rows) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)c.head_dim, (cuuint64_t)c.num_kv_heads, (cuuint64_t)c.block_size,
+                              (cuuint64_t)c.num_blocks};
+  const cuuint64_t strides[3] = {(cuuint64_t)c.head_stride * 2, (cuuint64_t)c.token_stride * 2,
+                                 (cuuint64_t)c.block_stride * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)seg_rows, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType dt = c.dtype == PKVD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return fn(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+template <typename T, int D>
+cudaError_t launch_tc_typed(const TcParams& prm, dim3 grid, cudaStream_t stream) {
+  constexpr int smem = TcLayout<D>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(prefill_tc_kernel<T, D>, grid, dim3(kTcThreads), smem, stream, prm);
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const PrefillArgs& a) {
+  const pkvd_cache& c = a.cache;
+  if (c.dtype != PKVD_F16 && c.dtype != PKVD_BF16) return false;
+  if (c.head_dim != 64 && c.head_dim != 128) return false;
+  if (c.block_size < 8) return false;                       // a TMA box must fill whole 8-row swizzle atoms
+  const int G = a.num_q_heads / c.num_kv_heads;
+  if (G < 1 || G > kTcRows) return false;
+  if ((reinterpret_cast<uintptr_t>(a.out) & 15u) || (reinterpret_cast<uintptr_t>(a.q) & 15u)) return false;
+  // the box walks the cache as nested dimensions: head inside token inside block
+  if (c.head_stride < c.head_dim || c.token_stride < c.head_stride * c.num_kv_heads ||
+      c.block_stride < c.token_stride * c.block_size)
+    return false;
+  CUtensorMap m;
+  return encode_cache_map(&m, c.k_base, c, c.block_size < kTcKeys ? c.block_size : kTcKeys);
+}
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
+  const pkvd_cache& c = a.cache;
+  const int G = a.num_q_heads / c.num_kv_heads;
+  TcParams prm;
+  const int seg_rows = c.block_size < kTcKeys ? c.block_size : kTcKeys;
+  if (!encode_cache_map(&prm.tmap_k, c.k_base, c, seg_rows) || !encode_cache_map(&prm.tmap_v, c.v_base, c, seg_rows))
+    return cudaErrorInvalidValue;
+  prm.out = a.out;
+  prm.q = a.q;
+  prm.tables = a.block_tables;
+  prm.max_blocks = a.max_blocks_per_seq;
+  prm.num_blocks = c.num_blocks;
+  prm.block_size = c.block_size;
+  prm.seg_rows = seg_rows;
+  prm.cu_q = a.cu_seqlens_q;
+  prm.cu_k = a.cu_seqlens_k;
+  prm.total_q = a.total_q;
+  prm.hq = a.num_q_heads;
+  prm.group = G;
+  prm.tile_tokens = kTcRows / G;
+  prm.scale_log2 = a.scale * 1.4426950408889634f;
+  prm.window = a.window;
+  prm.err = a.err;
+  const int tiles = (a.max_seqlen_q + prm.tile_tokens - 1) / prm.tile_tokens;
+  const dim3 grid(c.num_kv_heads, a.num_seqs, tiles);
+  if (c.dtype == PKVD_BF16)
+    return c.head_dim == 64 ? launch_tc_typed<__nv_bfloat16, 64>(prm, grid, stream)
+                            : launch_tc_typed<__nv_bfloat16, 128>(prm, grid, stream);
+  return c.head_dim == 64 ? launch_tc_typed<__half, 64>(prm, grid, stream)
+                          : launch_tc_typed<__half, 128>(prm, grid, stream);
+}
+
+}  // namespace pkvd

@@ -52,7 +52,7 @@ def to_f64(raw, dtype):
     return from_raw(raw, dtype).double().numpy()
 
 
-def run_prefill(pk, b, window=0, max_seqlen_q=None, total_rows=None):
+def run_prefill(pk, b, window=0, max_seqlen_q=None, total_rows=None, path=None):
     cache = b.cache.to(DEV)
     kc, vc = cache[0], cache[1]
     tables = torch.from_numpy(b.block_tables).to(DEV)
@@ -70,7 +70,7 @@ def run_prefill(pk, b, window=0, max_seqlen_q=None, total_rows=None):
     out = torch.full_like(q, 1024.0)
     pk.prefill_attention(q, kc, vc, tables, cu_q, cu_k,
                          b.max_seqlen_q if max_seqlen_q is None else max_seqlen_q,
-                         b.scale, window=window, out=out, err=err)
+                         b.scale, window=window, out=out, err=err, path=pk.PATH_AUTO if path is None else path)
     torch.cuda.synchronize()
     return cache.cpu(), slots.cpu().numpy(), out.cpu(), int(err.item())
 
@@ -98,9 +98,10 @@ def test_prefill_store_bit_exact(name):
     np.testing.assert_array_equal(raw_numpy(cache[1]), v_ref)
 
 
+@pytest.mark.parametrize("path", ["tc", "mma"])
 @pytest.mark.parametrize("window", [0, 1, 50, 200])
 @pytest.mark.parametrize("name", list(small_batches()))
-def test_prefill_attention_matches_oracle(name, window):
+def test_prefill_attention_matches_oracle(name, window, path):
     pk = require_gpu()
     b = wp.make_prefill_batch(small_batches()[name])
     k_ref, v_ref, _ = oracle_cache(b)
@@ -108,7 +109,7 @@ def test_prefill_attention_matches_oracle(name, window):
     ref = oracle.prefill.prefill_attention(b.q.double().numpy(), to_f64(k_ref, dt), to_f64(v_ref, dt),
                                            b.block_tables, b.cu_seqlens_q, b.cu_seqlens_k, b.scale,
                                            window=window)
-    _, _, out, err = run_prefill(pk, b, window=window)
+    _, _, out, err = run_prefill(pk, b, window=window, path={"tc": pk.PATH_TC, "mma": pk.PATH_MMA}[path])
     assert err == 0
     T, Hq, _ = ref.shape
     check_rows(out.double().numpy(), ref, [(t, h) for t in range(T) for h in range(Hq)])

@@ -666,6 +666,146 @@ def run_prefill_bench(args):
     print(json.dumps(line))
 
 
+# ----------------------------------------------------------------- serving timeline
+SERVE_DECODE_CONFIG = {"qwen3_prefill": "qwen3", "grok1_prefill": "grok1", "chunked_prefill": "longctx"}
+
+
+def run_serve_bench(args):
+    """One layer's hot path over a request's life: the prefill step of a batch
+    (store + causal attention over the cached prefixes + first-token sample),
+    then `steps` decode steps on the same paged cache (store + decode
+    attention + sample, one CUDA graph each).  Reports TTFT, TPOT and tok/s
+    (nanochat "04 · Engine", section "推理基准 infer_bench.py": TTFT / TPOT /
+    tok/s, with MFU for the compute-bound prefill and MBU for the
+    bandwidth-bound decode, and decode tok/s bounded by peak bandwidth over
+    the bytes read per step)."""
+    import paged_kv_decode_store_gb300 as pk
+    from workloads import prefill as wp
+    pcfg = wp.PREFILL_CONFIGS[args.serve]
+    dcfg = configs.get(SERVE_DECODE_CONFIG[args.serve])
+    b = wp.make_prefill_batch(pcfg)
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    B, bs, gen = pcfg.num_seqs, pcfg.block_size, max(args.steps, 4)
+    Hq, Hkv, D = pcfg.num_q_heads, pcfg.num_kv_heads, pcfg.head_dim
+    k_lens = b.k_lens.astype(np.int64)
+    # tables with room for `gen` more tokens: new blocks appended after the pool
+    need = [-(-int(k + gen) // bs) for k in k_lens]
+    width = max(need)
+    tables = np.full((B, width), -1, dtype=np.int32)
+    nb = b.num_blocks
+    for i in range(B):
+        have = -(-int(k_lens[i]) // bs)
+        tables[i, :have] = b.block_tables[i, :have]
+        tables[i, have:need[i]] = np.arange(nb, nb + need[i] - have)
+        nb += need[i] - have
+    cache = torch.empty((2, nb) + tuple(b.cache.shape[2:]), dtype=b.cache.dtype, device=dev)
+    cache[:, :b.num_blocks].copy_(b.cache.to(dev))
+    cache[:, b.num_blocks:].normal_()
+    kc, vc = cache[0], cache[1]
+    d = {"q": b.q.to(dev), "k": b.k_new.to(dev), "v": b.v_new.to(dev),
+         "tables": torch.from_numpy(tables).to(dev), "cu_q": torch.from_numpy(b.cu_seqlens_q).to(dev),
+         "cu_k": torch.from_numpy(b.cu_seqlens_k).to(dev)}
+    out = torch.empty_like(d["q"])
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    g = torch.Generator(device=dev).manual_seed(77)
+    ldt = workloads.synth.TORCH_DTYPES[dcfg.logits_dtype]
+    logits = torch.randn((B, dcfg.vocab), generator=g, device=dev).mul_(dcfg.logits_std).to(ldt)
+    temp = torch.full((B,), 0.8, device=dev)
+    top_k = torch.zeros(B, dtype=torch.int32, device=dev)
+    top_p = torch.full((B,), 0.95, device=dev)
+    seeds = torch.arange(B, dtype=torch.int64, device=dev) * 7919 + 1
+    offs = torch.zeros(B, dtype=torch.int64, device=dev)
+    first = torch.empty(B, dtype=torch.int32, device=dev)
+
+    def prefill():
+        pk.kv_store_prefill(d["k"], d["v"], d["tables"], d["cu_q"], d["cu_k"], kc, vc, err=err)
+        pk.prefill_attention(d["q"], kc, vc, d["tables"], d["cu_q"], d["cu_k"], b.max_seqlen_q, b.scale, out=out,
+                             err=err)
+        pk.sample(logits, temp, top_k, top_p, seeds, offs, out=first)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        prefill()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g_pre = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_pre):
+        prefill()
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+    ttft = []
+    for j in range(args.warmup + args.steps):
+        flush.add_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g_pre.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if j >= args.warmup:
+            ttft.append(e0.elapsed_time(e1))
+
+    # decode: the token at position k_len (then k_len + 1, ...) of every sequence
+    step = pk.DecodeStep(kc, vc, B, Hq, width, int(k_lens.max()) + gen, dcfg.vocab, ldt, b.scale)
+    step.q.normal_(generator=g)
+    step.k_new.normal_(generator=g)
+    step.v_new.normal_(generator=g)
+    step.block_tables.copy_(d["tables"])
+    ctx0 = torch.from_numpy((k_lens + 1).astype(np.int32)).to(dev)
+    step.context_lens.copy_(ctx0)
+    step.logits.copy_(logits)
+    step.temperature.copy_(temp)
+    step.top_p.copy_(top_p)
+    step.seeds.copy_(seeds)
+    step.capture()
+    tpot = []
+    for rnd in range(2):                    # a warm-up pass over the timeline, then the timed one
+        step.context_lens.copy_(ctx0)
+        for t in range(gen):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step.replay()
+            e1.record(stream)
+            step.context_lens.add_(1)       # the scheduler's bookkeeping between steps
+            step.offsets.add_(1)
+            if rnd:
+                tpot.append((e0, e1))
+    torch.cuda.synchronize()
+    tpot = [x.elapsed_time(y) for x, y in tpot]
+    if int(err.item()) or int(step.err.item()):
+        raise RuntimeError(f"device error flags {int(err.item())} / {int(step.err.item())}")
+
+    keys = prefill_keys(b.cu_seqlens_q, b.cu_seqlens_k)
+    flops = 4.0 * Hq * D * float(keys.sum())
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak_t = peaks.get("bf16_tflops") or 1900.0
+    peak_b, _ = peak_hbm()
+    dec_cfg = dcfg.scaled(num_seqs=B, table_kind="perm")
+    mid_ctx = (k_lens + 1 + gen // 2).astype(np.int32)
+    lay = workloads.Layout(mid_ctx, tables, nb, 0, int(mid_ctx.max()))
+    step_bytes = algorithmic_bytes(dec_cfg, lay)["step"]
+    ttft_ms, tpot_ms = statistics.mean(ttft), statistics.mean(tpot)
+    line = {
+        "metric": "serving timeline of one layer's hot path: TTFT, TPOT, tok/s; MFU (prefill), MBU (decode)",
+        "value": B / (tpot_ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": gen, "warmup": args.warmup,
+        "higher_is_better": True, "dtype": pcfg.dtype, "data": "synthetic",
+        "config": {"workload": pcfg.description + f"; then {gen} decode steps on the same cache",
+                   "prefill": pcfg.name, "decode_shapes": dcfg.name, "batch": B, "prompt_tokens": int(b.total_q),
+                   "cached_tokens": int((k_lens - b.q_lens).sum()), "vocab": dcfg.vocab,
+                   "l2": "flushed before each prefill; decode steps back to back (steady state)"},
+        "ttft_ms": ttft_ms, "tpot_ms": tpot_ms, "tokens_per_s": B / (tpot_ms * 1e-3),
+        "mfu_prefill": flops / (ttft_ms * 1e-3) / 1e12 / peak_t,
+        "mbu_decode": step_bytes / (tpot_ms * 1e-3) / 1e9 / peak_b,
+        "decode_step_bytes": step_bytes,
+        "decode_tokens_per_s_bound": B * peak_b * 1e9 / step_bytes,
+        "peaks": {"tflops": peak_t, "hbm_gbs": peak_b},
+        "gpu_launches": 3 * len(ttft) + step.kernels_per_step * gen,
+    }
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -687,6 +827,8 @@ def main():
                     help="time a varlen prefill step (store + causal attention) instead (one JSON line)")
     ap.add_argument("--prefill-path", default="auto", choices=["auto", "tc", "mma"],
                     help="prefill attention kernel: tcgen05 (auto picks it where it runs) or mma.sync")
+    ap.add_argument("--serve", default=None, choices=["qwen3_prefill", "grok1_prefill", "chunked_prefill"],
+                    help="serving timeline: the batch's prefill, then --steps decode steps (TTFT / TPOT, one line)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     cfg = configs.get(args.config)
@@ -702,6 +844,10 @@ def main():
     if args.prefill:
         if rank == 0:
             run_prefill_bench(args)
+        return
+    if args.serve:
+        if rank == 0:
+            run_serve_bench(args)
         return
 
     import paged_kv_decode_store_gb300 as pk

@@ -57,16 +57,19 @@ constexpr uint32_t kHalf = 128u * 128u;   // one 128-row x 64-column 16-bit half
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;         // S buffers at columns [0,128) and [128,256)
 constexpr uint32_t kColO = 256;       // O at [256, 256 + head_dim)
+constexpr uint32_t kColP = 384;       // P buffers (16-bit pairs) at [384, 448) and [448, 512)
 constexpr float kRebase = 8.f;        // re-base the running max when it grows by > 2^8
+
+// K and V each run up to three tiles ahead of the tensor cores.
+constexpr int kKStages = 3, kVStages = 3;
 
 template <int D>
 struct TcLayout {
   static constexpr int kHalves = D / 64;
   static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + kHalves * kHalf;          // kKStages stages
-  static constexpr uint32_t kV = kK + 3 * kHalves * kHalf;      // kVStages stages
-  static constexpr uint32_t kP = kV + 2 * kHalves * kHalf;      // 2 halves (128 keys)
-  static constexpr uint32_t kBar = kP + 2 * kHalf;
+  static constexpr uint32_t kK = kQ + kHalves * kHalf;                 // kKStages stages
+  static constexpr uint32_t kV = kK + kKStages * kHalves * kHalf;      // kVStages stages
+  static constexpr uint32_t kBar = kV + kVStages * kHalves * kHalf;
   static constexpr uint32_t kX = kBar + 256;                    // row-pair exchange: 2 x 128 floats
   // + alignment slack; at least 120 KB so that one CTA (which holds all 512
   // TMEM columns) is resident per SM
@@ -74,11 +77,12 @@ struct TcLayout {
 };
 
 // mbarrier slots (8 bytes each) after kBar
-// K runs three tiles ahead (S needs it first), V two (PV needs it after the softmax).
-constexpr int kKStages = 3, kVStages = 2;
+// P-full and PV-done have one barrier per P buffer (index j & 1): with P
+// double-buffered the softmax may finish tile j + 1 before PV(j) is issued,
+// and a single barrier would then run two phases ahead of its waiter.
 enum : int {
-  kKFull = 0, kKEmpty = 3, kVFull = 6, kVEmpty = 8, kSFull = 10, kPFull = 12, kPVDone = 13, kQFull = 14, kDrain = 15,
-  kNumBars = 16
+  kKFull = 0, kKEmpty = 3, kVFull = 6, kVEmpty = 9, kSFull = 12, kPFull = 14, kPVDone = 16,
+  kQFull = 18, kDrain = 19, kNumBars = 20
 };
 constexpr uint32_t kTmemSlot = 8 * kNumBars;   // the allocated TMEM base address
 
@@ -148,6 +152,18 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16: A (M x 16) lane i = row i,
+// 16-bit pairs along K packed in 32-bit columns.
+__device__ __forceinline__ void tc_mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -257,7 +273,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   const int nseg = kTcKeys / p.seg_rows;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], (i == kPFull || i == kQFull) ? (uint32_t)kSoftmax : 1u);
+    for (int i = 0; i < kNumBars; ++i)
+      mbar_init(&bars[i], (i == kPFull || i == kPFull + 1 || i == kQFull) ? (uint32_t)kSoftmax : 1u);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(base + L::kBar + kTmemSlot, kTmemCols);
@@ -378,18 +395,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
           tc_commit(&bars[kKEmpty + js % kKStages]);
           ++js;
           t_start = globaltimer_ns();
-        } else if (jp < js && mbar_test(&bars[kPFull], jp & 1) &&
+        } else if (jp < js && mbar_test(&bars[kPFull + (jp & 1)], (jp >> 1) & 1) &&
                    mbar_test(&bars[kVFull + jp % kVStages], (jp / kVStages) & 1)) {
           tc_fence_after();
           const uint32_t vb = base + L::kV + (jp % kVStages) * H * kHalf;
 #pragma unroll
-          for (int k = 0; k < kTcKeys / 16; ++k) {
-            const uint32_t poff = (k >> 2) * kHalf + (k & 3) * 32;
-            tc_mma(tmem + kColO, smem_desc(base + L::kP + poff, 16, 1024), smem_desc(vb + k * 2048, kHalf, 1024),
-                   id_pv, (jp > 0 || k > 0) ? 1u : 0u);
-          }
+          for (int k = 0; k < kTcKeys / 16; ++k)      // 16 keys = 8 packed P columns per step
+            tc_mma_tmem_a(tmem + kColO, tmem + kColP + (jp & 1) * (kTcKeys / 2) + k * 8,
+                          smem_desc(vb + k * 2048, kHalf, 1024), id_pv, (jp > 0 || k > 0) ? 1u : 0u);
           tc_commit(&bars[kVEmpty + jp % kVStages]);
-          tc_commit(&bars[kPVDone]);
+          tc_commit(&bars[kPVDone + (jp & 1)]);
           ++jp;
           t_start = globaltimer_ns();
         } else if (globaltimer_ns() - t_start > 2000000000ull) {
@@ -486,11 +501,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         pk[c / 2] = Mma<T>::pack(e0, e1);
       }
       l = l * alpha + rs;                          // this thread's share of the row sum
-      if (j > 0) {
-        // PV(j-1) has finished: O may be rescaled and the P tile rewritten
-        if (ok) ok = __all_sync(FULL_MASK, mbar_wait_bounded(&bars[kPVDone], (j - 1) & 1));
+      // P buffer j & 1 is free once PV(j - 2) has finished; O may be rescaled
+      // once PV(j - 1) has (each P buffer has its own completion barrier)
+      if (j >= 2 && ok) ok = __all_sync(FULL_MASK, mbar_wait_bounded(&bars[kPVDone + (j & 1)], ((j - 2) >> 1) & 1));
+      if (j >= 1 && __any_sync(FULL_MASK, scale_o)) {
+        if (ok) ok = __all_sync(FULL_MASK, mbar_wait_bounded(&bars[kPVDone + ((j - 1) & 1)], ((j - 1) >> 1) & 1));
         tc_fence_after();
-        if (ok && __any_sync(FULL_MASK, scale_o)) {
+        if (ok) {
 #pragma unroll 1
           for (int c4 = 0; c4 < kOCols / 32; ++c4) {
             float o[32];
@@ -504,11 +521,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
           tmem_st_wait();
         }
       }
-      // this thread's 64 keys are P half `half`: 8 chunks of 16 bytes per row
-#pragma unroll
-      for (int chunk = 0; chunk < 8; ++chunk)
-        st_shared_v4(base + L::kP + half * kHalf + swz(r, chunk),
-                     make_uint4(pk[chunk * 4], pk[chunk * 4 + 1], pk[chunk * 4 + 2], pk[chunk * 4 + 3]));
+      tc_fence_after();
+      // this thread's 64 keys: 32 packed columns of P buffer j & 1
+      tmem_st32(tmem + lane_base + kColP + (j & 1) * (kTcKeys / 2) + half * (kCols / 2),
+                reinterpret_cast<const float*>(pk));
+      tmem_st_wait();
       // V rows outside [lo, hi] of an edge tile become zeros (thread (r, h)
       // clears the h-th 64-column half of V row r)
       if (kbase < lo || kbase + kTcKeys - 1 > hi) {
@@ -523,9 +540,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars[kPFull]);
+      mbar_arrive(&bars[kPFull + (j & 1)]);
     }
-    if (ok) ok = __all_sync(FULL_MASK, mbar_wait_bounded(&bars[kPVDone], (n - 1) & 1));
+    if (ok) ok = __all_sync(FULL_MASK, mbar_wait_bounded(&bars[kPVDone + ((n - 1) & 1)], ((n - 1) >> 1) & 1));
     // the row sum: this thread's share plus its partner's
     xch[half * 128 + r] = l;
     pair_sync();

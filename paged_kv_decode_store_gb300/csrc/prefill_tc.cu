@@ -48,41 +48,40 @@ namespace pkvd {
 
 namespace {
 
-constexpr int kTcRows = 128;          // M: query rows per CTA
-constexpr int kTcKeys = 128;          // keys per tile
-constexpr int kTcThreads = 320;       // 8 softmax warps, producer, MMA
-constexpr int kSoftmax = 256;         // softmax threads: two per query row
+constexpr int kTcRows = 128;          // M: query rows per Q tile (two Q tiles per CTA)
+constexpr int kTcKeys = 128;          // keys per K/V tile
+constexpr int kTcThreads = 320;       // 2 x 4 softmax warps, producer, MMA
+constexpr int kGroup = 128;           // softmax threads per Q tile (one per row)
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr uint32_t kHalf = 128u * 128u;   // one 128-row x 64-column 16-bit half tile
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;         // S buffers at columns [0,128) and [128,256)
-constexpr uint32_t kColO = 256;       // O at [256, 256 + head_dim)
-constexpr uint32_t kColP = 384;       // P buffers (16-bit pairs) at [384, 448) and [448, 512)
+// TMEM columns: S of Q tile g at [128 g, 128 g + 128) (P of that tile is written
+// over its first 64 columns once S is read); O of Q tile g at [256 + g D, 256 + g D + D)
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 256;
 constexpr float kRebase = 8.f;        // re-base the running max when it grows by > 2^8
 
-// K and V each run up to three tiles ahead of the tensor cores.
-constexpr int kKStages = 3, kVStages = 3;
+// K runs up to three tiles ahead of the tensor cores, V two.
+constexpr int kKStages = 3, kVStages = 2;
 
 template <int D>
 struct TcLayout {
   static constexpr int kHalves = D / 64;
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + kHalves * kHalf;                 // kKStages stages
+  static constexpr uint32_t kQ = 0;                                    // 2 Q tiles
+  static constexpr uint32_t kK = kQ + 2 * kHalves * kHalf;             // kKStages stages
   static constexpr uint32_t kV = kK + kKStages * kHalves * kHalf;      // kVStages stages
   static constexpr uint32_t kBar = kV + kVStages * kHalves * kHalf;
-  static constexpr uint32_t kX = kBar + 256;                    // row-pair exchange: 2 x 128 floats
   // + alignment slack; at least 120 KB so that one CTA (which holds all 512
   // TMEM columns) is resident per SM
-  static constexpr uint32_t kBytes = kX + 1024 + 1024 > 122880u ? kX + 1024 + 1024 : 122880u;
+  static constexpr uint32_t kBytes = kBar + 256 + 1024 > 122880u ? kBar + 256 + 1024 : 122880u;
 };
 
-// mbarrier slots (8 bytes each) after kBar
-// P-full and PV-done have one barrier per P buffer (index j & 1): with P
-// double-buffered the softmax may finish tile j + 1 before PV(j) is issued,
-// and a single barrier would then run two phases ahead of its waiter.
+// mbarrier slots (8 bytes each) after kBar.  Per-Q-tile barriers take + g.
+// Every barrier's next phase depends on its waiter having passed the current
+// one, so no waiter ever sees a barrier two phases ahead.
 enum : int {
-  kKFull = 0, kKEmpty = 3, kVFull = 6, kVEmpty = 9, kSFull = 12, kPFull = 14, kPVDone = 16,
-  kQFull = 18, kDrain = 19, kNumBars = 20
+  kKFull = 0, kKEmpty = 3, kVFull = 6, kVReady = 8, kVEmpty = 10, kQFull = 12, kSFull = 14, kPFull = 16,
+  kPVDone = 18, kDrain = 20, kNumBars = 21
 };
 constexpr uint32_t kTmemSlot = 8 * kNumBars;   // the allocated TMEM base address
 
@@ -242,7 +241,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   const uint32_t base = (raw + 1023u) & ~1023u;          // 1024-byte aligned: whole swizzle atoms
   uint8_t* gbase = smem_raw + (base - raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + L::kBar);
-  const int hk = blockIdx.x, seq = blockIdx.y, ztile = blockIdx.z;
+  const int hk = blockIdx.x, seq = blockIdx.y, zpair = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   pdl_wait();      // the cache rows of this step come from the store kernel
@@ -253,28 +252,39 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   const int qlen = q1 - q0;
   if (q0 < 0 || qlen < 0 || klen < qlen || q1 > p.total_q ||
       (int64_t)klen > (int64_t)p.max_blocks * p.block_size) {
-    if (threadIdx.x == 0 && ztile == 0 && hk == 0) flag_error(p.err, PKVD_ERR_CONTEXT);
+    if (threadIdx.x == 0 && zpair == 0 && hk == 0) flag_error(p.err, PKVD_ERR_CONTEXT);
     return;
   }
-  if (ztile == 0 && hk == 0 && threadIdx.x == 0 && qlen > (int)gridDim.z * p.tile_tokens)
-    flag_error(p.err, PKVD_ERR_CONTEXT);
-  const int tok_end = qlen - ztile * p.tile_tokens;
-  if (tok_end <= 0) return;
-  const int tok_begin = max(0, tok_end - p.tile_tokens);
-  const int G = p.group;
-  const int qrows = (tok_end - tok_begin) * G;
-  const int cached = klen - qlen;
-  const int pos_first = cached + tok_begin, pos_last = cached + tok_end - 1;
-  const int lo = tc_window_start(pos_first + 1, p.window);
-  const int hi = pos_last;
-  const int kt_first = lo / kTcKeys, kt_last = hi / kTcKeys;
-  const int n = kt_last - kt_first + 1;
+  if (zpair == 0 && hk == 0 && threadIdx.x == 0 && qlen > 2 * (int)gridDim.z * p.tile_tokens)
+    flag_error(p.err, PKVD_ERR_CONTEXT);   // longer than max_seqlen_q: the earliest tokens are not computed
+  // Q tile g = 1 holds the later tokens (tile 2 zpair counted from the end),
+  // g = 0 the tile before it (may be empty).
+  const int Tt = p.tile_tokens, G = p.group, cached = klen - qlen;
+  int tb[2], te[2], lo_g[2], hi_g[2];
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    te[g] = qlen - (2 * zpair + 1 - g) * Tt;
+    tb[g] = max(0, te[g] - Tt);
+    lo_g[g] = tc_window_start(cached + tb[g] + 1, p.window);   // first key the tile's rows read
+    hi_g[g] = cached + te[g] - 1;                               // last key
+  }
+  if (te[1] <= 0) return;
+  const bool has0 = te[0] > 0;
+  const int lo = has0 ? lo_g[0] : lo_g[1], hi = hi_g[1];        // union of both tiles' keys
+  const int kt_first = lo / kTcKeys;
+  const int n = hi / kTcKeys - kt_first + 1;                    // K/V tiles of the CTA
+  int gf[2], gn[2];                                             // each Q tile's K/V tiles
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    gf[g] = lo_g[g] / kTcKeys - kt_first;
+    gn[g] = (g == 0 && !has0) ? 0 : hi_g[g] / kTcKeys - lo_g[g] / kTcKeys + 1;
+  }
   const int32_t* table = p.tables + (int64_t)seq * p.max_blocks;
   const int nseg = kTcKeys / p.seg_rows;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i)
-      mbar_init(&bars[i], (i == kPFull || i == kPFull + 1 || i == kQFull) ? (uint32_t)kSoftmax : 1u);
+      mbar_init(&bars[i], (i == kQFull || i == kQFull + 1 || i == kPFull || i == kPFull + 1) ? (uint32_t)kGroup : 1u);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(base + L::kBar + kTmemSlot, kTmemCols);
@@ -287,7 +297,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     // ------------------------------------------------------------ producer
     // Lane 0 polls for free stages and picks the next copy: K runs up to
     // kKStages tiles ahead but at most one tile ahead of V while V can go.
-    // Lane s looks up and copies segment s of the tile.
+    // Lane s looks up and copies segment s of the tile.  A V tile with rows
+    // outside [lo, hi] (the first and last tiles) is waited for here and
+    // those rows zeroed before the tile is released (V ready), so rows
+    // outside every query's range never weigh in.
     const uint32_t box = (uint32_t)p.seg_rows * 128u;
     int kt = 0, vt = 0;
     bool ok = true;
@@ -296,9 +309,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_v)) : "memory");
     }
     uint64_t t_start = globaltimer_ns();       // the last progress
-    // Block-table entries are fetched one tile ahead (lane s: segment s);
-    // kNone marks a segment that misses [lo, hi] (nothing to load).
-    constexpr int kNone = INT_MIN;
+    constexpr int kNone = INT_MIN;             // a segment that misses [lo, hi]: nothing to load
     auto fetch = [&](int t) -> int {
       if (t >= n || lane >= nseg) return kNone;
       const int ks = (kt_first + t) * kTcKeys + lane * p.seg_rows;
@@ -313,7 +324,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
             kt < n && (kt < kKStages || mbar_test(&bars[kKEmpty + kt % kKStages], ((kt / kKStages) - 1) & 1));
         const bool can_v =
             vt < kt && (vt < kVStages || mbar_test(&bars[kVEmpty + vt % kVStages], ((vt / kVStages) - 1) & 1));
-        // K leads V by at most one tile unless V cannot go
         if (can_v && (vt + 1 < kt || !can_k)) what = 2;
         else if (can_k) what = 1;
         else if (globaltimer_ns() - t_start > 2000000000ull) what = -1;
@@ -329,7 +339,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       const uint32_t loaded = __ballot_sync(FULL_MASK, good);
       if (what == 1 && __ballot_sync(FULL_MASK, raw != kNone && !good) && lane == 0)
         flag_error(p.err, PKVD_ERR_BLOCK_ID);
-      const int phys = raw;
       const int j = what == 1 ? kt : vt;
       const int stg = what == 1 ? kt % kKStages : vt % kVStages;
       uint64_t* bar = &bars[(what == 1 ? kKFull : kVFull) + stg];
@@ -349,7 +358,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       if ((loaded >> lane) & 1u) {
         const int ks = kbase + lane * p.seg_rows;
 #pragma unroll
-        for (int h = 0; h < H; ++h) tma_load4(dst0 + h * kHalf + lane * box, map, h * 64, hk, ks % p.block_size, phys, bar);
+        for (int h = 0; h < H; ++h) tma_load4(dst0 + h * kHalf + lane * box, map, h * 64, hk, ks % p.block_size, raw, bar);
+      }
+      if (what == 2) {
+        // V ready: at once, or, for an edge tile, once its rows outside [lo, hi] are zero
+        if (kbase < lo || kbase + kTcKeys - 1 > hi) {
+          if (lane == 0) ok = mbar_wait_bounded(bar, (vt / kVStages) & 1);
+          if (!(ok = __shfl_sync(FULL_MASK, ok, 0))) {
+            ++vt;
+            break;
+          }
+          for (int rr = lane; rr < kTcKeys; rr += 32) {
+            const int kp = kbase + rr;
+            if (kp >= lo && kp <= hi) continue;
+            for (int h = 0; h < H; ++h)
+              for (int c = 0; c < 8; ++c) st_shared_v4(dst0 + h * kHalf + rr * 128 + c * 16, make_uint4(0u, 0u, 0u, 0u));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) mbar_arrive(&bars[kVReady + stg]);
       }
       if (what == 1) {
         ++kt;
@@ -370,46 +398,65 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
-    // One thread issues whichever product is ready first: S(js) once K(js)
-    // has landed and the S buffer is free (PV(js - 2) issued), or PV(jp) once
-    // P(jp) and V(jp) are ready.
+    // One thread issues whatever is ready, for either Q tile g: S_g(j) once
+    // K has landed, Q_g is loaded and PV_g(j - 1) has finished (P_g(j - 1)
+    // lives in the S_g columns), or PV_g(j) once P_g(j) and V are ready.
+    // A K (V) stage is released by the last Q tile that uses it.
     if (lane == 0) {
       constexpr uint32_t fmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
       constexpr uint32_t id_s = tc_idesc(fmt, kTcKeys, 0), id_pv = tc_idesc(fmt, D, 1);
-      bool ok = mbar_wait_bounded(&bars[kQFull], 0);
-      tc_fence_after();
-      int js = 0, jp = 0;
+      int js[2] = {0, 0}, jp[2] = {0, 0};
+      bool ok = true;
       uint64_t t_start = globaltimer_ns();        // the last progress
-      while (ok && jp < n) {
-        if (js < n && js <= jp + 1 && mbar_test(&bars[kKFull + js % kKStages], (js / kKStages) & 1)) {
-          tc_fence_after();
-          const int sb = js & 1;
-          const uint32_t kb = base + L::kK + (js % kKStages) * H * kHalf;
+      auto uses = [&](int g, int t) { return t >= gf[g] && t < gf[g] + gn[g]; };
+      while (ok && (jp[0] < gn[0] || jp[1] < gn[1])) {
+        bool progressed = false;
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
-            tc_mma(tmem + kColS + sb * kTcKeys, smem_desc(base + L::kQ + off, 16, 1024),
-                   smem_desc(kb + off, 16, 1024), id_s, k > 0);
+        for (int g = 0; g < 2; ++g) {
+          if (js[g] < gn[g]) {
+            const int t = gf[g] + js[g];
+            const bool ready = (js[g] == 0 ? mbar_test(&bars[kQFull + g], 0)
+                                           : mbar_test(&bars[kPVDone + g], (js[g] - 1) & 1)) &&
+                               mbar_test(&bars[kKFull + t % kKStages], (t / kKStages) & 1);
+            if (ready) {
+              tc_fence_after();
+              const uint32_t qb = base + L::kQ + g * H * kHalf;
+              const uint32_t kb = base + L::kK + (t % kKStages) * H * kHalf;
+#pragma unroll
+              for (int k = 0; k < D / 16; ++k) {
+                const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
+                tc_mma(tmem + kColS + g * kTcKeys, smem_desc(qb + off, 16, 1024), smem_desc(kb + off, 16, 1024),
+                       id_s, k > 0);
+              }
+              tc_commit(&bars[kSFull + g]);
+              const int o = 1 - g;
+              if (!uses(o, t) || js[o] > t - gf[o]) tc_commit(&bars[kKEmpty + t % kKStages]);
+              ++js[g];
+              progressed = true;
+            }
           }
-          tc_commit(&bars[kSFull + sb]);
-          tc_commit(&bars[kKEmpty + js % kKStages]);
-          ++js;
-          t_start = globaltimer_ns();
-        } else if (jp < js && mbar_test(&bars[kPFull + (jp & 1)], (jp >> 1) & 1) &&
-                   mbar_test(&bars[kVFull + jp % kVStages], (jp / kVStages) & 1)) {
-          tc_fence_after();
-          const uint32_t vb = base + L::kV + (jp % kVStages) * H * kHalf;
+          if (jp[g] < js[g]) {
+            const int t = gf[g] + jp[g];
+            const bool ready = mbar_test(&bars[kPFull + g], jp[g] & 1) &&
+                               mbar_test(&bars[kVFull + t % kVStages], (t / kVStages) & 1) &&
+                               mbar_test(&bars[kVReady + t % kVStages], (t / kVStages) & 1);
+            if (ready) {
+              tc_fence_after();
+              const uint32_t vb = base + L::kV + (t % kVStages) * H * kHalf;
 #pragma unroll
-          for (int k = 0; k < kTcKeys / 16; ++k)      // 16 keys = 8 packed P columns per step
-            tc_mma_tmem_a(tmem + kColO, tmem + kColP + (jp & 1) * (kTcKeys / 2) + k * 8,
-                          smem_desc(vb + k * 2048, kHalf, 1024), id_pv, (jp > 0 || k > 0) ? 1u : 0u);
-          tc_commit(&bars[kVEmpty + jp % kVStages]);
-          tc_commit(&bars[kPVDone + (jp & 1)]);
-          ++jp;
-          t_start = globaltimer_ns();
-        } else if (globaltimer_ns() - t_start > 2000000000ull) {
-          ok = false;
+              for (int k = 0; k < kTcKeys / 16; ++k)      // 16 keys = 8 packed P columns per step
+                tc_mma_tmem_a(tmem + kColO + g * D, tmem + kColS + g * kTcKeys + k * 8,
+                              smem_desc(vb + k * 2048, kHalf, 1024), id_pv, (jp[g] > 0 || k > 0) ? 1u : 0u);
+              tc_commit(&bars[kPVDone + g]);
+              const int o = 1 - g;
+              if (!uses(o, t) || jp[o] > t - gf[o]) tc_commit(&bars[kVEmpty + t % kVStages]);
+              ++jp[g];
+              progressed = true;
+            }
+          }
         }
+        if (progressed) t_start = globaltimer_ns();
+        else if (globaltimer_ns() - t_start > 2000000000ull) ok = false;
       }
       if (!ok) {
         flag_error(p.err, PKVD_ERR_TIMEOUT);
@@ -419,158 +466,120 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     }
   } else {
     // ------------------------------------------------------------ softmax
-    // Two threads per query row: thread (r, half) owns TMEM lane r, key
-    // columns [64 half, 64 half + 64) of S and P, and output columns
-    // [half D/2, half D/2 + D/2) of O.  The pair (warps w and w + 4) trades
-    // row maxima and sums through shared memory behind a 64-thread barrier.
-    const int r = threadIdx.x & 127, half = threadIdx.x >> 7;
+    // Group g (warps 4g .. 4g + 3) owns Q tile g; thread r owns its row r =
+    // TMEM lane r: it reads the row's S from TMEM, masks (causal, window),
+    // keeps a running max re-based only when it grows by more than 2^8
+    // (exact; O is rescaled in TMEM rarely), writes P = 2^(s - max) as packed
+    // 16-bit pairs over the first 64 S columns, and at the end reads O,
+    // divides by the row sum and stores it.
+    const int g = warp >> 2, r = threadIdx.x & 127;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const int pair_bar = 1 + (warp & 3);
-    float* xch = reinterpret_cast<float*>(gbase + L::kX);   // [2][128]
-    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
-    const bool live = r < qrows;
-    const int tt = live ? r / G : 0, g = live ? r - (r / G) * G : 0;
-    const int pr = pos_first + tt;                 // padding rows mirror row 0
-    const int wr = tc_window_start(pr + 1, p.window);
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
-                                                        ((int64_t)(q0 + tok_begin + tt) * p.hq + (int64_t)hk * G + g) * D);
+    // this group's tile, as scalars (no runtime-indexed arrays)
+    const int my_tb = g ? tb[1] : tb[0], my_te = g ? te[1] : te[0];
+    const int my_gf = g ? gf[1] : gf[0], my_gn = g ? gn[1] : gn[0];
+    if (my_gn > 0) {
+      const int qrows = (my_te - my_tb) * G;
+      const bool live = r < qrows;
+      const int tt = live ? r / G : 0, gi = live ? r - (r / G) * G : 0;
+      const int pr = cached + my_tb + tt;          // padding rows mirror row 0
+      const int wr = tc_window_start(pr + 1, p.window);
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const T*>(p.q) + ((int64_t)(q0 + my_tb + tt) * p.hq + (int64_t)hk * G + gi) * D);
 #pragma unroll
-      for (int c = half * (D / 16); c < (half + 1) * (D / 16); ++c) {
-        const uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-        st_shared_v4(base + L::kQ + (c >> 3) * kHalf + swz(r, c & 7), v);
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+          st_shared_v4(base + L::kQ + (g * H + (c >> 3)) * kHalf + swz(r, c & 7), v);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[kQFull + g]);
       }
-      fence_proxy_async_smem();
-      mbar_arrive(&bars[kQFull]);
-    }
-
-    constexpr int kCols = kTcKeys / 2;            // key columns per thread
-    constexpr int kOCols = D / 2;                 // output columns per thread
-    const int c_base = half * kCols;
-    float m_ref = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int st = j & 1;
-      const int kbase = (kt_first + j) * kTcKeys;
-      // this row's usable columns of the tile, as bits of this thread's 64
-      const int c_lo = max(wr - kbase - c_base, 0), c_hi = min(pr - kbase - c_base, kCols - 1);
-      const bool row_full = c_lo == 0 && c_hi == kCols - 1;
-      uint32_t mw[2];
+      const uint32_t s_addr = tmem + lane_base + kColS + g * kTcKeys;
+      const uint32_t o_addr = tmem + lane_base + kColO + g * D;
+      float m_ref = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < my_gn; ++j) {
+        const int kbase = (kt_first + my_gf + j) * kTcKeys;
+        const int c_lo = max(wr - kbase, 0), c_hi = min(pr - kbase, kTcKeys - 1);
+        const bool row_full = c_lo == 0 && c_hi == kTcKeys - 1;
+        uint32_t mw[kTcKeys / 32];
 #pragma unroll
-      for (int w = 0; w < 2; ++w) {
-        const int a = min(max(c_lo - 32 * w, 0), 32), z = min(max(c_hi + 1 - 32 * w, 0), 32);
-        mw[w] = (z == 32 ? 0xffffffffu : ((1u << z) - 1u)) & ~(a == 32 ? 0xffffffffu : ((1u << a) - 1u));
-      }
-
-      // After a timeout (ok false) the loop still runs to the end without
-      // waiting, so the two warps of a pair always meet at the same barriers.
-      if (ok) ok = __all_sync(FULL_MASK, mbar_wait_bounded(&bars[kSFull + st], (j >> 1) & 1));
-      tc_fence_after();
-      const uint32_t s_addr = tmem + lane_base + kColS + st * kTcKeys + c_base;
-      float v[kCols];
-      tmem_ld32(s_addr, v);
-      tmem_ld32(s_addr + 32, v + 32);
-      tmem_ld_wait();
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int c = 0; c < kCols; ++c) {
-        const float x = v[c] * p.scale_log2;
-        v[c] = (row_full || ((mw[c >> 5] >> (c & 31)) & 1u)) ? x : -INFINITY;
-        mx[c & 3] = fmaxf(mx[c & 3], v[c]);
-      }
-      const float m_own = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      xch[half * 128 + r] = m_own;
-      pair_sync();
-      const float mt = fmaxf(m_own, xch[(half ^ 1) * 128 + r]);
-      pair_sync();                                 // both read before the next tile writes
-      // Re-base the running max only when it grows by more than 2^kRebase:
-      // exponents stay <= 2^8 and O is rescaled rarely (exact either way).
-      // Both threads of a row take the same decisions from the same values.
-      const bool rebase = mt > m_ref + kRebase;
-      const bool scale_o = rebase && m_ref != -INFINITY;
-      const float alpha = scale_o ? tc_ex2(m_ref - mt) : 1.f;
-      if (rebase) m_ref = mt;
-      const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-      // P = 2^(score - mu), packed to 16-bit pairs in registers
-      uint32_t pk[kCols / 2];
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < kCols; c += 2) {
-        const float e0 = tc_ex2(v[c] - mu), e1 = tc_ex2(v[c + 1] - mu);
-        rs += e0 + e1;
-        pk[c / 2] = Mma<T>::pack(e0, e1);
-      }
-      l = l * alpha + rs;                          // this thread's share of the row sum
-      // P buffer j & 1 is free once PV(j - 2) has finished; O may be rescaled
-      // once PV(j - 1) has (each P buffer has its own completion barrier)
-      if (j >= 2 && ok) ok = __all_sync(FULL_MASK, mbar_wait_bounded(&bars[kPVDone + (j & 1)], ((j - 2) >> 1) & 1));
-      if (j >= 1 && __any_sync(FULL_MASK, scale_o)) {
-        if (ok) ok = __all_sync(FULL_MASK, mbar_wait_bounded(&bars[kPVDone + ((j - 1) & 1)], ((j - 1) >> 1) & 1));
+        for (int w = 0; w < kTcKeys / 32; ++w) {
+          const int a = min(max(c_lo - 32 * w, 0), 32), z = min(max(c_hi + 1 - 32 * w, 0), 32);
+          mw[w] = (z == 32 ? 0xffffffffu : ((1u << z) - 1u)) & ~(a == 32 ? 0xffffffffu : ((1u << a) - 1u));
+        }
+        ok = __all_sync(FULL_MASK, mbar_wait_bounded(&bars[kSFull + g], j & 1));
+        if (!ok) break;
         tc_fence_after();
-        if (ok) {
+        float v[kTcKeys];
+#pragma unroll
+        for (int c4 = 0; c4 < kTcKeys / 32; ++c4) tmem_ld32(s_addr + c4 * 32, v + c4 * 32);
+        tmem_ld_wait();
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < kTcKeys; ++c) {
+          const float x = v[c] * p.scale_log2;
+          v[c] = (row_full || ((mw[c >> 5] >> (c & 31)) & 1u)) ? x : -INFINITY;
+          mx[c & 3] = fmaxf(mx[c & 3], v[c]);
+        }
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        const bool rebase = mt > m_ref + kRebase;
+        const bool scale_o = rebase && m_ref != -INFINITY;
+        const float alpha = scale_o ? tc_ex2(m_ref - mt) : 1.f;
+        if (rebase) m_ref = mt;
+        const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+        uint32_t pk[kTcKeys / 2];
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < kTcKeys; c += 2) {
+          const float e0 = tc_ex2(v[c] - mu), e1 = tc_ex2(v[c + 1] - mu);
+          rs += e0 + e1;
+          pk[c / 2] = Mma<T>::pack(e0, e1);
+        }
+        l = l * alpha + rs;
+        // PV(j - 1) has finished (S(j) was issued after it): O may be rescaled
+        if (__any_sync(FULL_MASK, scale_o)) {
 #pragma unroll 1
-          for (int c4 = 0; c4 < kOCols / 32; ++c4) {
+          for (int c4 = 0; c4 < D / 32; ++c4) {
             float o[32];
-            const uint32_t oa = tmem + lane_base + kColO + half * kOCols + c4 * 32;
-            tmem_ld32(oa, o);
+            tmem_ld32(o_addr + c4 * 32, o);
             tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tmem_st32(oa, o);
-          }
-          tmem_st_wait();
-        }
-      }
-      tc_fence_after();
-      // this thread's 64 keys: 32 packed columns of P buffer j & 1
-      tmem_st32(tmem + lane_base + kColP + (j & 1) * (kTcKeys / 2) + half * (kCols / 2),
-                reinterpret_cast<const float*>(pk));
-      tmem_st_wait();
-      // V rows outside [lo, hi] of an edge tile become zeros (thread (r, h)
-      // clears the h-th 64-column half of V row r)
-      if (kbase < lo || kbase + kTcKeys - 1 > hi) {
-        if (ok) ok = __all_sync(FULL_MASK, mbar_wait_bounded(&bars[kVFull + j % kVStages], (j / kVStages) & 1));
-        const int kp = kbase + r;
-        if ((kp < lo || kp > hi) && half < H) {
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_shared_v4(base + L::kV + ((j % kVStages) * H + half) * kHalf + r * 128 + c * 16,
-                         make_uint4(0u, 0u, 0u, 0u));
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bars[kPFull + (j & 1)]);
-    }
-    if (ok) ok = __all_sync(FULL_MASK, mbar_wait_bounded(&bars[kPVDone + ((n - 1) & 1)], ((n - 1) >> 1) & 1));
-    // the row sum: this thread's share plus its partner's
-    xch[half * 128 + r] = l;
-    pair_sync();
-    const float l_row = l + xch[(half ^ 1) * 128 + r];
-    if (ok) {
-      tc_fence_after();
-      const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-      T* dst = static_cast<T*>(p.out) + ((int64_t)(q0 + tok_begin + tt) * p.hq + (int64_t)hk * G + g) * D +
-               half * kOCols;
-#pragma unroll
-      for (int c4 = 0; c4 < kOCols / 32; ++c4) {
-        float o[32];
-        tmem_ld32(tmem + lane_base + kColO + half * kOCols + c4 * 32, o);
-        tmem_ld_wait();
-        if (live) {
-#pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            uint4 w;
-            w.x = Mma<T>::pack(o[c8 * 8 + 0] * inv, o[c8 * 8 + 1] * inv);
-            w.y = Mma<T>::pack(o[c8 * 8 + 2] * inv, o[c8 * 8 + 3] * inv);
-            w.z = Mma<T>::pack(o[c8 * 8 + 4] * inv, o[c8 * 8 + 5] * inv);
-            w.w = Mma<T>::pack(o[c8 * 8 + 6] * inv, o[c8 * 8 + 7] * inv);
-            *reinterpret_cast<uint4*>(dst + c4 * 32 + c8 * 8) = w;
+            tmem_st32(o_addr + c4 * 32, o);
           }
         }
+        tmem_st32(s_addr, reinterpret_cast<const float*>(pk));
+        tmem_st32(s_addr + 32, reinterpret_cast<const float*>(pk + 32));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[kPFull + g]);
       }
-    } else if (lane == 0) {
-      flag_error(p.err, PKVD_ERR_TIMEOUT);
+      if (ok) ok = __all_sync(FULL_MASK, mbar_wait_bounded(&bars[kPVDone + g], (my_gn - 1) & 1));
+      if (ok) {
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        T* dst = static_cast<T*>(p.out) + ((int64_t)(q0 + my_tb + tt) * p.hq + (int64_t)hk * G + gi) * D;
+#pragma unroll
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+          float o[32];
+          tmem_ld32(o_addr + c4 * 32, o);
+          tmem_ld_wait();
+          if (live) {
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+              uint4 w;
+              w.x = Mma<T>::pack(o[c8 * 8 + 0] * inv, o[c8 * 8 + 1] * inv);
+              w.y = Mma<T>::pack(o[c8 * 8 + 2] * inv, o[c8 * 8 + 3] * inv);
+              w.z = Mma<T>::pack(o[c8 * 8 + 4] * inv, o[c8 * 8 + 5] * inv);
+              w.w = Mma<T>::pack(o[c8 * 8 + 6] * inv, o[c8 * 8 + 7] * inv);
+              *reinterpret_cast<uint4*>(dst + c4 * 32 + c8 * 8) = w;
+            }
+          }
+        }
+      } else if (lane == 0) {
+        flag_error(p.err, PKVD_ERR_TIMEOUT);
+      }
     }
   }
 
@@ -667,7 +676,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
   prm.window = a.window;
   prm.err = a.err;
   const int tiles = (a.max_seqlen_q + prm.tile_tokens - 1) / prm.tile_tokens;
-  const dim3 grid(c.num_kv_heads, a.num_seqs, tiles);
+  const dim3 grid(c.num_kv_heads, a.num_seqs, (tiles + 1) / 2);   // two Q tiles per CTA
   if (c.dtype == PKVD_BF16)
     return c.head_dim == 64 ? launch_tc_typed<__nv_bfloat16, 64>(prm, grid, stream)
                             : launch_tc_typed<__nv_bfloat16, 128>(prm, grid, stream);

@@ -61,11 +61,11 @@ constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
 constexpr float kRebase = 8.f;        // re-base the running max when it grows by > 2^8
 
-// K runs up to three tiles ahead of the tensor cores, V two.
-constexpr int kKStages = 3, kVStages = 2;
-
 template <int D>
 struct TcLayout {
+  // K and V stages: as many as shared memory holds (K three and V two tiles
+  // ahead of the tensor cores for head_dim 128, four each for 64)
+  static constexpr int kKStages = D == 64 ? 4 : 3, kVStages = D == 64 ? 4 : 2;
   static constexpr int kHalves = D / 64;
   static constexpr uint32_t kQ = 0;                                    // 2 Q tiles
   static constexpr uint32_t kK = kQ + 2 * kHalves * kHalf;             // kKStages stages
@@ -80,8 +80,8 @@ struct TcLayout {
 // Every barrier's next phase depends on its waiter having passed the current
 // one, so no waiter ever sees a barrier two phases ahead.
 enum : int {
-  kKFull = 0, kKEmpty = 3, kVFull = 6, kVReady = 8, kVEmpty = 10, kQFull = 12, kSFull = 14, kPFull = 16,
-  kPVDone = 18, kDrain = 20, kNumBars = 21
+  kKFull = 0, kKEmpty = 4, kVFull = 8, kVReady = 12, kVEmpty = 16, kQFull = 20, kSFull = 22, kPFull = 24,
+  kPVDone = 26, kDrain = 28, kNumBars = 29
 };
 constexpr uint32_t kTmemSlot = 8 * kNumBars;   // the allocated TMEM base address
 
@@ -236,6 +236,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
   using L = TcLayout<D>;
   constexpr int H = L::kHalves;
+  constexpr int kKStages = L::kKStages, kVStages = L::kVStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;          // 1024-byte aligned: whole swizzle atoms

@@ -81,8 +81,12 @@ struct TcLayout {
 // one, so no waiter ever sees a barrier two phases ahead.
 enum : int {
   kKFull = 0, kKEmpty = 4, kVFull = 8, kVReady = 12, kVEmpty = 16, kQFull = 20, kSFull = 22, kPFull = 24,
-  kPVDone = 26, kDrain = 28, kNumBars = 29
+  kPVDone = 26, kSRead = 28, kDrain = 30, kNumBars = 31
 };
+// With head_dim 64 TMEM also holds a separate P buffer per Q tile at
+// [384 + 64 g, 448 + 64 g): the next S may then be computed as soon as the
+// softmax has read the current one (S-read barrier) instead of after its PV.
+constexpr uint32_t kColP64 = 384;
 constexpr uint32_t kTmemSlot = 8 * kNumBars;   // the allocated TMEM base address
 
 struct TcParams {
@@ -237,6 +241,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   using L = TcLayout<D>;
   constexpr int H = L::kHalves;
   constexpr int kKStages = L::kKStages, kVStages = L::kVStages;
+  constexpr bool kSepP = D == 64;                        // P in its own TMEM columns
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;          // 1024-byte aligned: whole swizzle atoms
@@ -285,7 +290,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i)
-      mbar_init(&bars[i], (i == kQFull || i == kQFull + 1 || i == kPFull || i == kPFull + 1) ? (uint32_t)kGroup : 1u);
+      mbar_init(&bars[i], (i == kQFull || i == kQFull + 1 || i == kPFull || i == kPFull + 1 || i == kSRead ||
+                           i == kSRead + 1) ? (uint32_t)kGroup : 1u);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(base + L::kBar + kTmemSlot, kTmemCols);
@@ -417,7 +423,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
           if (js[g] < gn[g]) {
             const int t = gf[g] + js[g];
             const bool ready = (js[g] == 0 ? mbar_test(&bars[kQFull + g], 0)
-                                           : mbar_test(&bars[kPVDone + g], (js[g] - 1) & 1)) &&
+                                           : kSepP ? mbar_test(&bars[kSRead + g], (js[g] - 1) & 1)
+                                                   : mbar_test(&bars[kPVDone + g], (js[g] - 1) & 1)) &&
                                mbar_test(&bars[kKFull + t % kKStages], (t / kKStages) & 1);
             if (ready) {
               tc_fence_after();
@@ -446,7 +453,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
               const uint32_t vb = base + L::kV + (t % kVStages) * H * kHalf;
 #pragma unroll
               for (int k = 0; k < kTcKeys / 16; ++k)      // 16 keys = 8 packed P columns per step
-                tc_mma_tmem_a(tmem + kColO + g * D, tmem + kColS + g * kTcKeys + k * 8,
+                tc_mma_tmem_a(tmem + kColO + g * D, tmem + (kSepP ? kColP64 + g * 64 : kColS + g * kTcKeys) + k * 8,
                               smem_desc(vb + k * 2048, kHalf, 1024), id_pv, (jp[g] > 0 || k > 0) ? 1u : 0u);
               tc_commit(&bars[kPVDone + g]);
               const int o = 1 - g;
@@ -516,6 +523,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
 #pragma unroll
         for (int c4 = 0; c4 < kTcKeys / 32; ++c4) tmem_ld32(s_addr + c4 * 32, v + c4 * 32);
         tmem_ld_wait();
+        if constexpr (kSepP) {
+          tc_fence_before();
+          mbar_arrive(&bars[kSRead + g]);            // the next S may overwrite these columns
+        }
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int c = 0; c < kTcKeys; ++c) {
@@ -538,7 +549,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
           pk[c / 2] = Mma<T>::pack(e0, e1);
         }
         l = l * alpha + rs;
-        // PV(j - 1) has finished (S(j) was issued after it): O may be rescaled
+        if constexpr (kSepP) {
+          // the P buffer and O are free once PV(j - 1) has finished
+          if (j > 0) {
+            ok = __all_sync(FULL_MASK, mbar_wait_bounded(&bars[kPVDone + g], (j - 1) & 1));
+            if (!ok) break;
+            tc_fence_after();
+          }
+        }
+        // PV(j - 1) has finished: O may be rescaled
         if (__any_sync(FULL_MASK, scale_o)) {
 #pragma unroll 1
           for (int c4 = 0; c4 < D / 32; ++c4) {
@@ -550,8 +569,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
             tmem_st32(o_addr + c4 * 32, o);
           }
         }
-        tmem_st32(s_addr, reinterpret_cast<const float*>(pk));
-        tmem_st32(s_addr + 32, reinterpret_cast<const float*>(pk + 32));
+        const uint32_t p_addr = kSepP ? tmem + lane_base + kColP64 + g * 64 : s_addr;
+        tmem_st32(p_addr, reinterpret_cast<const float*>(pk));
+        tmem_st32(p_addr + 32, reinterpret_cast<const float*>(pk + 32));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars[kPFull + g]);

@@ -34,6 +34,13 @@ def small_batches():
                                     head_dim=64, block_size=64, dtype="f16", q_kind="fixed",
                                     q_args=(20, 9), hit_kind="fixed", hit_args=(1, 0)),
         "chunked_small": wp.CHUNKED_PREFILL.scaled(num_seqs=2, q_args=(96,), hit_args=(256, 2)),
+        # block 8: one TMA box per 8-row swizzle atom; block 128: one box per K/V tile
+        "bs8_f16_d128": wp.PrefillConfig(name="bs8", index=10, num_seqs=3, num_q_heads=8, num_kv_heads=2,
+                                         head_dim=128, block_size=8, dtype="f16", q_kind="fixed",
+                                         q_args=(41, 300, 7), hit_kind="fixed", hit_args=(3, 0, 20)),
+        "bs128_bf16_d64": wp.PrefillConfig(name="bs128", index=11, num_seqs=3, num_q_heads=4, num_kv_heads=2,
+                                           head_dim=64, block_size=128, dtype="bf16", q_kind="fixed",
+                                           q_args=(129, 500, 2), hit_kind="fixed", hit_args=(1, 2, 0)),
     }
 
 

@@ -7,32 +7,34 @@
 // (k_len_i - q_len_i) + j and attends causally to positions 0..p of its
 // sequence through the block table).
 //
-// One CTA per (KV head, sequence, tile of 128 query rows); row = token * G +
-// query head of the group, so every K/V tile serves the whole GQA group.
-// Six warps with fixed roles:
-//   warps 0-3  softmax: thread t owns query row t = TMEM lane t.  Loads its Q
-//              row into shared memory, then per 128-key tile reads its row of
-//              S from TMEM, masks, keeps a running max (re-based only when it
-//              grows by more than 2^8, so O is rarely rescaled), writes
-//              P = 2^(S - max) as 16-bit values into shared memory, and at the
-//              end reads O from TMEM, divides by the row sum and stores it.
-//   warp 4     producer: TMA (cp.async.bulk.tensor, 128-byte swizzle) of the
+// One CTA per (KV head, sequence, pair of 128-row Q tiles); row = token * G +
+// query head of the group, so every K/V tile serves the whole GQA group, and
+// both Q tiles of the pair share each K/V tile the CTA loads.  Pairs are
+// counted from the end of each sequence and the pair index is the slowest grid
+// dimension: the heaviest causal work starts first.  Ten warps with fixed roles:
+//   warps 0-3, 4-7  softmax of Q tile 0 and 1: thread r owns query row r =
+//              TMEM lane r.  Loads its Q row into shared memory, then per
+//              128-key tile reads its row of S from TMEM, masks (causal,
+//              window), keeps a running max (re-based only when it grows by
+//              more than 2^8, so O is rarely rescaled), writes P = 2^(S - max)
+//              as packed 16-bit pairs into TMEM, and at the end reads O from
+//              TMEM, divides by the row sum and stores it.
+//   warp 8     producer: TMA (cp.async.bulk.tensor, 128-byte swizzle) of the
 //              K and V rows of each tile, one box per (cache block segment,
-//              64-column half), into two stages each.
-//   warp 5     MMA: allocates 512 TMEM columns; one thread issues
-//              S = Q K^T (M 128, N 128 keys, K = head_dim) into one of two S
-//              buffers and O += P V (M 128, N = head_dim, K 128 keys) with
-//              tcgen05.mma kind::f16 (fp32 accumulate), and signals mbarriers
-//              with tcgen05.commit.
-// S(j+1) and PV(j-1) run on the tensor cores while the softmax of tile j
-// runs.  Keys outside [first window start, last position] of the tile, and
-// segments whose block id is bad, are masked in S; their V rows are zeroed
-// in shared memory before PV, so poisoned rows never weigh in.
+//              64-column half); zeroes V rows outside the pair's key range in
+//              the first and last tiles before releasing them.
+//   warp 9     MMA: allocates 512 TMEM columns; one thread issues, whenever
+//              ready, S = Q K^T (M 128, N 128 keys, K = head_dim) and
+//              O += P V (M 128, N = head_dim, K 128 keys, P from TMEM) for
+//              either Q tile with tcgen05.mma kind::f16 (fp32 accumulate), and
+//              signals mbarriers with tcgen05.commit.
+// Keys outside a row's range are masked in S; segments whose block id is bad
+// read as zeros.
 //
 // Shared-memory operand layout (K-major, 128-byte swizzle): a 128-row tile of
 // 64 16-bit columns is 128 rows of 128 bytes, 16-byte chunk c of row r at
-// r*128 + ((c ^ (r % 8)) * 16); head_dim 128 uses two such halves.  Q, K and
-// P are read K-major (stride between 8-row groups 1024 B); V is read
+// r*128 + ((c ^ (r % 8)) * 16); head_dim 128 uses two such halves.  Q and K
+// are read K-major (stride between 8-row groups 1024 B); V is read
 // MN-major (head_dim contiguous: 1024 B between 8-key groups, one half-tile
 // between 64-column halves).
 #include <cuda.h>

@@ -88,23 +88,24 @@ def algorithmic_bytes(cfg, layout, window=0, extras=False):
             "step": attn + store + slots + sample}
 
 
-def kernel_source_hash():
+def kernel_source_hash(prefix="attention"):
+    """Hash of the kernel sources whose names start with `prefix`."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "paged_kv_decode_store_gb300", "csrc")
     for f in sorted(os.listdir(d)):
-        if f.startswith("attention"):
+        if f.startswith(prefix):
             with open(os.path.join(d, f), "rb") as fh:
                 h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(config_name):
-    """DRAM bytes per attention launch from the committed ncu summary, if it
-    was taken on the current attention sources."""
-    path = os.path.join(ROOT, "profiles", "attention_traffic.txt")
+def recorded_traffic(config_name, summary="attention_traffic.txt", prefix="attention"):
+    """DRAM bytes per kernel launch from a committed ncu summary, if it was
+    taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", summary)
     if not os.path.exists(path):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(prefix)
     for ln in open(path):
         parts = ln.split()
         if len(parts) >= 3 and not ln.startswith("#") and parts[0] == want and parts[1] == config_name:
@@ -653,7 +654,8 @@ def run_prefill_bench(args):
                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
                      "peak_source": "measured bf16 burst" if peaks.get("bf16_tflops") else "fallback",
-                     "traffic": None},
+                     "traffic": None if args.prefill_path == "mma" else
+                     recorded_traffic(cfg.name, "prefill_traffic.txt", "prefill_tc")},
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps, "clocks": clocks, "device_err_flag": 0,

@@ -18,6 +18,17 @@ int device_sm_count() {
   return n;
 }
 
+int64_t device_l2_bytes() {
+  static int64_t cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return 0;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
 }  // namespace pkvd
 
 using namespace pkvd;

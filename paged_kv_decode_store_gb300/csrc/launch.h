@@ -107,5 +107,6 @@ cudaError_t launch_sample_extras(const void* logits, int dtype, int num_rows, in
                                  float* top_probs, int32_t* top_ids, cudaStream_t stream);
 
 int device_sm_count();   // current device, cached; <= 0 on failure
+int64_t device_l2_bytes();   // current device's L2 size in bytes, cached; 0 on failure
 
 }  // namespace pkvd

@@ -10,8 +10,9 @@
 // One CTA per (KV head, sequence, pair of 128-row Q tiles); row = token * G +
 // query head of the group, so every K/V tile serves the whole GQA group, and
 // both Q tiles of the pair share each K/V tile the CTA loads.  Pairs are
-// counted from the end of each sequence and the pair index is the slowest grid
-// dimension: the heaviest causal work starts first.  Ten warps with fixed roles:
+// counted from the end of each sequence.  While the batch's K/V fits in L2
+// the heaviest pairs of every sequence start first; otherwise CTAs of one
+// (sequence, KV head) run together so that its K/V tiles stay in L2.  Ten warps with fixed roles:
 //   warps 0-3, 4-7  softmax of Q tile 0 and 1: thread r owns query row r =
 //              TMEM lane r.  Loads its Q row into shared memory, then per
 //              128-key tile reads its row of S from TMEM, masks (causal,
@@ -107,6 +108,9 @@ struct TcParams {
   int hq;
   int group;
   int tile_tokens;
+  int pairs;             // Q-tile pairs per (sequence, KV head): the grid is pairs x Hkv x num_seqs
+  int num_seqs;
+  int64_t l2_bytes;      // the device's L2 size, for the CTA order
   float scale_log2;
   int window;
   int32_t* err;
@@ -249,21 +253,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   const uint32_t base = (raw + 1023u) & ~1023u;          // 1024-byte aligned: whole swizzle atoms
   uint8_t* gbase = smem_raw + (base - raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + L::kBar);
-  const int hk = blockIdx.x, seq = blockIdx.y, zpair = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   pdl_wait();      // the cache rows of this step come from the store kernel
   pdl_trigger();
 
-  const int q0 = p.cu_q[seq], q1 = p.cu_q[seq + 1];
-  const int klen = p.cu_k[seq + 1] - p.cu_k[seq];
+  // CTA order: while the batch's K/V fits in L2, KV head fastest and pair
+  // slowest (the heaviest causal work of every sequence first); otherwise
+  // pair fastest, so CTAs resident together share one (sequence, KV head) and
+  // its K/V tiles stay in L2.  Every CTA takes the same decision; the
+  // sequence lengths of both candidate orders are loaded together with the
+  // batch's key count (one round trip).
+  // the grid is (KV heads, sequences, pairs); lin is the linear CTA index
+  const int nh = (int)gridDim.x;
+  const int lin = blockIdx.x + nh * (blockIdx.y + p.num_seqs * blockIdx.z);
+  const int seq_a = (lin / nh) % p.num_seqs, seq_b = lin / (p.pairs * nh);
+  const int total_keys = p.cu_k[p.num_seqs];
+  const int qa0 = p.cu_q[seq_a], qa1 = p.cu_q[seq_a + 1], ka0 = p.cu_k[seq_a], ka1 = p.cu_k[seq_a + 1];
+  const int qb0 = p.cu_q[seq_b], qb1 = p.cu_q[seq_b + 1], kb0 = p.cu_k[seq_b], kb1 = p.cu_k[seq_b + 1];
+  const bool by_cost = (int64_t)total_keys * nh * D * 4 <= p.l2_bytes;   // K and V, 16-bit
+  const int seq = by_cost ? seq_a : seq_b;
+  const int hk = by_cost ? lin % nh : (lin / p.pairs) % nh;
+  const int zpair = by_cost ? lin / (nh * p.num_seqs) : lin % p.pairs;
+  const int q0 = by_cost ? qa0 : qb0, q1 = by_cost ? qa1 : qb1;
+  const int klen = by_cost ? ka1 - ka0 : kb1 - kb0;
   const int qlen = q1 - q0;
   if (q0 < 0 || qlen < 0 || klen < qlen || q1 > p.total_q ||
       (int64_t)klen > (int64_t)p.max_blocks * p.block_size) {
     if (threadIdx.x == 0 && zpair == 0 && hk == 0) flag_error(p.err, PKVD_ERR_CONTEXT);
     return;
   }
-  if (zpair == 0 && hk == 0 && threadIdx.x == 0 && qlen > 2 * (int)gridDim.z * p.tile_tokens)
+  if (zpair == 0 && hk == 0 && threadIdx.x == 0 && qlen > 2 * p.pairs * p.tile_tokens)
     flag_error(p.err, PKVD_ERR_CONTEXT);   // longer than max_seqlen_q: the earliest tokens are not computed
   // Q tile g = 1 holds the later tokens (tile 2 zpair counted from the end),
   // g = 0 the tile before it (may be empty).
@@ -663,7 +683,8 @@ bool prefill_tc_supported(const PrefillArgs& a) {
   const pkvd_cache& c = a.cache;
   if (c.dtype != PKVD_F16 && c.dtype != PKVD_BF16) return false;
   if (c.head_dim != 64 && c.head_dim != 128) return false;
-  if (c.block_size < 8) return false;                       // a TMA box must fill whole 8-row swizzle atoms
+  if (c.block_size < 8) return false;
+                       // a TMA box must fill whole 8-row swizzle atoms
   const int G = a.num_q_heads / c.num_kv_heads;
   if (G < 1 || G > kTcRows) return false;
   if ((reinterpret_cast<uintptr_t>(a.out) & 15u) || (reinterpret_cast<uintptr_t>(a.q) & 15u)) return false;
@@ -699,7 +720,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
   prm.window = a.window;
   prm.err = a.err;
   const int tiles = (a.max_seqlen_q + prm.tile_tokens - 1) / prm.tile_tokens;
-  const dim3 grid(c.num_kv_heads, a.num_seqs, (tiles + 1) / 2);   // two Q tiles per CTA
+  prm.pairs = (tiles + 1) / 2;                                     // two Q tiles per CTA
+  prm.num_seqs = a.num_seqs;
+  prm.l2_bytes = device_l2_bytes();
+  if (prm.pairs > 65535 || a.num_seqs > 65535) return cudaErrorInvalidConfiguration;
+  const dim3 grid(c.num_kv_heads, a.num_seqs, prm.pairs);
   if (c.dtype == PKVD_BF16)
     return c.head_dim == 64 ? launch_tc_typed<__nv_bfloat16, 64>(prm, grid, stream)
                             : launch_tc_typed<__nv_bfloat16, 128>(prm, grid, stream);

@@ -565,7 +565,7 @@ def run_prefill_bench(args):
     def store():
         pk.kv_store_prefill(d["k"], d["v"], d["tables"], d["cu_q"], d["cu_k"], kc, vc, err=err)
 
-    path = {"auto": pk.PATH_AUTO, "tc": pk.PATH_TC, "mma": pk.PATH_MMA}[args.prefill_path]
+    path = {"auto": pk.PATH_AUTO, "tc": pk.PATH_TC, "mma": pk.PATH_MMA, "fma": pk.PATH_FMA}[args.prefill_path]
 
     def attend():
         pk.prefill_attention(d["q"], kc, vc, d["tables"], d["cu_q"], d["cu_k"], maxq, b.scale, window=window,
@@ -650,11 +650,12 @@ def run_prefill_bench(args):
         "attention_path": args.prefill_path,
         "roofline": {"kernel": ("prefill_attention_kernel (mma.sync m16n8k16, fp32 accumulation)"
                                 if args.prefill_path == "mma" else
+                                "prefill_fma_kernel (fp32 CUDA-core dot products)" if args.prefill_path == "fma" else
                                 "prefill_tc_kernel (tcgen05.mma kind::f16, TMA 128B-swizzled K/V, TMEM accumulators)"),
                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
                      "peak_source": "measured bf16 burst" if peaks.get("bf16_tflops") else "fallback",
-                     "traffic": None if args.prefill_path == "mma" else
+                     "traffic": None if args.prefill_path in ("mma", "fma") else
                      recorded_traffic(cfg.name, "prefill_traffic.txt", "prefill_tc")},
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -827,8 +828,8 @@ def main():
     ap.add_argument("--prefill", default=None,
                     choices=["qwen3_prefill", "grok1_prefill", "chunked_prefill"],
                     help="time a varlen prefill step (store + causal attention) instead (one JSON line)")
-    ap.add_argument("--prefill-path", default="auto", choices=["auto", "tc", "mma"],
-                    help="prefill attention kernel: tcgen05 (auto picks it where it runs) or mma.sync")
+    ap.add_argument("--prefill-path", default="auto", choices=["auto", "tc", "mma", "fma"],
+                    help="prefill attention kernel: tcgen05 (auto picks it where it runs), mma.sync or CUDA cores")
     ap.add_argument("--serve", default=None, choices=["qwen3_prefill", "grok1_prefill", "chunked_prefill"],
                     help="serving timeline: the batch's prefill, then --steps decode steps (TTFT / TPOT, one line)")
     args = ap.parse_args()

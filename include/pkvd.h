@@ -72,7 +72,7 @@ typedef enum { PKVD_F32 = 0, PKVD_F16 = 1, PKVD_BF16 = 2 } pkvd_dtype;
  * pkvd_prefill_attention_ex. */
 typedef enum {
   PKVD_PATH_AUTO = 0,   /* the library's choice for the shape              */
-  PKVD_PATH_FMA = 1,    /* fp32 CUDA-core dot products (decode only)       */
+  PKVD_PATH_FMA = 1,    /* fp32 CUDA-core dot products                     */
   PKVD_PATH_MMA = 2,    /* warp-level mma.sync m16n8k16 tensor-core path   */
   PKVD_PATH_TC = 3      /* tcgen05: TMA-fed operands, TMEM accumulators
                            (prefill only)                                  */
@@ -298,9 +298,10 @@ pkvd_status pkvd_kv_store_prefill(const void* k, const void* v, const int32_t* b
  *         aligned; rows t >= cu_seqlens_q[num_seqs] are not written.
  *         Tensor-core products with fp32 accumulation; the softmax weights
  *         are rounded to the cache dtype for the second product.
- * Requirements: cache dtype f16 or bf16 (PKVD_UNSUPPORTED_DTYPE for f32),
- *         head_dim 64 or 128, num_q_heads % num_kv_heads == 0, group size
- *         <= 128, num_seqs <= 65535, window >= 0.
+ * Requirements: head_dim 64 or 128, num_q_heads % num_kv_heads == 0,
+ *         num_seqs <= 65535, window >= 0; f16 / bf16 caches with group size
+ *         <= 128 run on the tensor cores, f32 caches (and 16-bit ones on
+ *         request) on the CUDA cores with group size <= 16.
  * Device errors: q_len > k_len, cu_seqlens_q[i+1] > total_q, k_len past the
  *         table or q_len > max_seqlen_q set PKVD_ERR_CONTEXT (that
  *         sequence's rows, or in the last case its earliest rows, are not
@@ -315,10 +316,11 @@ pkvd_status pkvd_prefill_attention(void* out, const void* q, const pkvd_cache* c
 
 /* Same as pkvd_prefill_attention with an explicit compute path:
  * PKVD_PATH_TC (tcgen05 MMAs on TMA-loaded 128-byte-swizzled tiles with TMEM
- * accumulators; needs block_size >= 8, 16-byte aligned q and out, and a cache
- * whose strides nest head < token < block), PKVD_PATH_MMA (mma.sync), or
- * PKVD_PATH_AUTO (TC when it can run the call, else MMA; what
- * pkvd_prefill_attention does).  PKVD_UNSUPPORTED_SHAPE if the path cannot
+ * accumulators; 16-bit caches, needs block_size >= 8, 16-byte aligned q and
+ * out, and a cache whose strides nest head < token < block), PKVD_PATH_MMA
+ * (mma.sync, 16-bit caches), PKVD_PATH_FMA (fp32 CUDA-core arithmetic, any
+ * cache dtype, group size <= 16), or PKVD_PATH_AUTO (TC when it can run the
+ * call, else MMA, else FMA; what pkvd_prefill_attention does).  PKVD_UNSUPPORTED_SHAPE if the path cannot
  * run the call.  Both paths compute the same function; on the TC path cache
  * rows of a 16-row-aligned group that meets a sequence's range may be
  * fetched, but rows outside [ws, p] never weigh in. */

@@ -153,8 +153,8 @@ pkvd_status pkvd_prefill_attention_ex(void* out, const void* q, const pkvd_cache
                                       const int32_t* cu_seqlens_k, int32_t num_seqs, int32_t total_q,
                                       int32_t max_seqlen_q, int32_t num_q_heads, float scale, int32_t window,
                                       void* stream, int32_t* err_flag, int32_t path) {
-  if (path != PKVD_PATH_AUTO && path != PKVD_PATH_MMA && path != PKVD_PATH_TC)
-    return path == PKVD_PATH_FMA ? PKVD_UNSUPPORTED_SHAPE : PKVD_INVALID_ARG;
+  if (path != PKVD_PATH_AUTO && path != PKVD_PATH_MMA && path != PKVD_PATH_TC && path != PKVD_PATH_FMA)
+    return PKVD_INVALID_ARG;
   if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || window < 0) return PKVD_INVALID_ARG;
   if (!std::isfinite(scale)) return PKVD_INVALID_ARG;
   const pkvd_status cs = check_cache(cache, false);
@@ -162,14 +162,17 @@ pkvd_status pkvd_prefill_attention_ex(void* out, const void* q, const pkvd_cache
   if (num_q_heads <= 0) return PKVD_INVALID_ARG;
   if (num_q_heads % cache->num_kv_heads) return PKVD_UNSUPPORTED_SHAPE;
   const int group = num_q_heads / cache->num_kv_heads;
-  if (!prefill_supported(cache->dtype, cache->head_dim, group)) {
+  const bool mma = prefill_supported(cache->dtype, cache->head_dim, group);
+  const bool fma = prefill_fma_supported(cache->dtype, cache->head_dim, group, cache->num_kv_heads);
+  if ((path == PKVD_PATH_MMA || path == PKVD_PATH_TC) && !mma)
     return cache->dtype == PKVD_F32 ? PKVD_UNSUPPORTED_DTYPE : PKVD_UNSUPPORTED_SHAPE;
-  }
+  if ((path == PKVD_PATH_FMA || path == PKVD_PATH_AUTO) && !fma && !mma) return PKVD_UNSUPPORTED_SHAPE;
+  if (path == PKVD_PATH_FMA && !fma) return PKVD_UNSUPPORTED_SHAPE;
   if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return PKVD_OK;
   if (!out || !q || !block_tables || !cu_seqlens_q || !cu_seqlens_k || max_blocks_per_seq <= 0)
     return PKVD_INVALID_ARG;
   if (!aligned16(q) || (reinterpret_cast<uintptr_t>(out) & 3u)) return PKVD_UNSUPPORTED_SHAPE;
-  const int tiles = (max_seqlen_q + prefill_tile_tokens(group) - 1) / prefill_tile_tokens(group);
+  const int tiles = mma ? (max_seqlen_q + prefill_tile_tokens(group) - 1) / prefill_tile_tokens(group) : 0;
   if (num_seqs > 65535 || tiles > 65535) return PKVD_UNSUPPORTED_SHAPE;
   PrefillArgs a;
   a.out = out;
@@ -186,11 +189,13 @@ pkvd_status pkvd_prefill_attention_ex(void* out, const void* q, const pkvd_cache
   a.scale = scale;
   a.window = window;
   a.err = err_flag;
-  const bool tc = prefill_tc_supported(a);
+  const bool tc = mma && prefill_tc_supported(a);
   if (path == PKVD_PATH_TC && !tc) return PKVD_UNSUPPORTED_SHAPE;
-  if (path == PKVD_PATH_TC || (path == PKVD_PATH_AUTO && tc))
-    return from_cuda(launch_prefill_tc(a, static_cast<cudaStream_t>(stream)));
-  return from_cuda(launch_prefill_attention(a, static_cast<cudaStream_t>(stream)));
+  if (path == PKVD_PATH_AUTO) path = tc ? PKVD_PATH_TC : mma ? PKVD_PATH_MMA : PKVD_PATH_FMA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (path == PKVD_PATH_TC) return from_cuda(launch_prefill_tc(a, st));
+  if (path == PKVD_PATH_MMA) return from_cuda(launch_prefill_attention(a, st));
+  return from_cuda(launch_prefill_fma(a, st));
 }
 
 pkvd_status pkvd_prefill_attention(void* out, const void* q, const pkvd_cache* cache, const int32_t* block_tables,

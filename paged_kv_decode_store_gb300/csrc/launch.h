@@ -80,6 +80,8 @@ struct PrefillArgs {
 };
 bool prefill_supported(int dtype, int head_dim, int group);
 bool prefill_tc_supported(const PrefillArgs& a);
+bool prefill_fma_supported(int dtype, int head_dim, int group, int num_kv_heads);
+cudaError_t launch_prefill_fma(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
 int prefill_tile_tokens(int group);
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t stream);

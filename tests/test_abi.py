@@ -115,7 +115,15 @@ def test_prefill_host_checks(L):
     def attn(cache, hq=48, q=1 << 22, out=1 << 21, seqs=4, total=100, maxq=64, scale=0.088, window=0):
         return L.pkvd_prefill_attention(out, q, ctypes.byref(cache), 1 << 23, 8, 1 << 24, 1 << 25, seqs, total,
                                         maxq, hq, ctypes.c_float(scale), window, None, None)
-    assert attn(_cache(dtype=0)) == 2                          # no fp32 prefill kernel
+    def attn_ex(cache, path, hq=48):
+        return L.pkvd_prefill_attention_ex(1 << 21, 1 << 22, ctypes.byref(cache), 1 << 23, 8, 1 << 24, 1 << 25, 4,
+                                           100, 64, hq, ctypes.c_float(0.088), 0, None, None, path)
+    # every call below is rejected on the host (the pointers are fake)
+    assert attn_ex(_cache(dtype=0), path=2) == 2                # no fp32 tensor-core prefill
+    assert attn_ex(_cache(dtype=0), path=3) == 2
+    assert attn_ex(_cache(dtype=0), path=0, hq=8 * 17) == 3    # fp32 goes to the CUDA-core path: group <= 16
+    assert attn_ex(_cache(), path=1, hq=8 * 17) == 3
+    assert attn_ex(_cache(), path=9) == 1
     assert attn(_cache(), hq=44) == 3                          # 44 % 8 != 0
     assert attn(_cache(num_kv_heads=1, block_stride=16 * 128, token_stride=128), hq=129) == 3   # group > 128
     assert attn(_cache(head_dim=96)) == 3

@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from workloads import prefill as wp
-from gpu_helpers import require_gpu, raw_numpy, from_raw, RTOL_16
+from gpu_helpers import require_gpu, raw_numpy, from_raw, RTOL_16, ATOL_F32
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -41,6 +41,13 @@ def small_batches():
         "bs128_bf16_d64": wp.PrefillConfig(name="bs128", index=11, num_seqs=3, num_q_heads=4, num_kv_heads=2,
                                            head_dim=64, block_size=128, dtype="bf16", q_kind="fixed",
                                            q_args=(129, 500, 2), hit_kind="fixed", hit_args=(1, 2, 0)),
+        # fp32 caches: the CUDA-core path only
+        "f32_d64": wp.PrefillConfig(name="f32a", index=12, num_seqs=3, num_q_heads=4, num_kv_heads=2, head_dim=64,
+                                    block_size=16, dtype="f32", q_kind="fixed", q_args=(17, 40, 1),
+                                    hit_kind="fixed", hit_args=(1, 0, 3)),
+        "f32_d128_g4": wp.PrefillConfig(name="f32b", index=13, num_seqs=2, num_q_heads=8, num_kv_heads=2,
+                                        head_dim=128, block_size=32, dtype="f32", q_kind="fixed", q_args=(70, 33),
+                                        hit_kind="fixed", hit_args=(2, 0), prefix_kind="shared"),
     }
 
 
@@ -82,13 +89,19 @@ def run_prefill(pk, b, window=0, max_seqlen_q=None, total_rows=None, path=None):
     return cache.cpu(), slots.cpu().numpy(), out.cpu(), int(err.item())
 
 
-def check_rows(out, ref, pairs):
+def check_rows(out, ref, pairs, f32=False):
+    """16-bit caches: relative error per (token, head) <= 2e-2; fp32: max abs
+    error <= 1e-4 (the decode attention's tolerances)."""
     worst = 0.0
     for t, h in pairs:
         o, r = out[t, h], ref[t, h]
         assert np.all(np.isfinite(o)), (t, h)
-        e = float(np.abs(o - r).max() / max(np.abs(r).max(), 1e-6))
-        assert e <= RTOL_16, (t, h, e)
+        if f32:
+            e = float(np.abs(o - r).max())
+            assert e <= ATOL_F32, (t, h, e)
+        else:
+            e = float(np.abs(o - r).max() / max(np.abs(r).max(), 1e-6))
+            assert e <= RTOL_16, (t, h, e)
         worst = max(worst, e)
     return worst
 
@@ -105,21 +118,25 @@ def test_prefill_store_bit_exact(name):
     np.testing.assert_array_equal(raw_numpy(cache[1]), v_ref)
 
 
-@pytest.mark.parametrize("path", ["tc", "mma"])
+@pytest.mark.parametrize("path", ["tc", "mma", "fma"])
 @pytest.mark.parametrize("window", [0, 1, 50, 200])
 @pytest.mark.parametrize("name", list(small_batches()))
 def test_prefill_attention_matches_oracle(name, window, path):
+    cfg = small_batches()[name]
+    if cfg.dtype == "f32" and path != "fma":
+        pytest.skip("the tensor-core paths take 16-bit caches")
     pk = require_gpu()
-    b = wp.make_prefill_batch(small_batches()[name])
+    b = wp.make_prefill_batch(cfg)
     k_ref, v_ref, _ = oracle_cache(b)
     dt = b.cache.dtype
     ref = oracle.prefill.prefill_attention(b.q.double().numpy(), to_f64(k_ref, dt), to_f64(v_ref, dt),
                                            b.block_tables, b.cu_seqlens_q, b.cu_seqlens_k, b.scale,
                                            window=window)
-    _, _, out, err = run_prefill(pk, b, window=window, path={"tc": pk.PATH_TC, "mma": pk.PATH_MMA}[path])
+    _, _, out, err = run_prefill(pk, b, window=window,
+                                 path={"tc": pk.PATH_TC, "mma": pk.PATH_MMA, "fma": pk.PATH_FMA}[path])
     assert err == 0
     T, Hq, _ = ref.shape
-    check_rows(out.double().numpy(), ref, [(t, h) for t in range(T) for h in range(Hq)])
+    check_rows(out.double().numpy(), ref, [(t, h) for t in range(T) for h in range(Hq)], f32=cfg.dtype == "f32")
 
 
 def test_rows_past_the_batch_are_untouched():

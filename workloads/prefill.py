@@ -31,7 +31,7 @@ from dataclasses import dataclass, replace
 import numpy as np
 import torch
 
-TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16}
+TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
 
 @dataclass(frozen=True)

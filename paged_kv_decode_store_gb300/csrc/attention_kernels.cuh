@@ -414,7 +414,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cta = blockIdx.x, grid = gridDim.x;
-  pdl_wait();                       // the cache rows stored by the previous kernel
+  // Everything up to the producer's first copy reads only inputs of this call
+  // (context lengths, block tables, q), never memory the previous kernel (the
+  // KV store) writes, so it runs before the dependency wait and overlaps that
+  // kernel; the producer waits before its first cache read.
 
   // ---- scan the chunk counts: total, this CTA's slice, and its first row
   // (every CTA computes the same scan; CTA 0 flags bad lengths)
@@ -503,6 +506,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) paged_decode_partition_kernel
     long long row_start = c0 - ch;          // flat index of the row's chunk 0
     bool first_seg = true;
     int tb_seq = -1, tb_base = 0, tb_val = -1;
+    if (nch > 0) {            // the first table window, fetched before the wait
+      const int lb = (tok_base + ch * kChunk) / p.block_size;
+      tb_seq = seq;
+      tb_base = lb;
+      tb_val = lb + lane < p.max_blocks ? p.tables[(int64_t)seq * p.max_blocks + lb + lane] : -1;
+    }
+    pdl_wait();               // the cache rows stored by the previous kernel
     int it = 0;
     for (; it < nit; ++it) {
       while (ch >= nch && seq + 1 < p.num_seqs) {

@@ -39,6 +39,14 @@
  *     The caller zeroes it and reads it back when it wants to know.
  *   - dtype codes: PKVD_F32, PKVD_F16, PKVD_BF16.  q, the new K/V, the cache
  *     and the attention output share one dtype.
+ *   - Kernels are launched as programmatic dependents of the previous work
+ *     on the stream: they may start while a preceding kernel that signalled
+ *     early completion (griddepcontrol.launch_dependents) still runs, and
+ *     then read their *inputs* (lengths, tables, q, cu_seqlens, sampling
+ *     parameters) before waiting for it; they wait before touching the cache
+ *     or any output.  Kernels of this library only signal early when they
+ *     do not write another call's inputs; a caller's own kernel that signals
+ *     early must not write the inputs of the call that follows it.
  */
 #ifndef PKVD_H
 #define PKVD_H

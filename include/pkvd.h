@@ -41,12 +41,12 @@
  *     and the attention output share one dtype.
  *   - Kernels are launched as programmatic dependents of the previous work
  *     on the stream: they may start while a preceding kernel that signalled
- *     early completion (griddepcontrol.launch_dependents) still runs, and
- *     then read their *inputs* (lengths, tables, q, cu_seqlens, sampling
- *     parameters) before waiting for it; they wait before touching the cache
- *     or any output.  Kernels of this library only signal early when they
- *     do not write another call's inputs; a caller's own kernel that signals
- *     early must not write the inputs of the call that follows it.
+ *     early completion (griddepcontrol.launch_dependents) still runs.  Before
+ *     waiting for it they read only inputs that no kernel of this library
+ *     writes (context lengths, block tables, q); everything else (the cache,
+ *     slot_mapping, outputs, workspaces) comes after the wait.  A caller's
+ *     own kernel that signals early must not write those inputs of the call
+ *     that follows it.
  */
 #ifndef PKVD_H
 #define PKVD_H

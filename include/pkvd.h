@@ -22,6 +22,12 @@
  *                  nanochat "04 · Engine" section 3 top-k; nano-vllm "run
  *                  model" Gumbel-max sampler).
  *
+ * Around it: the varlen prefill store and causal attention over cached
+ * prefixes (nano-vllm "prefix cache"), sliding-window decode attention
+ * (nanochat "推理基准 infer_bench.py"), the rest of Grok-1's sample_token
+ * (mask, token probability, top-8), and a host block manager with prefix
+ * sharing and copy-on-write.
+ *
  * Conventions for every entry point:
  *   - All tensor arguments are DEVICE pointers unless stated; sizes are
  *     element counts; strides are in elements.  `stream` is a cudaStream_t
@@ -96,8 +102,9 @@ typedef enum {
  * ("allocated kv cache") layer l is k_base = &kv_cache[0, l, 0, 0, 0, 0],
  * v_base = &kv_cache[1, l, 0, 0, 0, 0], block_stride = block_size*H*D,
  * token_stride = H*D, head_stride = D.
- * Requirements: head_dim in {64, 128}; block_size a power of two >= 16;
- * head_dim elements contiguous; base pointers and every stride times the
+ * Requirements: head_dim in {64, 128}; block_size a power of two (>= 16 for
+ * the decode attention, >= 8 for the tcgen05 prefill path); head_dim
+ * elements contiguous; base pointers and every stride times the
  * element size multiples of 16 bytes.
  */
 typedef struct {

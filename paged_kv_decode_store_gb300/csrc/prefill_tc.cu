@@ -139,6 +139,30 @@ __device__ __forceinline__ float tc_ex2(float x) {
   return y;
 }
 
+// Three-input maximum (one instruction on sm_100-family parts).
+__device__ __forceinline__ float tc_max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed pair arithmetic on two fp32 lanes (one instruction each).
+__device__ __forceinline__ void tc_fma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+  unsigned long long a, bb, cc, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(bb) : "f"(b));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(cc) : "f"(c));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(bb), "l"(cc));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
+}
+__device__ __forceinline__ void tc_add2(float& d0, float& d1, float a0, float a1) {
+  unsigned long long a, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(d0), "f"(d1));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(d), "l"(a));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
+}
+
 // ------------------------------------------------------------ tcgen05 PTX
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
@@ -243,6 +267,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
 }
 
 template <typename T, int D>
+// 10 warps: an SM sub-partition holds three of them, so at most 168 registers a thread
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
   using L = TcLayout<D>;
   constexpr int H = L::kHalves;
@@ -549,28 +574,42 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
           tc_fence_before();
           mbar_arrive(&bars[kSRead + g]);            // the next S may overwrite these columns
         }
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        // raw scores: the scale (> 0) is applied inside the exponent, so the
+        // row max is taken over the raw values and scaled once
+        if (!row_full) {
 #pragma unroll
-        for (int c = 0; c < kTcKeys; ++c) {
-          const float x = v[c] * p.scale_log2;
-          v[c] = (row_full || ((mw[c >> 5] >> (c & 31)) & 1u)) ? x : -INFINITY;
-          mx[c & 3] = fmaxf(mx[c & 3], v[c]);
+          for (int c = 0; c < kTcKeys; ++c)
+            v[c] = ((mw[c >> 5] >> (c & 31)) & 1u) ? v[c] : -INFINITY;
         }
-        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kTcKeys; c += 8) {
+          mx0 = tc_max3(mx0, v[c], v[c + 1]);
+          mx1 = tc_max3(mx1, v[c + 2], v[c + 3]);
+          mx2 = tc_max3(mx2, v[c + 4], v[c + 5]);
+          mx3 = tc_max3(mx3, v[c + 6], v[c + 7]);
+        }
+        const float mt = fmaxf(tc_max3(mx0, mx1, mx2), mx3) * p.scale_log2;
         const bool rebase = mt > m_ref + kRebase;
         const bool scale_o = rebase && m_ref != -INFINITY;
         const float alpha = scale_o ? tc_ex2(m_ref - mt) : 1.f;
         if (rebase) m_ref = mt;
         const float mu = m_ref == -INFINITY ? 0.f : m_ref;
         uint32_t pk[kTcKeys / 2];
-        float rs = 0.f;
+        float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
 #pragma unroll
-        for (int c = 0; c < kTcKeys; c += 2) {
-          const float e0 = tc_ex2(v[c] - mu), e1 = tc_ex2(v[c + 1] - mu);
-          rs += e0 + e1;
+        for (int c = 0; c < kTcKeys; c += 4) {
+          // 2^(scale * s - mu) for two keys per packed FMA; masked keys give 2^-inf = 0
+          float a0, a1, a2, a3;
+          tc_fma2(a0, a1, v[c], v[c + 1], p.scale_log2, -mu);
+          tc_fma2(a2, a3, v[c + 2], v[c + 3], p.scale_log2, -mu);
+          const float e0 = tc_ex2(a0), e1 = tc_ex2(a1), e2 = tc_ex2(a2), e3 = tc_ex2(a3);
+          if (c & 4) tc_add2(rs2, rs3, e0, e1), tc_add2(rs2, rs3, e2, e3);
+          else tc_add2(rs0, rs1, e0, e1), tc_add2(rs0, rs1, e2, e3);
           pk[c / 2] = Mma<T>::pack(e0, e1);
+          pk[c / 2 + 1] = Mma<T>::pack(e2, e3);
         }
-        l = l * alpha + rs;
+        l = l * alpha + ((rs0 + rs1) + (rs2 + rs3));
         if constexpr (kSepP) {
           // the P buffer and O are free once PV(j - 1) has finished
           if (j > 0) {

@@ -12,7 +12,7 @@
 // both Q tiles of the pair share each K/V tile the CTA loads.  Pairs are
 // counted from the end of each sequence.  While the batch's K/V fits in L2
 // the heaviest pairs of every sequence start first; otherwise CTAs of one
-// (sequence, KV head) run together so that its K/V tiles stay in L2.  Ten warps with fixed roles:
+// (sequence, KV head) run together so that its K/V tiles stay in L2.  Eleven warps with fixed roles:
 //   warps 0-3, 4-7  softmax of Q tile 0 and 1: thread r owns query row r =
 //              TMEM lane r.  Loads its Q row into shared memory, then per
 //              128-key tile reads its row of S from TMEM, masks (causal,
@@ -20,10 +20,11 @@
 //              more than 2^8, so O is rarely rescaled), writes P = 2^(S - max)
 //              as packed 16-bit pairs into TMEM, and at the end reads O from
 //              TMEM, divides by the row sum and stores it.
-//   warp 8     producer: TMA (cp.async.bulk.tensor, 128-byte swizzle) of the
-//              K and V rows of each tile, one box per (cache block segment,
-//              64-column half); zeroes V rows outside the pair's key range in
-//              the first and last tiles before releasing them.
+//   warps 8, 10  producers of K and of V: TMA (cp.async.bulk.tensor, 128-byte
+//              swizzle) of each tile's rows, one box per (cache block
+//              segment, 64-column half); the V warp zeroes rows outside the
+//              pair's key range in the first and last tiles before releasing
+//              them.
 //   warp 9     MMA: allocates 512 TMEM columns; one thread issues, whenever
 //              ready, S = Q K^T (M 128, N 128 keys, K = head_dim) and
 //              O += P V (M 128, N = head_dim, K 128 keys, P from TMEM) for
@@ -53,9 +54,9 @@ namespace {
 
 constexpr int kTcRows = 128;          // M: query rows per Q tile (two Q tiles per CTA)
 constexpr int kTcKeys = 128;          // keys per K/V tile
-constexpr int kTcThreads = 320;       // 2 x 4 softmax warps, producer, MMA
+constexpr int kTcThreads = 352;       // 2 x 4 softmax warps, K producer, MMA, V producer
 constexpr int kGroup = 128;           // softmax threads per Q tile (one per row)
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kProducerWarp = 8, kMmaWarp = 9, kVProducerWarp = 10;
 constexpr uint32_t kHalf = 128u * 128u;   // one 128-row x 64-column 16-bit half tile
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: S of Q tile g at [128 g, 128 g + 128) (P of that tile is written
@@ -267,7 +268,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
 }
 
 template <typename T, int D>
-// 10 warps: an SM sub-partition holds three of them, so at most 168 registers a thread
+// 11 warps: an SM sub-partition holds three of them, so at most 168 registers a thread
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
   using L = TcLayout<D>;
   constexpr int H = L::kHalves;
@@ -347,60 +348,55 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + L::kBar + kTmemSlot);
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    // Lane 0 polls for free stages and picks the next copy: K runs up to
-    // kKStages tiles ahead but at most one tile ahead of V while V can go.
-    // Lane s looks up and copies segment s of the tile.  A V tile with rows
-    // outside [lo, hi] (the first and last tiles) is waited for here and
-    // those rows zeroed before the tile is released (V ready), so rows
-    // outside every query's range never weigh in.
+  if (warp == kProducerWarp || warp == kVProducerWarp) {
+    // ------------------------------------------------------------ producers
+    // Warp 8 copies the K tiles, warp 10 the V tiles, each as fast as its
+    // ring of stages frees up (one warp issuing both was the bottleneck: a
+    // tile of 16-row segments takes 16 TMA issues per operand).  Lane 0 polls
+    // for the next free stage; lane s looks up (three tiles ahead) and copies
+    // segment s of the tile.  A V tile with rows outside [lo, hi] (the first
+    // and last tiles) is waited for here and those rows zeroed before the tile
+    // is released (V ready), so rows outside every query's range never weigh in.
+    const bool is_v = warp == kVProducerWarp;
+    const int stages = is_v ? kVStages : kKStages;
+    const int full0 = is_v ? kVFull : kKFull, empty0 = is_v ? kVEmpty : kKEmpty;
+    const uint32_t ring = base + (is_v ? L::kV : L::kK);
+    const CUtensorMap* map = is_v ? &p.tmap_v : &p.tmap_k;
     const uint32_t box = (uint32_t)p.seg_rows * 128u;
-    int kt = 0, vt = 0;
+    int t = 0;
     bool ok = true;
-    if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_k)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_v)) : "memory");
-    }
+    if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
     uint64_t t_start = globaltimer_ns();       // the last progress
     constexpr int kNone = INT_MIN;             // a segment that misses [lo, hi]: nothing to load
-    auto fetch = [&](int t) -> int {
-      if (t >= n || lane >= nseg) return kNone;
-      const int ks = (kt_first + t) * kTcKeys + lane * p.seg_rows;
+    auto fetch = [&](int tt) -> int {
+      if (tt >= n || lane >= nseg) return kNone;
+      const int ks = (kt_first + tt) * kTcKeys + lane * p.seg_rows;
       if (ks > hi || ks + p.seg_rows - 1 < lo) return kNone;
       return __ldg(table + ks / p.block_size);
     };
-    int k_cur = fetch(0), k_next = fetch(1), v_cur = k_cur, v_next = k_next;
-    while (kt < n || vt < n) {
-      int what = 0;   // 1: issue K(kt), 2: issue V(vt), -1: gave up
+    // each lane's block id of tiles t .. t + 3
+    int b0 = fetch(0), b1 = fetch(1), b2 = fetch(2), b3 = fetch(3);
+    while (t < n) {
+      int go = 0;   // 1: issue tile t, -1: gave up
       if (lane == 0) {
-        const bool can_k =
-            kt < n && (kt < kKStages || mbar_test(&bars[kKEmpty + kt % kKStages], ((kt / kKStages) - 1) & 1));
-        const bool can_v =
-            vt < kt && (vt < kVStages || mbar_test(&bars[kVEmpty + vt % kVStages], ((vt / kVStages) - 1) & 1));
-        if (can_v && (vt + 1 < kt || !can_k)) what = 2;
-        else if (can_k) what = 1;
-        else if (globaltimer_ns() - t_start > 2000000000ull) what = -1;
+        if (t < stages || mbar_test(&bars[empty0 + t % stages], ((t / stages) - 1) & 1)) go = 1;
+        else if (globaltimer_ns() - t_start > 2000000000ull) go = -1;
       }
-      what = __shfl_sync(FULL_MASK, what, 0);
-      if (what < 0) {
+      go = __shfl_sync(FULL_MASK, go, 0);
+      if (go < 0) {
         ok = false;
         break;
       }
-      if (what == 0) continue;
-      const int raw = what == 1 ? k_cur : v_cur;
-      const bool good = raw != kNone && raw >= 0 && raw < p.num_blocks;
+      if (go == 0) continue;
+      const bool good = b0 != kNone && b0 >= 0 && b0 < p.num_blocks;
       const uint32_t loaded = __ballot_sync(FULL_MASK, good);
-      if (what == 1 && __ballot_sync(FULL_MASK, raw != kNone && !good) && lane == 0)
-        flag_error(p.err, PKVD_ERR_BLOCK_ID);
-      const int j = what == 1 ? kt : vt;
-      const int stg = what == 1 ? kt % kKStages : vt % kVStages;
-      uint64_t* bar = &bars[(what == 1 ? kKFull : kVFull) + stg];
-      const uint32_t dst0 = base + (what == 1 ? L::kK : L::kV) + stg * H * kHalf;
-      const CUtensorMap* map = what == 1 ? &p.tmap_k : &p.tmap_v;
-      const int kbase = (kt_first + j) * kTcKeys;
+      if (!is_v && __ballot_sync(FULL_MASK, b0 != kNone && !good) && lane == 0) flag_error(p.err, PKVD_ERR_BLOCK_ID);
+      const int stg = t % stages;
+      uint64_t* bar = &bars[full0 + stg];
+      const uint32_t dst0 = ring + stg * H * kHalf;
+      const int kbase = (kt_first + t) * kTcKeys;
       // a segment with a bad block id reads as zeros (like the mma.sync path)
-      if (raw != kNone && !good) {
+      if (b0 != kNone && !good) {
         for (int h = 0; h < H; ++h)
           for (uint32_t o = 0; o < box; o += 16) st_shared_v4(dst0 + h * kHalf + lane * box + o, make_uint4(0u, 0u, 0u, 0u));
         fence_proxy_async_smem();
@@ -412,14 +408,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       if ((loaded >> lane) & 1u) {
         const int ks = kbase + lane * p.seg_rows;
 #pragma unroll
-        for (int h = 0; h < H; ++h) tma_load4(dst0 + h * kHalf + lane * box, map, h * 64, hk, ks % p.block_size, raw, bar);
+        for (int h = 0; h < H; ++h) tma_load4(dst0 + h * kHalf + lane * box, map, h * 64, hk, ks % p.block_size, b0, bar);
       }
-      if (what == 2) {
+      if (is_v) {
         // V ready: at once, or, for an edge tile, once its rows outside [lo, hi] are zero
         if (kbase < lo || kbase + kTcKeys - 1 > hi) {
-          if (lane == 0) ok = mbar_wait_bounded(bar, (vt / kVStages) & 1);
+          if (lane == 0) ok = mbar_wait_bounded(bar, (t / stages) & 1);
           if (!(ok = __shfl_sync(FULL_MASK, ok, 0))) {
-            ++vt;
+            ++t;
             break;
           }
           for (int rr = lane; rr < kTcKeys; rr += 32) {
@@ -433,22 +429,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         }
         if (lane == 0) mbar_arrive(&bars[kVReady + stg]);
       }
-      if (what == 1) {
-        ++kt;
-        k_cur = k_next;
-        k_next = fetch(kt + 1);
-      } else {
-        ++vt;
-        v_cur = v_next;
-        v_next = fetch(vt + 1);
-      }
+      ++t;
+      b0 = b1;
+      b1 = b2;
+      b2 = b3;
+      b3 = fetch(t + 3);
       if (lane == 0) t_start = globaltimer_ns();
     }
     if (!ok && lane == 0) {
-      // gave up: let the copies still in flight land before the CTA leaves
+      // gave up: let this warp's copies still in flight land before the CTA leaves
       flag_error(p.err, PKVD_ERR_TIMEOUT);
-      for (int t = max(0, kt - kKStages); t < kt; ++t) mbar_wait_bounded(&bars[kKFull + t % kKStages], (t / kKStages) & 1);
-      for (int t = max(0, vt - kVStages); t < vt; ++t) mbar_wait_bounded(&bars[kVFull + t % kVStages], (t / kVStages) & 1);
+      for (int u = max(0, t - stages); u < t; ++u) mbar_wait_bounded(&bars[full0 + u % stages], (u / stages) & 1);
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA

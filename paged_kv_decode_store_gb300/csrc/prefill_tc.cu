@@ -12,7 +12,7 @@
 // both Q tiles of the pair share each K/V tile the CTA loads.  Pairs are
 // counted from the end of each sequence.  While the batch's K/V fits in L2
 // the heaviest pairs of every sequence start first; otherwise CTAs of one
-// (sequence, KV head) run together so that its K/V tiles stay in L2.  Eleven warps with fixed roles:
+// (sequence, KV head) run together so that its K/V tiles stay in L2.  Twelve warps with fixed roles:
 //   warps 0-3, 4-7  softmax of Q tile 0 and 1: thread r owns query row r =
 //              TMEM lane r.  Loads its Q row into shared memory, then per
 //              128-key tile reads its row of S from TMEM, masks (causal,
@@ -25,11 +25,11 @@
 //              segment, 64-column half); the V warp zeroes rows outside the
 //              pair's key range in the first and last tiles before releasing
 //              them.
-//   warp 9     MMA: allocates 512 TMEM columns; one thread issues, whenever
-//              ready, S = Q K^T (M 128, N 128 keys, K = head_dim) and
-//              O += P V (M 128, N = head_dim, K 128 keys, P from TMEM) for
-//              either Q tile with tcgen05.mma kind::f16 (fp32 accumulate), and
-//              signals mbarriers with tcgen05.commit.
+//   warps 9, 11  MMA for Q tile 0 and 1 (warp 9 also allocates the 512 TMEM
+//              columns): one thread each issues S = Q K^T (M 128, N 128 keys,
+//              K = head_dim) and O += P V (M 128, N = head_dim, K 128 keys, P
+//              from TMEM) for its Q tile with tcgen05.mma kind::f16 (fp32
+//              accumulate), and signals mbarriers with tcgen05.commit.
 // Keys outside a row's range are masked in S; segments whose block id is bad
 // read as zeros.
 //
@@ -54,9 +54,9 @@ namespace {
 
 constexpr int kTcRows = 128;          // M: query rows per Q tile (two Q tiles per CTA)
 constexpr int kTcKeys = 128;          // keys per K/V tile
-constexpr int kTcThreads = 352;       // 2 x 4 softmax warps, K producer, MMA, V producer
+constexpr int kTcThreads = 384;       // 2 x 4 softmax warps, K producer, MMA 0, V producer, MMA 1
 constexpr int kGroup = 128;           // softmax threads per Q tile (one per row)
-constexpr int kProducerWarp = 8, kMmaWarp = 9, kVProducerWarp = 10;
+constexpr int kProducerWarp = 8, kMmaWarp = 9, kVProducerWarp = 10, kMmaWarp1 = 11;
 constexpr uint32_t kHalf = 128u * 128u;   // one 128-row x 64-column 16-bit half tile
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: S of Q tile g at [128 g, 128 g + 128) (P of that tile is written
@@ -77,7 +77,7 @@ struct TcLayout {
   static constexpr uint32_t kBar = kV + kVStages * kHalves * kHalf;
   // + alignment slack; at least 120 KB so that one CTA (which holds all 512
   // TMEM columns) is resident per SM
-  static constexpr uint32_t kBytes = kBar + 256 + 1024 > 122880u ? kBar + 256 + 1024 : 122880u;
+  static constexpr uint32_t kBytes = kBar + 512 + 1024 > 122880u ? kBar + 512 + 1024 : 122880u;
 };
 
 // mbarrier slots (8 bytes each) after kBar.  Per-Q-tile barriers take + g.
@@ -85,7 +85,7 @@ struct TcLayout {
 // one, so no waiter ever sees a barrier two phases ahead.
 enum : int {
   kKFull = 0, kKEmpty = 4, kVFull = 8, kVReady = 12, kVEmpty = 16, kQFull = 20, kSFull = 22, kPFull = 24,
-  kPVDone = 26, kSRead = 28, kDrain = 30, kNumBars = 31
+  kPVDone = 26, kSRead = 28, kDrain = 30, kNumBars = 32
 };
 // With head_dim 64 TMEM also holds a separate P buffer per Q tile at
 // [384 + 64 g, 448 + 64 g): the next S may then be computed as soon as the
@@ -116,6 +116,18 @@ struct TcParams {
   int window;
   int32_t* err;
 };
+
+// Spin (test_wait) until the phase with this parity has completed; false
+// after 2 s without it (the caller flags PKVD_ERR_TIMEOUT).
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity);
+__device__ __forceinline__ bool mbar_poll_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t spin = 0;; ++spin) {
+    if (mbar_test(bar, parity)) return true;
+    if ((spin & 255u) == 255u && globaltimer_ns() - t0 > 2000000000ull) return false;
+  }
+}
 
 // Non-blocking: has the phase with this parity completed?
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
@@ -268,7 +280,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
 }
 
 template <typename T, int D>
-// 11 warps: an SM sub-partition holds three of them, so at most 168 registers a thread
+// 12 warps: an SM sub-partition holds three of them, so at most 168 registers a thread
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
   using L = TcLayout<D>;
   constexpr int H = L::kHalves;
@@ -339,7 +351,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i)
       mbar_init(&bars[i], (i == kQFull || i == kQFull + 1 || i == kPFull || i == kPFull + 1 || i == kSRead ||
-                           i == kSRead + 1) ? (uint32_t)kGroup : 1u);
+                           i == kSRead + 1) ? (uint32_t)kGroup
+                          : kSepP && ((i >= kKEmpty && i < kKEmpty + 4) || (i >= kVEmpty && i < kVEmpty + 4)) ? 2u
+                                                                                                              : 1u);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(base + L::kBar + kTmemSlot, kTmemCols);
@@ -441,73 +455,140 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       flag_error(p.err, PKVD_ERR_TIMEOUT);
       for (int u = max(0, t - stages); u < t; ++u) mbar_wait_bounded(&bars[full0 + u % stages], (u / stages) & 1);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp || warp == kMmaWarp1) {
     // ---------------------------------------------------------------- MMA
-    // One thread issues whatever is ready, for either Q tile g: S_g(j) once
-    // K has landed, Q_g is loaded and PV_g(j - 1) has finished (P_g(j - 1)
-    // lives in the S_g columns), or PV_g(j) once P_g(j) and V are ready.
-    // A K (V) stage is released by the last Q tile that uses it.
-    if (lane == 0) {
-      constexpr uint32_t fmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
-      constexpr uint32_t id_s = tc_idesc(fmt, kTcKeys, 0), id_pv = tc_idesc(fmt, D, 1);
-      int js[2] = {0, 0}, jp[2] = {0, 0};
-      bool ok = true;
-      uint64_t t_start = globaltimer_ns();        // the last progress
-      auto uses = [&](int g, int t) { return t >= gf[g] && t < gf[g] + gn[g]; };
-      while (ok && (jp[0] < gn[0] || jp[1] < gn[1])) {
-        bool progressed = false;
+    // head_dim 64: one issuing thread per Q tile (warp 9: tile 0, warp 11:
+    // tile 1), so a thread that stalls while the tensor pipe takes one tile's
+    // products never holds up the other's.  Tile g's sequence: S_g(j) once
+    // K(j) has landed (and Q_g, for j = 0) and the softmax has read
+    // S_g(j - 1) (P_g has its own columns), so S_g(j) is issued before
+    // PV_g(j - 1); PV_g(j) once P_g(j) and V(j) are ready.  A K or V stage is
+    // released when both Q tiles are done with it: its empty barrier counts
+    // two arrivals, and a tile that only one Q tile uses gets both from that
+    // tile's commits.
+    if constexpr (kSepP) {
+      const int g = warp == kMmaWarp ? 0 : 1, o = 1 - g;
+      if (lane == 0 && gn[g] > 0) {
+        constexpr uint32_t fmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+        constexpr uint32_t id_s = tc_idesc(fmt, kTcKeys, 0), id_pv = tc_idesc(fmt, D, 1);
+        bool ok = true;
+        auto wait = [&](int bar, uint32_t parity) {
+          if (ok) ok = mbar_poll_bounded(&bars[bar], parity);
+        };
+        auto release = [&](int empty, int t) {
+          tc_commit(&bars[empty]);
+          if (!(t >= gf[o] && t < gf[o] + gn[o])) tc_commit(&bars[empty]);   // the other tile's share
+        };
+        auto issue_s = [&](int j) {
+          const int t = gf[g] + j;
+          wait(kKFull + t % kKStages, (t / kKStages) & 1);
+          if (!ok) return;
+          tc_fence_after();
+          const uint32_t qb = base + L::kQ + g * H * kHalf;
+          const uint32_t kb = base + L::kK + (t % kKStages) * H * kHalf;
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          if (js[g] < gn[g]) {
-            const int t = gf[g] + js[g];
-            const bool ready = (js[g] == 0 ? mbar_test(&bars[kQFull + g], 0)
-                                           : kSepP ? mbar_test(&bars[kSRead + g], (js[g] - 1) & 1)
-                                                   : mbar_test(&bars[kPVDone + g], (js[g] - 1) & 1)) &&
-                               mbar_test(&bars[kKFull + t % kKStages], (t / kKStages) & 1);
-            if (ready) {
-              tc_fence_after();
-              const uint32_t qb = base + L::kQ + g * H * kHalf;
-              const uint32_t kb = base + L::kK + (t % kKStages) * H * kHalf;
-#pragma unroll
-              for (int k = 0; k < D / 16; ++k) {
-                const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
-                tc_mma(tmem + kColS + g * kTcKeys, smem_desc(qb + off, 16, 1024), smem_desc(kb + off, 16, 1024),
-                       id_s, k > 0);
-              }
-              tc_commit(&bars[kSFull + g]);
-              const int o = 1 - g;
-              if (!uses(o, t) || js[o] > t - gf[o]) tc_commit(&bars[kKEmpty + t % kKStages]);
-              ++js[g];
-              progressed = true;
-            }
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
+            tc_mma(tmem + kColS + g * kTcKeys, smem_desc(qb + off, 16, 1024), smem_desc(kb + off, 16, 1024), id_s, k > 0);
           }
-          if (jp[g] < js[g]) {
-            const int t = gf[g] + jp[g];
-            const bool ready = mbar_test(&bars[kPFull + g], jp[g] & 1) &&
-                               mbar_test(&bars[kVFull + t % kVStages], (t / kVStages) & 1) &&
-                               mbar_test(&bars[kVReady + t % kVStages], (t / kVStages) & 1);
-            if (ready) {
-              tc_fence_after();
-              const uint32_t vb = base + L::kV + (t % kVStages) * H * kHalf;
+          tc_commit(&bars[kSFull + g]);
+          release(kKEmpty + t % kKStages, t);
+        };
+        auto issue_pv = [&](int j) {
+          const int t = gf[g] + j;
+          wait(kPFull + g, j & 1);
+          wait(kVFull + t % kVStages, (t / kVStages) & 1);
+          wait(kVReady + t % kVStages, (t / kVStages) & 1);
+          if (!ok) return;
+          tc_fence_after();
+          const uint32_t vb = base + L::kV + (t % kVStages) * H * kHalf;
 #pragma unroll
-              for (int k = 0; k < kTcKeys / 16; ++k)      // 16 keys = 8 packed P columns per step
-                tc_mma_tmem_a(tmem + kColO + g * D, tmem + (kSepP ? kColP64 + g * 64 : kColS + g * kTcKeys) + k * 8,
-                              smem_desc(vb + k * 2048, kHalf, 1024), id_pv, (jp[g] > 0 || k > 0) ? 1u : 0u);
-              tc_commit(&bars[kPVDone + g]);
-              const int o = 1 - g;
-              if (!uses(o, t) || jp[o] > t - gf[o]) tc_commit(&bars[kVEmpty + t % kVStages]);
-              ++jp[g];
-              progressed = true;
-            }
+          for (int k = 0; k < kTcKeys / 16; ++k)      // 16 keys = 8 packed P columns per step
+            tc_mma_tmem_a(tmem + kColO + g * D, tmem + kColP64 + g * 64 + k * 8, smem_desc(vb + k * 2048, kHalf, 1024),
+                          id_pv, (j > 0 || k > 0) ? 1u : 0u);
+          tc_commit(&bars[kPVDone + g]);
+          release(kVEmpty + t % kVStages, t);
+        };
+        wait(kQFull + g, 0);
+        issue_s(0);
+        for (int j = 0; j < gn[g] && ok; ++j) {
+          if (j + 1 < gn[g]) {
+            wait(kSRead + g, j & 1);
+            issue_s(j + 1);
           }
+          issue_pv(j);
         }
-        if (progressed) t_start = globaltimer_ns();
-        else if (globaltimer_ns() - t_start > 2000000000ull) ok = false;
+        if (!ok) {
+          flag_error(p.err, PKVD_ERR_TIMEOUT);
+          tc_commit(&bars[kDrain + g]);      // wait for the tensor-core work already issued
+          mbar_wait_bounded(&bars[kDrain + g], 0);
+        }
       }
-      if (!ok) {
-        flag_error(p.err, PKVD_ERR_TIMEOUT);
-        tc_commit(&bars[kDrain]);          // wait for the tensor-core work already issued
-        mbar_wait_bounded(&bars[kDrain], 0);
+    } else if (warp == kMmaWarp) {
+      // head_dim 128: one thread issues whatever is ready for either Q tile
+      // (S_g(j) needs PV_g(j - 1) finished, so a second issuer only
+      // interleaves the two tiles' products and delays both)
+      if (lane == 0) {
+        constexpr uint32_t fmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+        constexpr uint32_t id_s = tc_idesc(fmt, kTcKeys, 0), id_pv = tc_idesc(fmt, D, 1);
+        int js[2] = {0, 0}, jp[2] = {0, 0};
+        bool ok = true;
+        uint64_t t_start = globaltimer_ns();        // the last progress
+        auto uses = [&](int g, int t) { return t >= gf[g] && t < gf[g] + gn[g]; };
+        while (ok && (jp[0] < gn[0] || jp[1] < gn[1])) {
+          bool progressed = false;
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            if (js[g] < gn[g]) {
+              const int t = gf[g] + js[g];
+              const bool ready = (js[g] == 0 ? mbar_test(&bars[kQFull + g], 0)
+                                             : mbar_test(&bars[kPVDone + g], (js[g] - 1) & 1)) &&
+                                 mbar_test(&bars[kKFull + t % kKStages], (t / kKStages) & 1);
+              if (ready) {
+                tc_fence_after();
+                const uint32_t qb = base + L::kQ + g * H * kHalf;
+                const uint32_t kb = base + L::kK + (t % kKStages) * H * kHalf;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                  const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
+                  tc_mma(tmem + kColS + g * kTcKeys, smem_desc(qb + off, 16, 1024), smem_desc(kb + off, 16, 1024),
+                         id_s, k > 0);
+                }
+                tc_commit(&bars[kSFull + g]);
+                const int o = 1 - g;
+                if (!uses(o, t) || js[o] > t - gf[o]) tc_commit(&bars[kKEmpty + t % kKStages]);
+                ++js[g];
+                progressed = true;
+              }
+            }
+            if (jp[g] < js[g]) {
+              const int t = gf[g] + jp[g];
+              const bool ready = mbar_test(&bars[kPFull + g], jp[g] & 1) &&
+                                 mbar_test(&bars[kVFull + t % kVStages], (t / kVStages) & 1) &&
+                                 mbar_test(&bars[kVReady + t % kVStages], (t / kVStages) & 1);
+              if (ready) {
+                tc_fence_after();
+                const uint32_t vb = base + L::kV + (t % kVStages) * H * kHalf;
+#pragma unroll
+                for (int k = 0; k < kTcKeys / 16; ++k)      // 16 keys = 8 packed P columns per step
+                  tc_mma_tmem_a(tmem + kColO + g * D, tmem + kColS + g * kTcKeys + k * 8,
+                                smem_desc(vb + k * 2048, kHalf, 1024), id_pv, (jp[g] > 0 || k > 0) ? 1u : 0u);
+                tc_commit(&bars[kPVDone + g]);
+                const int o = 1 - g;
+                if (!uses(o, t) || jp[o] > t - gf[o]) tc_commit(&bars[kVEmpty + t % kVStages]);
+                ++jp[g];
+                progressed = true;
+              }
+            }
+          }
+          if (progressed) t_start = globaltimer_ns();
+          else if (globaltimer_ns() - t_start > 2000000000ull) ok = false;
+        }
+        if (!ok) {
+          flag_error(p.err, PKVD_ERR_TIMEOUT);
+          tc_commit(&bars[kDrain]);          // wait for the tensor-core work already issued
+          mbar_wait_bounded(&bars[kDrain], 0);
+        }
       }
     }
   } else {

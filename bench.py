@@ -15,7 +15,8 @@ Reported (one JSON line on rank 0):
   e2e          the same metric through the public API with host buffers:
                pinned host -> device copy of the step's inputs, the step, and
                device -> host copy of its outputs, all inside the timing
-  cpu_baseline the float64 oracle on a bounded sample, on the host cores
+  cpu_baseline the float64 oracle on a bounded sample, on every host core
+               (single-threaded processes), with the one-thread figure beside it
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config qwen3]
     python bench.py --impl reference ...   (the oracle as the reference arm)
@@ -273,65 +274,121 @@ sys.path.insert(0, sys.argv[1])
 import numpy as np
 import oracle
 d = np.load(sys.argv[2])
+# the per-row inputs, read once (each access of an npz member reads it again)
+q, knew, vnew, logits, ctx_all = d["q"], d["knew"], d["vnew"], d["logits"], d["ctx"]
+temp, topk, topp, seeds = d["temp"], d["topk"], d["topp"], d["seeds"]
+bs, scale = int(d["bs"]), float(d["scale"])
 budget = float(sys.argv[3])
-rows = int(d["q"].shape[0])
-t0 = time.perf_counter()
-done = 0
-for i in range(rows):
-    kc, vc = d["k%d" % i], d["v%d" % i]
-    tab = d["t%d" % i][None, :]
-    ctx = d["ctx"][i:i + 1]
-    slots = oracle.paging.decode_slot_mapping(tab, ctx, int(d["bs"]))
-    oracle.store.kv_store(d["knew"][i:i + 1], d["vnew"][i:i + 1], slots, kc, vc)
-    oracle.attention.decode_attention(d["q"][i:i + 1], kc, vc, tab, ctx, float(d["scale"]))
-    oracle.sampler.sample_row(d["logits"][i], float(d["temp"][i]), int(d["topk"][i]), float(d["topp"][i]),
-                              int(d["seeds"][i]), 0)
-    done += 1
-    if time.perf_counter() - t0 > budget:
+offset, stride, cycle = int(sys.argv[4]), int(sys.argv[5]), int(sys.argv[6])
+mine = list(range(offset, int(q.shape[0]), stride))
+counts, held = {}, {}
+elapsed = 0.0      # oracle time only: reading a row's arrays from the file is not timed
+k = 0
+while mine and (k < len(mine) or cycle):
+    i = mine[k % len(mine)]
+    k += 1
+    if i in held:
+        kc, vc, tab = held[i]
+    else:
+        kc, vc, tab = d["k%d" % i], d["v%d" % i], d["t%d" % i][None, :]
+        if cycle:
+            held[i] = (kc, vc, tab)
+    ctx = ctx_all[i:i + 1]
+    t0 = time.perf_counter()
+    slots = oracle.paging.decode_slot_mapping(tab, ctx, bs)
+    oracle.store.kv_store(knew[i:i + 1], vnew[i:i + 1], slots, kc, vc)
+    oracle.attention.decode_attention(q[i:i + 1], kc, vc, tab, ctx, scale)
+    oracle.sampler.sample_row(logits[i], float(temp[i]), int(topk[i]), float(topp[i]), int(seeds[i]), 0)
+    elapsed += time.perf_counter() - t0
+    counts[i] = counts.get(i, 0) + 1
+    if elapsed > budget:
         break
-print(json.dumps({"rows": done, "seconds": time.perf_counter() - t0}))
+print(json.dumps({"counts": counts, "seconds": elapsed}))
 """
 
 
-def oracle_sample(cfg, w, budget_s=15.0, max_rows=None):
-    """Run the float64 oracle on whole rows of the workload in a single-threaded
-    subprocess until ~budget_s; return (rows done, seconds, bytes of those rows)."""
-    lay = w.layout
-    B = lay.num_seqs if max_rows is None else min(max_rows, lay.num_seqs)
-    order = np.argsort(lay.context_lens[:B])[::-1]
-    order = np.concatenate([order[len(order) // 2:], order[:len(order) // 2]])  # mid-length rows first
-    arrays = {"bs": np.array(cfg.block_size), "scale": np.array(w.scale)}
-    sel = order[:B]
-    arrays["q"] = w.q[torch.from_numpy(sel.copy()).to(w.q.device)].double().cpu().numpy()
-    arrays["knew"] = w.k_new[torch.from_numpy(sel.copy()).to(w.q.device)].double().cpu().numpy()
-    arrays["vnew"] = w.v_new[torch.from_numpy(sel.copy()).to(w.q.device)].double().cpu().numpy()
-    arrays["logits"] = w.logits[torch.from_numpy(sel.copy()).to(w.q.device)].double().cpu().numpy()
-    arrays["ctx"] = lay.context_lens[sel]
-    arrays["temp"], arrays["topk"], arrays["topp"] = w.temperature[sel], w.top_k[sel], w.top_p[sel]
-    arrays["seeds"] = w.seeds[sel]
-    bs = cfg.block_size
-    for j, i in enumerate(sel):
-        n = -(-int(lay.context_lens[i]) // bs)
-        idx = torch.from_numpy(lay.block_tables[i, :n].astype(np.int64)).to(w.cache.device)
-        arrays["k%d" % j] = w.cache[0, lay.layer].index_select(0, idx).double().cpu().numpy()
-        arrays["v%d" % j] = w.cache[1, lay.layer].index_select(0, idx).double().cpu().numpy()
-        arrays["t%d" % j] = np.arange(n, dtype=np.int64)
-    fd, path = tempfile.mkstemp(suffix=".npz")
-    os.close(fd)
-    np.savez(path, **arrays)
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, "-c", ORACLE_SCRIPT, ROOT, path, str(budget_s)], capture_output=True,
-                       text=True, env=env)
-    os.unlink(path)
-    if r.returncode:
-        raise RuntimeError(r.stderr[-2000:])
-    res = json.loads(r.stdout.strip().splitlines()[-1])
-    done = res["rows"]
-    rows = sel[:done]
-    sub = workloads.Layout(lay.context_lens[rows], lay.block_tables[rows], lay.num_blocks, lay.layer,
-                           lay.max_context_len)
-    nbytes = algorithmic_bytes(cfg, sub)["step"]
-    return done, res["seconds"], nbytes
+class OracleSample:
+    """Whole rows of a decode workload (mid-length rows first) written once to
+    a temporary file for the float64 oracle, which runs in single-threaded
+    subprocesses (OMP/BLAS threads 1)."""
+
+    def __init__(self, cfg, w, max_rows=None):
+        self.cfg, self.lay = cfg, w.layout
+        lay = self.lay
+        B = lay.num_seqs if max_rows is None else min(max_rows, lay.num_seqs)
+        order = np.argsort(lay.context_lens[:B])[::-1]
+        order = np.concatenate([order[len(order) // 2:], order[:len(order) // 2]])  # mid-length rows first
+        sel = order[:B]
+        self.sel = sel
+        rows = torch.from_numpy(sel.copy()).to(w.q.device)
+        arrays = {"bs": np.array(cfg.block_size), "scale": np.array(w.scale)}
+        arrays["q"] = w.q[rows].double().cpu().numpy()
+        arrays["knew"] = w.k_new[rows].double().cpu().numpy()
+        arrays["vnew"] = w.v_new[rows].double().cpu().numpy()
+        arrays["logits"] = w.logits[rows].double().cpu().numpy()
+        arrays["ctx"] = lay.context_lens[sel]
+        arrays["temp"], arrays["topk"], arrays["topp"] = w.temperature[sel], w.top_k[sel], w.top_p[sel]
+        arrays["seeds"] = w.seeds[sel]
+        bs = cfg.block_size
+        for j, i in enumerate(sel):
+            n = -(-int(lay.context_lens[i]) // bs)
+            idx = torch.from_numpy(lay.block_tables[i, :n].astype(np.int64)).to(w.cache.device)
+            arrays["k%d" % j] = w.cache[0, lay.layer].index_select(0, idx).double().cpu().numpy()
+            arrays["v%d" % j] = w.cache[1, lay.layer].index_select(0, idx).double().cpu().numpy()
+            arrays["t%d" % j] = np.arange(n, dtype=np.int64)
+        fd, self.path = tempfile.mkstemp(suffix=".npz")
+        os.close(fd)
+        np.savez(self.path, **arrays)
+        self.row_bytes = {}
+
+    def bytes_of(self, i):
+        if i not in self.row_bytes:
+            lay = self.lay
+            one = workloads.Layout(lay.context_lens[i:i + 1], lay.block_tables[i:i + 1], lay.num_blocks, lay.layer,
+                                   lay.max_context_len)
+            self.row_bytes[i] = algorithmic_bytes(self.cfg, one)["step"]
+        return self.row_bytes[i]
+
+    def run(self, budget_s, procs=1):
+        """(rows done, seconds, bytes of those rows).  procs == 1: one pass over
+        the rows until ~budget_s of oracle time.  procs > 1: that many
+        processes, started together, each cycling through its share of the rows
+        for ~budget_s; seconds is the slowest one's oracle time."""
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        cycle = 1 if procs > 1 else 0
+        ps = [subprocess.Popen([sys.executable, "-c", ORACLE_SCRIPT, ROOT, self.path, str(budget_s), str(k),
+                                str(procs), str(cycle)], stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True,
+                               env=env)
+              for k in range(procs)]
+        outs = [p.communicate() for p in ps]
+        done = nbytes = 0
+        secs = 0.0
+        for p, (out, err) in zip(ps, outs):
+            if p.returncode:
+                raise RuntimeError(err[-2000:])
+            res = json.loads(out.strip().splitlines()[-1])
+            secs = max(secs, res["seconds"])
+            for j, c in res["counts"].items():
+                done += c
+                nbytes += c * self.bytes_of(int(self.sel[int(j)]))
+        return done, secs, nbytes
+
+    def close(self):
+        if os.path.exists(self.path):
+            os.unlink(self.path)
+
+
+def host_cores():
+    return max(1, os.cpu_count() or 1)
+
+
+def oracle_sample(cfg, w, budget_s=15.0, max_rows=None, procs=1):
+    """One bounded oracle run on rows of the workload: (rows, seconds, bytes)."""
+    smp = OracleSample(cfg, w, max_rows)
+    try:
+        return smp.run(budget_s, procs)
+    finally:
+        smp.close()
 
 
 # ----------------------------------------------------------------- main
@@ -365,25 +422,32 @@ def run_reference(args, cfg, ws, rank, local):
     if rank != 0:
         return
     w = workloads.make_workload(cfg, device=f"cuda:{local}" if torch.cuda.is_available() else "cpu")
-    per_step = []
-    for _ in range(args.warmup):
-        oracle_sample(cfg, w, budget_s=min(5.0, args.cpu_seconds), max_rows=8)
-    rows_tot = secs_tot = bytes_tot = 0
-    for _ in range(args.steps):
-        done, secs, nbytes = oracle_sample(cfg, w, budget_s=args.cpu_seconds)
-        per_step.append(secs)
-        rows_tot += done
-        secs_tot += secs
-        bytes_tot += nbytes
+    cores = host_cores()
+    # a step: every host core runs the oracle on its share of the rows for a
+    # bounded time, so the whole run stays within about a minute of oracle time
+    budget = max(1.0, min(args.cpu_seconds, 60.0 / max(1, args.steps)))
+    smp = OracleSample(cfg, w)
+    try:
+        for _ in range(args.warmup):
+            smp.run(min(1.0, budget), procs=cores)
+        rows_tot = secs_tot = bytes_tot = 0
+        for _ in range(args.steps):
+            done, secs, nbytes = smp.run(budget, procs=cores)
+            rows_tot += done
+            secs_tot += secs
+            bytes_tot += nbytes
+    finally:
+        smp.close()
     value = bytes_tot / secs_tot / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs_tot / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_block(cfg, w.layout),
             "tokens_per_s": rows_tot / secs_tot,
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": f"{rows_tot} whole rows (store + attention + sampler) over {args.steps} "
-                                       f"steps, ~{args.cpu_seconds:.0f} s each"},
+                                       f"steps of ~{budget:.0f} s, {cores} single-threaded processes "
+                                       f"(os.cpu_count() = {os.cpu_count()})"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -489,11 +553,11 @@ kc, vc = d["kc"], d["vc"]
 slots = oracle.prefill.prefill_slot_mapping(tab, cu_q, cu_k, bs)
 oracle.store.kv_store(d["knew"], d["vnew"], slots, kc, vc)
 pairs = [tuple(int(x) for x in p) for p in d["pairs"]]
+q, scale = d["q"], float(d["scale"])     # read once: each access of an npz member reads it again
 t0 = time.perf_counter()
 done = 0
 while done < len(pairs) and time.perf_counter() - t0 < budget:
-    oracle.prefill.prefill_attention(d["q"], kc, vc, tab, cu_q, cu_k, float(d["scale"]),
-                                     pairs=pairs[done:done + 16])
+    oracle.prefill.prefill_attention(q, kc, vc, tab, cu_q, cu_k, scale, pairs=pairs[done:done + 16])
     done = min(done + 16, len(pairs))
 print(json.dumps({"pairs": done, "seconds": time.perf_counter() - t0}))
 """
@@ -912,10 +976,21 @@ def main():
         "clocks": clocks, "device_err_flag": err,
     }
     if not args.no_cpu_baseline and ws == 1:
-        done, secs, cbytes = oracle_sample(cfg, w, budget_s=args.cpu_seconds)
-        line["cpu_baseline"] = {"value": cbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                "sample": f"{done} whole rows of this workload (store + attention + sampler), "
-                                          f"{secs:.1f} s, single thread"}
+        # the oracle on the host: one thread (one pass over the rows), then
+        # every core (single-threaded processes over shares of the rows)
+        cores = host_cores()
+        smp = OracleSample(cfg, w)
+        try:
+            done1, secs1, bytes1 = smp.run(args.cpu_seconds, procs=1)
+            done_n, secs_n, bytes_n = smp.run(max(1.0, min(args.cpu_seconds, 30.0 / cores)), procs=cores)
+        finally:
+            smp.close()
+        line["cpu_baseline"] = {
+            "value": bytes_n / secs_n / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done_n} whole rows of this workload (store + attention + sampler) in {secs_n:.1f} s on "
+                      f"{cores} single-threaded processes (os.cpu_count() = {os.cpu_count()})",
+            "single_thread": {"value": bytes1 / secs1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"{done1} whole rows, {secs1:.1f} s"}}
     print(json.dumps(line))
 
 

@@ -240,20 +240,25 @@ pkvd_status pkvd_paged_decode_attention_window(void* out, const void* q, const p
 
 /*
  * pkvd_paged_decode_attention_noalloc -- the same attention as
- * pkvd_paged_decode_attention (same arguments, results and errors), for
- * callers that cannot allocate device memory where they call it: code that
- * runs while a CUDA graph is captured, hosts embedded in a runtime that owns
- * every device allocation, plain C callers without an allocator.  The pages
- * describe no such entry point; it exists for those callers only.
+ * pkvd_paged_decode_attention (same arguments without the workspace pair,
+ * same results and errors), for callers that cannot allocate device memory
+ * where they call it: engines that give all free device memory to the paged
+ * KV cache at start-up (a later cudaMalloc fails), plugins inside a runtime
+ * that owns every device allocation, latency-critical loops where
+ * cudaMalloc/cudaFree would synchronise the device, plain C hosts without a
+ * device allocator.  The pages describe no such entry point; it exists for
+ * those callers only.
  *
  * Instead of a caller workspace it uses one 16 MiB scratch array built into
  * the library (held on every GPU that loads the library until the process
  * exits).  Shapes whose workspace (pkvd_decode_workspace_bytes) exceeds
  * 16 MiB are rejected with PKVD_WORKSPACE_TOO_SMALL before anything is
  * enqueued.  All calls on a GPU share the array: calls that overlap on the
- * GPU (unordered streams) race and give wrong results.  The first call on
- * each device looks up the array's device address (cudaGetSymbolAddress)
- * with that device current; make that first call before any stream capture.
+ * GPU (unordered streams) race and give wrong results.  Each call writes
+ * every part of the array it reads, so nothing needs clearing between
+ * calls.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.
  * Nothing is allocated.
  */
 pkvd_status pkvd_paged_decode_attention_noalloc(void* out, const void* q, const pkvd_cache* cache,

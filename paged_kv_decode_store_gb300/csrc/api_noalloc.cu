@@ -3,33 +3,40 @@
 // workspace.
 //
 // For callers that cannot allocate device memory at the point of the call:
-// code that runs while a CUDA graph is being captured (cudaMalloc is not
-// allowed there), host programs embedded in a runtime that owns all device
-// allocations (plugins, custom allocators, real-time loops where an
-// allocation would synchronise the device), and plain C callers without an
-// allocator of their own.  They pass inputs and outputs only.
+// engines that hand all free device memory to the paged KV cache at start-up
+// (a later cudaMalloc fails or evicts cache blocks), plugins inside a runtime
+// that owns every device allocation through its own pool, latency-critical
+// loops where cudaMalloc/cudaFree would synchronise the device, and plain C
+// hosts with no device allocator of their own.  They pass inputs and outputs
+// only.
 //
 // The scratch is one file-scope device array of kNoAllocScratchBytes.  Every
 // GPU that loads this library holds it until the process exits, and every
 // call on that GPU shares it: calls that overlap on the GPU (different
 // streams without ordering between them) race on it and give wrong results.
+// Nothing in it has to start at zero: each call writes every merge record it
+// later reads, so the previous call's contents do no harm.
 // In host code the array's name is only a host-side stand-in, so its device
 // address is looked up with cudaGetSymbolAddress, once per device, by the
-// first call on that device (with that device current).  That first call
-// must therefore come before any stream capture; later calls can be captured.
+// first call on that device (with that device current).  Make that first
+// call before any stream capture.
+#include <atomic>
+
 #include "launch.h"
 
 namespace pkvd {
 
-// 16 MiB: enough for every shape this library supports up to a few thousand
-// rows x 64 query heads (the largest benchmark shape needs about 10.3 MB).
+// 16 MiB.  The attention workspace grows with the partition grid (at most one
+// CTA per SM) and the query heads, not with the rows: on a 152-SM GPU, 64
+// query heads at head_dim 128 need 152 x 2 x 64 x 132 x 4 B = 10.3 MB, and
+// 128 such heads (20.5 MB) are rejected.
 constexpr size_t kNoAllocScratchBytes = 16u << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+std::atomic<void*> g_scratch_addr[kMaxDevices] = {};   // set once per device
 
 // Device address of the scratch on the current device (set-up on first use).
 cudaError_t scratch_address(void** out) {
@@ -37,13 +44,13 @@ cudaError_t scratch_address(void** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!g_scratch_addr[dev]) {
-    void* ptr = nullptr;
+  void* ptr = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (!ptr) {   // threads racing here all look up, and store, the same address
     e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = ptr;
+    g_scratch_addr[dev].store(ptr, std::memory_order_release);
   }
-  *out = g_scratch_addr[dev];
+  *out = ptr;
   return cudaSuccess;
 }
 }  // namespace

@@ -1,9 +1,10 @@
 """The allocation-free attention entry point.
 
 pkvd_paged_decode_attention_noalloc serves callers that cannot allocate
-device memory where they call (inside graph capture, runtimes that own all
-allocations, plain C hosts): it runs the same attention on a scratch array
-built into the library.  Here it is called through the C ABI and compared,
+device memory where they call (engines whose paged KV cache took all free
+memory at start-up, plugins in a runtime that owns every allocation, loops
+that must not synchronise on cudaMalloc, plain C hosts): it runs the same
+attention on a scratch array built into the library.  Here it is called through the C ABI and compared,
 on two calls in a row, with the regular entry point that takes a workspace.
 This file is collected last so that a failure here leaves every other test
 already run.

@@ -34,9 +34,14 @@
  *     (NULL = legacy default stream).  Every call only enqueues work on
  *     `stream` and returns; nothing synchronises, nothing allocates, no
  *     state is kept between calls.  The caller owns every buffer, including
- *     workspaces, and may capture the calls in a CUDA graph.  (The one
- *     exception is the host block manager below: an object the caller
- *     creates and destroys, touched by host calls only.)
+ *     workspaces, and may capture the calls in a CUDA graph.  (Two
+ *     exceptions: the host block manager below, an object the caller
+ *     creates and destroys, touched by host calls only; and
+ *     pkvd_paged_decode_attention_noalloc, which takes no workspace but
+ *     uses a scratch array built into the library and looks up its address
+ *     on its first call per device.  Its own comment gives its rules; the
+ *     sentences above on workspaces, state and graph capture do not cover
+ *     it.)
  *   - Argument checks run on the host before anything is enqueued and return
  *     a status code; the library never aborts, exits or traps.
  *   - `err_flag`, where present, is an optional device int32.  Kernels OR

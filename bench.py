@@ -972,6 +972,7 @@ def main():
                      "peak_source": peak_src, "traffic": recorded_traffic(cfg.name)},
         "e2e": {"value": ws * nbytes["step"] / (e2e_total / args.steps * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_total / args.steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        # the step graph's kernels, plus partition + merge of the attention-only replays
         "gpu_launches": step.kernels_per_step * args.steps + 2 * args.steps,
         "clocks": clocks, "device_err_flag": err,
     }

@@ -44,7 +44,7 @@ import workloads  # noqa: E402
 from workloads import configs  # noqa: E402
 
 METRIC = "decode-attention HBM GB/s (% of ~8 TB/s) and decode tokens/s per batch×ctx"
-DEFAULT_CONFIG = "qwen3"
+DEFAULT_CONFIG = "longctx"
 FLUSH_BYTES = 512 << 20
 
 
@@ -100,9 +100,12 @@ def kernel_source_hash(prefix="attention"):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(config_name, summary="attention_traffic.txt", prefix="attention"):
-    """DRAM bytes per kernel launch from a committed ncu summary, if it was
-    taken on the current kernel sources."""
+def recorded_traffic(config_name, algorithmic, summary="attention_traffic.txt", prefix="attention"):
+    """DRAM bytes (read + write) of one kernel launch from a committed ncu
+    summary, if it was taken on the current kernel sources: {"bytes",
+    "source"}, or None.  A record taken on a smaller profiling variant of the
+    workload (the fourth field gives that variant's algorithmic bytes) is
+    scaled to the full launch by the ratio of algorithmic bytes."""
     path = os.path.join(ROOT, "profiles", summary)
     if not os.path.exists(path):
         return None
@@ -110,7 +113,13 @@ def recorded_traffic(config_name, summary="attention_traffic.txt", prefix="atten
     for ln in open(path):
         parts = ln.split()
         if len(parts) >= 3 and not ln.startswith("#") and parts[0] == want and parts[1] == config_name:
-            return int(parts[2])
+            measured = int(parts[2])
+            profiled = int(parts[3]) if len(parts) >= 4 and parts[3].isdigit() else algorithmic
+            if profiled == algorithmic:
+                return {"bytes": measured, "source": f"ncu, one launch of this workload ({summary})"}
+            return {"bytes": int(round(measured * algorithmic / profiled)),
+                    "source": f"ncu, one launch of a smaller variant ({profiled} algorithmic bytes, "
+                              f"{measured} DRAM bytes), scaled by algorithmic bytes ({summary})"}
     return None
 
 
@@ -283,6 +292,7 @@ offset, stride, cycle = int(sys.argv[4]), int(sys.argv[5]), int(sys.argv[6])
 mine = list(range(offset, int(q.shape[0]), stride))
 counts, held = {}, {}
 elapsed = 0.0      # oracle time only: reading a row's arrays from the file is not timed
+attn = 0.0         # of which the attention call
 k = 0
 while mine and (k < len(mine) or cycle):
     i = mine[k % len(mine)]
@@ -297,28 +307,42 @@ while mine and (k < len(mine) or cycle):
     t0 = time.perf_counter()
     slots = oracle.paging.decode_slot_mapping(tab, ctx, bs)
     oracle.store.kv_store(knew[i:i + 1], vnew[i:i + 1], slots, kc, vc)
+    t1 = time.perf_counter()
     oracle.attention.decode_attention(q[i:i + 1], kc, vc, tab, ctx, scale)
+    t2 = time.perf_counter()
     oracle.sampler.sample_row(logits[i], float(temp[i]), int(topk[i]), float(topp[i]), int(seeds[i]), 0)
     elapsed += time.perf_counter() - t0
+    attn += t2 - t1
     counts[i] = counts.get(i, 0) + 1
     if elapsed > budget:
         break
-print(json.dumps({"counts": counts, "seconds": elapsed}))
+print(json.dumps({"counts": counts, "seconds": elapsed, "attention_seconds": attn}))
 """
 
 
 class OracleSample:
-    """Whole rows of a decode workload (mid-length rows first) written once to
-    a temporary file for the float64 oracle, which runs in single-threaded
-    subprocesses (OMP/BLAS threads 1)."""
+    """Whole rows of a decode workload (mid-length rows first, at most
+    `max_rows` and `max_bytes` of float64 K/V) written once to a temporary
+    file for the float64 oracle, which runs in single-threaded subprocesses
+    (OMP/BLAS threads 1)."""
 
-    def __init__(self, cfg, w, max_rows=None):
+    def __init__(self, cfg, w, max_rows=None, max_bytes=1.5e9):
         self.cfg, self.lay = cfg, w.layout
         lay = self.lay
         B = lay.num_seqs if max_rows is None else min(max_rows, lay.num_seqs)
-        order = np.argsort(lay.context_lens[:B])[::-1]
+        order = np.argsort(lay.context_lens)[::-1]
         order = np.concatenate([order[len(order) // 2:], order[:len(order) // 2]])  # mid-length rows first
-        sel = order[:B]
+        per_token = 2 * cfg.num_kv_heads * cfg.head_dim * 8          # float64 K and V of one token
+        sel, total = [], 0
+        for i in order:
+            if len(sel) >= B:
+                break
+            b = int(lay.context_lens[i]) * per_token
+            if sel and total + b > max_bytes:
+                continue
+            sel.append(int(i))
+            total += b
+        sel = np.array(sel, dtype=np.int64)
         self.sel = sel
         rows = torch.from_numpy(sel.copy()).to(w.q.device)
         arrays = {"bs": np.array(cfg.block_size), "scale": np.array(w.scale)}
@@ -341,37 +365,48 @@ class OracleSample:
         np.savez(self.path, **arrays)
         self.row_bytes = {}
 
+    @property
+    def num_rows(self):
+        return int(self.sel.shape[0])
+
     def bytes_of(self, i):
+        """(step bytes, attention bytes) of row i alone."""
         if i not in self.row_bytes:
             lay = self.lay
             one = workloads.Layout(lay.context_lens[i:i + 1], lay.block_tables[i:i + 1], lay.num_blocks, lay.layer,
                                    lay.max_context_len)
-            self.row_bytes[i] = algorithmic_bytes(self.cfg, one)["step"]
+            b = algorithmic_bytes(self.cfg, one)
+            self.row_bytes[i] = (b["step"], b["attention"])
         return self.row_bytes[i]
 
     def run(self, budget_s, procs=1):
-        """(rows done, seconds, bytes of those rows).  procs == 1: one pass over
-        the rows until ~budget_s of oracle time.  procs > 1: that many
-        processes, started together, each cycling through its share of the rows
-        for ~budget_s; seconds is the slowest one's oracle time."""
+        """One bounded oracle run: {"rows", "seconds", "bytes", "attention_seconds",
+        "attention_bytes", "procs"}.  procs == 1: one pass over the rows until
+        ~budget_s of oracle time.  procs > 1: that many processes (at most one
+        per row), started together, each cycling through its share of the rows
+        for ~budget_s; the seconds are the slowest process's."""
         env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        procs = max(1, min(procs, self.num_rows))
         cycle = 1 if procs > 1 else 0
         ps = [subprocess.Popen([sys.executable, "-c", ORACLE_SCRIPT, ROOT, self.path, str(budget_s), str(k),
                                 str(procs), str(cycle)], stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True,
                                env=env)
               for k in range(procs)]
         outs = [p.communicate() for p in ps]
-        done = nbytes = 0
-        secs = 0.0
+        res = {"rows": 0, "seconds": 0.0, "bytes": 0, "attention_seconds": 0.0, "attention_bytes": 0,
+               "procs": procs}
         for p, (out, err) in zip(ps, outs):
             if p.returncode:
                 raise RuntimeError(err[-2000:])
-            res = json.loads(out.strip().splitlines()[-1])
-            secs = max(secs, res["seconds"])
-            for j, c in res["counts"].items():
-                done += c
-                nbytes += c * self.bytes_of(int(self.sel[int(j)]))
-        return done, secs, nbytes
+            r = json.loads(out.strip().splitlines()[-1])
+            res["seconds"] = max(res["seconds"], r["seconds"])
+            res["attention_seconds"] = max(res["attention_seconds"], r["attention_seconds"])
+            for j, c in r["counts"].items():
+                sb, ab = self.bytes_of(int(self.sel[int(j)]))
+                res["rows"] += c
+                res["bytes"] += c * sb
+                res["attention_bytes"] += c * ab
+        return res
 
     def close(self):
         if os.path.exists(self.path):
@@ -383,7 +418,7 @@ def host_cores():
 
 
 def oracle_sample(cfg, w, budget_s=15.0, max_rows=None, procs=1):
-    """One bounded oracle run on rows of the workload: (rows, seconds, bytes)."""
+    """One bounded oracle run on rows of the workload (see OracleSample.run)."""
     smp = OracleSample(cfg, w, max_rows)
     try:
         return smp.run(budget_s, procs)
@@ -418,7 +453,9 @@ def barrier(ws):
 
 
 def run_reference(args, cfg, ws, rank, local):
-    """The oracle, as it stands, as the reference arm (rank 0 only)."""
+    """The oracle, as it stands, as the reference arm (rank 0 only): `value`
+    is the same quantity as the GPU arm's, the attention's algorithmic bytes
+    over the oracle's attention time."""
     if rank != 0:
         return
     w = workloads.make_workload(cfg, device=f"cuda:{local}" if torch.cuda.is_available() else "cpu")
@@ -427,27 +464,29 @@ def run_reference(args, cfg, ws, rank, local):
     # bounded time, so the whole run stays within about a minute of oracle time
     budget = max(1.0, min(args.cpu_seconds, 60.0 / max(1, args.steps)))
     smp = OracleSample(cfg, w)
+    tot = {"rows": 0, "seconds": 0.0, "bytes": 0, "attention_seconds": 0.0, "attention_bytes": 0}
     try:
         for _ in range(args.warmup):
             smp.run(min(1.0, budget), procs=cores)
-        rows_tot = secs_tot = bytes_tot = 0
         for _ in range(args.steps):
-            done, secs, nbytes = smp.run(budget, procs=cores)
-            rows_tot += done
-            secs_tot += secs
-            bytes_tot += nbytes
+            r = smp.run(budget, procs=cores)
+            procs = r["procs"]
+            for key in tot:
+                tot[key] += r[key]
     finally:
         smp.close()
-    value = bytes_tot / secs_tot / 1e9
+    value = tot["attention_bytes"] / tot["attention_seconds"] / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs_tot / args.steps,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot["seconds"] / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_block(cfg, w.layout),
-            "tokens_per_s": rows_tot / secs_tot,
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                             "sample": f"{rows_tot} whole rows (store + attention + sampler) over {args.steps} "
-                                       f"steps of ~{budget:.0f} s, {cores} single-threaded processes "
-                                       f"(os.cpu_count() = {os.cpu_count()})"},
+            "tokens_per_s": tot["rows"] / tot["seconds"],
+            "step_gbs": tot["bytes"] / tot["seconds"] / 1e9,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": procs, "kind": "oracle",
+                             "sample": f"{tot['rows']} whole rows (store + attention + sampler; value = attention "
+                                       f"bytes / attention time) of {smp.num_rows} mid-length rows, over "
+                                       f"{args.steps} steps of ~{budget:.0f} s on {procs} single-threaded "
+                                       f"processes (os.cpu_count() = {os.cpu_count()})"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -720,7 +759,7 @@ def run_prefill_bench(args):
                      "frac": achieved / peak,
                      "peak_source": "measured bf16 burst" if peaks.get("bf16_tflops") else "fallback",
                      "traffic": None if args.prefill_path in ("mma", "fma") else
-                     recorded_traffic(cfg.name, "prefill_traffic.txt", "prefill_tc")},
+                     (recorded_traffic(cfg.name, None, "prefill_traffic.txt", "prefill_tc") or {}).get("bytes")},
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps, "clocks": clocks, "device_err_flag": 0,
@@ -894,6 +933,10 @@ def main():
                     help="time a varlen prefill step (store + causal attention) instead (one JSON line)")
     ap.add_argument("--prefill-path", default="auto", choices=["auto", "tc", "mma", "fma"],
                     help="prefill attention kernel: tcgen05 (auto picks it where it runs), mma.sync or CUDA cores")
+    ap.add_argument("--per-config", default="grok1,qwen3,nanochat",
+                    help="more decode workloads timed after the headline one, in the same line (none: skip)")
+    ap.add_argument("--profile-attention", default=None, choices=sorted(PROFILE_VARIANTS),
+                    help="run one workload's attention call --steps times (the command ncu captures)")
     ap.add_argument("--serve", default=None, choices=["qwen3_prefill", "grok1_prefill", "chunked_prefill"],
                     help="serving timeline: the batch's prefill, then --steps decode steps (TTFT / TPOT, one line)")
     args = ap.parse_args()
@@ -907,6 +950,10 @@ def main():
     if args.block_manager:
         if rank == 0:
             run_block_manager_bench(args)
+        return
+    if args.profile_attention:
+        if rank == 0:
+            run_profile_attention(args)
         return
     if args.prefill:
         if rank == 0:
@@ -926,6 +973,7 @@ def main():
     nbytes = algorithmic_bytes(cfg, lay, window=args.window, extras=args.extras)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
+    n_attn = max(args.steps, ATTENTION_TIMINGS)
 
     step.capture()
     for _ in range(args.warmup):
@@ -938,11 +986,14 @@ def main():
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         step_ms = time_steps(step, flush, args.steps, stream)
-        attn_ms = time_attention(step, flush, args.steps, stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        attn_ms = time_attention(step, flush, n_attn, stream)
     torch.cuda.synchronize()
     barrier(ws)
     total_ms = max_over_ranks(sum(step_ms), ws, dev)
-    attn_mean = max_over_ranks(statistics.mean(attn_ms), ws, dev)
+    step_med = max_over_ranks(statistics.median(step_ms), ws, dev)
+    attn_med = max_over_ranks(statistics.median(attn_ms), ws, dev)
     clocks = clk.summary()
 
     pinned = {k: v.cpu() for k, v in host.items()}
@@ -957,23 +1008,35 @@ def main():
     if rank != 0:
         return
     ms_per_step = total_ms / args.steps
-    value = ws * nbytes["step"] / (ms_per_step * 1e-3) / 1e9
     peak, peak_src = peak_hbm()
-    attn_gbs = nbytes["attention"] / (attn_mean * 1e-3) / 1e9
+    attn_gbs = nbytes["attention"] / (attn_med * 1e-3) / 1e9
+    step_gbs = nbytes["step"] / (step_med * 1e-3) / 1e9
+    traffic = recorded_traffic(cfg.name, nbytes["attention"]) if not args.window else None
+    e2e_step_ms = e2e_total / args.steps
     line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "metric": METRIC, "value": ws * attn_gbs, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic", "config": config_block(cfg, lay, args.window, args.extras),
+        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+        "config": config_block(cfg, lay, args.window, args.extras),
+        "value_is": (f"paged decode attention (partition + LSE merge) algorithmic HBM bytes / median attention "
+                     f"time over {n_attn} graph replays, L2 flushed before each; ms_per_step and tokens_per_s "
+                     f"are the whole step (store, attention, merge, sampler) over the {args.steps} timed steps"),
         "tokens_per_s": ws * lay.num_seqs / (ms_per_step * 1e-3),
-        "step_bytes": nbytes["step"], "attention_bytes": nbytes["attention"],
-        "attention_ms": attn_mean, "attention_path": args.path,
+        "step": {"ms_median": step_med, "ms_mean": ms_per_step, "bytes": nbytes["step"], "gbs": ws * step_gbs,
+                 "frac": step_gbs / peak, "tokens_per_s_median": ws * lay.num_seqs / (step_med * 1e-3)},
+        "attention_bytes": nbytes["attention"], "attention_ms_median": attn_med,
+        "attention_ms_mean": statistics.mean(attn_ms), "attention_path": args.path,
         "roofline": {"kernel": "paged_decode_attention (partition + LSE merge kernels)", "bound": "hbm",
                      "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
-                     "peak_source": peak_src, "traffic": recorded_traffic(cfg.name)},
-        "e2e": {"value": ws * nbytes["step"] / (e2e_total / args.steps * 1e-3) / 1e9, "unit": "GB/s",
-                "ms_per_step": e2e_total / args.steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                     "peak_source": f"{peak_src} (copy peak, burst)", "traffic": traffic and traffic["bytes"],
+                     "traffic_source": traffic and traffic["source"]},
+        "e2e": {"value": ws * nbytes["attention"] / (e2e_step_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_step_ms, "tokens_per_s": ws * lay.num_seqs / (e2e_step_ms * 1e-3),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "is": "the attention bytes over the whole host-staged step (inputs copied in from pinned memory, "
+                      "the step, outputs copied back)"},
         # the step graph's kernels, plus partition + merge of the attention-only replays
-        "gpu_launches": step.kernels_per_step * args.steps + 2 * args.steps,
+        "gpu_launches": step.kernels_per_step * args.steps + 2 * n_attn,
         "clocks": clocks, "device_err_flag": err,
     }
     if not args.no_cpu_baseline and ws == 1:
@@ -982,17 +1045,100 @@ def main():
         cores = host_cores()
         smp = OracleSample(cfg, w)
         try:
-            done1, secs1, bytes1 = smp.run(args.cpu_seconds, procs=1)
-            done_n, secs_n, bytes_n = smp.run(max(1.0, min(args.cpu_seconds, 30.0 / cores)), procs=cores)
+            one = smp.run(args.cpu_seconds, procs=1)
+            alln = smp.run(max(1.0, min(args.cpu_seconds, 30.0 / cores)), procs=cores)
         finally:
             smp.close()
         line["cpu_baseline"] = {
-            "value": bytes_n / secs_n / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{done_n} whole rows of this workload (store + attention + sampler) in {secs_n:.1f} s on "
-                      f"{cores} single-threaded processes (os.cpu_count() = {os.cpu_count()})",
-            "single_thread": {"value": bytes1 / secs1 / 1e9, "unit": "GB/s", "cores": 1,
-                              "sample": f"{done1} whole rows, {secs1:.1f} s"}}
+            "value": alln["attention_bytes"] / alln["attention_seconds"] / 1e9, "unit": "GB/s",
+            "cores": alln["procs"], "kind": "oracle",
+            "sample": f"{alln['rows']} whole rows (store + attention + sampler) of {smp.num_rows} mid-length rows "
+                      f"of this workload in {alln['seconds']:.1f} s on {alln['procs']} single-threaded processes "
+                      f"(os.cpu_count() = {os.cpu_count()}); value = attention bytes / attention time",
+            "step_gbs": alln["bytes"] / alln["seconds"] / 1e9,
+            "tokens_per_s": alln["rows"] / alln["seconds"],
+            "single_thread": {"value": one["attention_bytes"] / one["attention_seconds"] / 1e9, "unit": "GB/s",
+                              "cores": 1, "sample": f"{one['rows']} whole rows, {one['seconds']:.1f} s"}}
+    others = [c for c in args.per_config.split(",") if c and c != "none" and c != cfg.name]
+    if others and ws == 1:
+        del w, step, host, pinned, hb
+        torch.cuda.empty_cache()
+        line["per_config"] = {name: measure_config(configs.get(name), dev, path, args, flush, stream, local,
+                                                   peak)
+                              for name in others}
     print(json.dumps(line))
+
+
+ATTENTION_TIMINGS = 100           # attention-call timings per workload (the median is reported)
+
+
+def measure_config(cfg, dev, path, args, flush, stream, local, peak):
+    """One more workload, timed like the headline one (its own clock record):
+    attention alone (median of ATTENTION_TIMINGS graph replays) and the whole
+    step (median of as many replays), each against the HBM roofline."""
+    w, step, host = build_step(cfg, dev, path)
+    lay = w.layout
+    nbytes = algorithmic_bytes(cfg, lay)
+    n = max(args.steps, ATTENTION_TIMINGS)
+    step.capture()
+    for _ in range(args.warmup):
+        flush.add_(1)
+        step.replay()
+    time_attention(step, flush, 3, stream)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        step_ms = time_steps(step, flush, n, stream)
+        attn_ms = time_attention(step, flush, n, stream)
+    torch.cuda.synchronize()
+    err = int(step.err.item())
+    a_med, s_med = statistics.median(attn_ms), statistics.median(step_ms)
+    a_gbs = nbytes["attention"] / (a_med * 1e-3) / 1e9
+    s_gbs = nbytes["step"] / (s_med * 1e-3) / 1e9
+    traffic = recorded_traffic(cfg.name, nbytes["attention"])
+    res = {"workload": cfg.description, "timings": n,
+           "attention_us": 1e3 * a_med, "attention_bytes": nbytes["attention"], "attention_gbs": a_gbs,
+           "attention_frac": a_gbs / peak,
+           "traffic": traffic and traffic["bytes"], "traffic_source": traffic and traffic["source"],
+           "traffic_over_algorithmic": traffic and traffic["bytes"] / nbytes["attention"],
+           "step_us": 1e3 * s_med, "step_bytes": nbytes["step"], "step_gbs": s_gbs, "step_frac": s_gbs / peak,
+           "tokens_per_s": lay.num_seqs / (s_med * 1e-3), "clocks": clk.summary(), "device_err_flag": err}
+    del w, step, host
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_profile_attention(args):
+    """The attention call of a workload (its profiling variant, small enough
+    for counter captures), `--steps` times back to back after one store: the
+    command that ncu captures for the DRAM-traffic records."""
+    import paged_kv_decode_store_gb300 as pk
+    cfg = PROFILE_VARIANTS[args.profile_attention]
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    w, step, _ = build_step(cfg, dev, pk.PATH_AUTO)
+    step.enqueue()
+    for _ in range(args.steps):
+        pk.paged_decode_attention(step.q, step.k_cache, step.v_cache, step.block_tables, step.context_lens,
+                                  step.max_context_len, step.scale, out=step.out, workspace=step.workspace,
+                                  err=step.err)
+    torch.cuda.synchronize()
+    if int(step.err.item()):
+        raise RuntimeError(f"device error flag {int(step.err.item())}")
+    nbytes = algorithmic_bytes(cfg, w.layout)
+    print(json.dumps({"profile_attention": args.profile_attention, "attention_bytes": nbytes["attention"],
+                      "calls": args.steps, "workload": cfg.description,
+                      "device_gb": torch.cuda.max_memory_allocated() / 1e9}))
+
+
+# Workloads whose attention launch ncu captures for DRAM traffic: the full
+# shapes where the device footprint is small, else the same shapes with a
+# smaller pool (one cache layer; a quarter of the rows).
+PROFILE_VARIANTS = {
+    "grok1": configs.GROK1,
+    "nanochat": configs.NANOCHAT,
+    "qwen3": configs.QWEN3.scaled(num_layers=1),
+    "longctx": configs.LONGCTX.scaled(num_seqs=64),
+}
 
 
 if __name__ == "__main__":

@@ -38,8 +38,8 @@
  *     exceptions: the host block manager below, an object the caller
  *     creates and destroys, touched by host calls only; and
  *     pkvd_paged_decode_attention_noalloc, which takes no workspace but
- *     uses a scratch array built into the library and looks up its address
- *     on its first call per device.  Its own comment gives its rules; the
+ *     uses a scratch array built into the library and remembers its device
+ *     address for calls under capture.  Its own comment gives its rules; the
  *     sentences above on workspaces, state and graph capture do not cover
  *     it.)
  *   - Argument checks run on the host before anything is enqueued and return
@@ -261,9 +261,14 @@ pkvd_status pkvd_paged_decode_attention_window(void* out, const void* q, const p
  * enqueued.  All calls on a GPU share the array: calls that overlap on the
  * GPU (unordered streams) race and give wrong results.  Each call writes
  * every part of the array it reads, so nothing needs clearing between
- * calls.  The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.
+ * calls.  Every call made outside stream capture looks up the array's
+ * device address (cudaGetSymbolAddress) in the current context, so a
+ * cudaDeviceReset or a context the caller made with the driver API is
+ * followed.  A call on a capturing stream reuses the address the last
+ * uncaptured call on that device found: make one uncaptured call per
+ * device, in the context that will replay the graph, before capturing.
+ * Argument checks, and their status codes, are the workspace entry
+ * point's; the 16 MiB limit is checked after them.
  * Nothing is allocated.
  */
 pkvd_status pkvd_paged_decode_attention_noalloc(void* out, const void* q, const pkvd_cache* cache,

@@ -1,31 +1,37 @@
 // The C ABI (include/pkvd.h): host-side argument checks, then one launcher
 // call per entry point.  Nothing here allocates, synchronises or keeps state
-// beyond a per-device SM-count cache.
+// beyond per-device memos of the SM count and L2 size.
 #include <cmath>
 
+#include "device_cache.h"
 #include "launch.h"
 
 namespace pkvd {
 
+namespace {
+PerDeviceMemo<int> g_sm_count;
+PerDeviceMemo<int64_t> g_l2_bytes;
+}  // namespace
+
 int device_sm_count() {
-  static int cache[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
-  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  const int known = g_sm_count.get(dev);
+  if (known > 0) return known;
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-  if (dev < 64) cache[dev] = n;
+  g_sm_count.put(dev, n);
   return n;
 }
 
 int64_t device_l2_bytes() {
-  static int64_t cache[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  const int64_t known = g_l2_bytes.get(dev);
+  if (known > 0) return known;
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return 0;
-  if (dev < 64) cache[dev] = n;
+  g_l2_bytes.put(dev, n);
   return n;
 }
 
@@ -218,22 +224,27 @@ pkvd_status pkvd_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, i
   return PKVD_OK;
 }
 
-namespace {
-pkvd_status attention_call(void* out, const void* q, const pkvd_cache* cache, const int32_t* block_tables,
-                           int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t max_context_len,
-                           int32_t num_seqs, int32_t num_q_heads, float scale, int32_t window, void* workspace,
-                           size_t workspace_bytes, void* stream, int32_t* err_flag, int32_t path) {
+}  // extern "C"
+
+namespace pkvd {
+
+pkvd_status attention_validate(void* out, const void* q, const pkvd_cache* cache, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t max_context_len,
+                               int32_t num_seqs, int32_t num_q_heads, float scale, int32_t window, int32_t* path,
+                               int* grid, size_t* need) {
+  *grid = 0;
+  *need = 0;
   if (num_seqs < 0 || num_q_heads <= 0 || max_context_len < 0 || !std::isfinite(scale)) return PKVD_INVALID_ARG;
   const pkvd_status cs = check_cache(cache, true);
   if (cs != PKVD_OK) return cs;
   if (num_q_heads % cache->num_kv_heads) return PKVD_UNSUPPORTED_SHAPE;
   const int G = num_q_heads / cache->num_kv_heads;
-  if (path == PKVD_PATH_AUTO) path = attention_default_path(cache->dtype, cache->head_dim, cache->num_kv_heads, G);
-  if (path != PKVD_PATH_FMA && path != PKVD_PATH_MMA) {
-    if (path == 0 || path == PKVD_PATH_TC) return PKVD_UNSUPPORTED_SHAPE;
+  if (*path == PKVD_PATH_AUTO) *path = attention_default_path(cache->dtype, cache->head_dim, cache->num_kv_heads, G);
+  if (*path != PKVD_PATH_FMA && *path != PKVD_PATH_MMA) {
+    if (*path == 0 || *path == PKVD_PATH_TC) return PKVD_UNSUPPORTED_SHAPE;
     return PKVD_INVALID_ARG;
   }
-  if (!attention_path_supported(path, cache->dtype, cache->head_dim, cache->num_kv_heads, G))
+  if (!attention_path_supported(*path, cache->dtype, cache->head_dim, cache->num_kv_heads, G))
     return PKVD_UNSUPPORTED_SHAPE;
   if (num_seqs == 0) return PKVD_OK;
   if (!out || !q || !block_tables || !context_lens || max_blocks_per_seq <= 0) return PKVD_INVALID_ARG;
@@ -242,8 +253,26 @@ pkvd_status attention_call(void* out, const void* q, const pkvd_cache* cache, co
   if (sms <= 0) return PKVD_CUDA_ERROR;
   // a window shortens every row's span: fewer units, never a larger grid
   const int span = (window > 0 && window < max_context_len) ? window : max_context_len;
-  const int grid = attention_grid(num_seqs, span, sms);
-  const size_t need = attention_workspace_bytes(num_seqs, num_q_heads, cache->head_dim, grid);
+  *grid = attention_grid(num_seqs, span, sms);
+  *need = attention_workspace_bytes(num_seqs, num_q_heads, cache->head_dim, *grid);
+  return PKVD_OK;
+}
+
+}  // namespace pkvd
+
+extern "C" {
+
+namespace {
+pkvd_status attention_call(void* out, const void* q, const pkvd_cache* cache, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t max_context_len,
+                           int32_t num_seqs, int32_t num_q_heads, float scale, int32_t window, void* workspace,
+                           size_t workspace_bytes, void* stream, int32_t* err_flag, int32_t path) {
+  int grid = 0;
+  size_t need = 0;
+  const pkvd_status vs = attention_validate(out, q, cache, block_tables, max_blocks_per_seq, context_lens,
+                                            max_context_len, num_seqs, num_q_heads, scale, window, &path, &grid,
+                                            &need);
+  if (vs != PKVD_OK || num_seqs == 0) return vs;
   if (!workspace || workspace_bytes < need) return PKVD_WORKSPACE_TOO_SMALL;
   if (!aligned16(workspace)) return PKVD_UNSUPPORTED_SHAPE;
   AttnArgs a;

@@ -17,11 +17,16 @@
 // Nothing in it has to start at zero: each call writes every merge record it
 // later reads, so the previous call's contents do no harm.
 // In host code the array's name is only a host-side stand-in, so its device
-// address is looked up with cudaGetSymbolAddress, once per device, by the
-// first call on that device (with that device current).  Make that first
-// call before any stream capture.
+// address is looked up with cudaGetSymbolAddress, with the call's device
+// current, on every call made outside stream capture: the address belongs to
+// the current context, which a cudaDeviceReset or a caller-made driver
+// context replaces.  A call made while its stream is capturing reuses the
+// address that the last uncaptured call on that device found (a lookup could
+// load the module, which capture forbids), so make one uncaptured call on
+// each device, in the context that will replay the graph, before capturing.
 #include <atomic>
 
+#include "device_cache.h"
 #include "launch.h"
 
 namespace pkvd {
@@ -35,21 +40,28 @@ constexpr size_t kNoAllocScratchBytes = 16u << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices] = {};   // set once per device
+// the address the last uncaptured call on each device found
+PerDeviceMemo<uintptr_t> g_scratch_addr;
 
-// Device address of the scratch on the current device (set-up on first use).
-cudaError_t scratch_address(void** out) {
+// Device address of the scratch in the current context.
+cudaError_t scratch_address(cudaStream_t stream, void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  void* ptr = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (!ptr) {   // threads racing here all look up, and store, the same address
-    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev].store(ptr, std::memory_order_release);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return e;
+  if (cap != cudaStreamCaptureStatusNone) {
+    const uintptr_t known = g_scratch_addr.get(dev);
+    if (known) {
+      *out = reinterpret_cast<void*>(known);
+      return cudaSuccess;
+    }
   }
+  void* ptr = nullptr;
+  e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+  if (e != cudaSuccess) return e;
+  if (cap == cudaStreamCaptureStatusNone) g_scratch_addr.put(dev, reinterpret_cast<uintptr_t>(ptr));
   *out = ptr;
   return cudaSuccess;
 }
@@ -66,16 +78,17 @@ pkvd_status pkvd_paged_decode_attention_noalloc(void* out, const void* q, const 
                                                 const int32_t* context_lens, int32_t max_context_len,
                                                 int32_t num_seqs, int32_t num_q_heads, float scale, void* stream,
                                                 int32_t* err_flag) {
-  // argument checks first, so a bad call never touches the device
-  if (num_seqs < 0 || num_q_heads <= 0 || max_context_len < 0) return PKVD_INVALID_ARG;
-  if (!cache || cache->head_dim <= 0) return PKVD_INVALID_ARG;
-  const int sms = device_sm_count();
-  if (sms <= 0) return PKVD_CUDA_ERROR;
-  const int grid = attention_grid(num_seqs, max_context_len, sms);
-  const size_t need = attention_workspace_bytes(num_seqs, num_q_heads, cache->head_dim, grid);
+  // the workspace entry point's own checks first, so every invalid call gets
+  // the same status from both entry points and never touches the device
+  int32_t path = PKVD_PATH_AUTO;
+  int grid = 0;
+  size_t need = 0;
+  const pkvd_status vs = attention_validate(out, q, cache, block_tables, max_blocks_per_seq, context_lens,
+                                            max_context_len, num_seqs, num_q_heads, scale, 0, &path, &grid, &need);
+  if (vs != PKVD_OK || num_seqs == 0) return vs;
   if (need > kNoAllocScratchBytes) return PKVD_WORKSPACE_TOO_SMALL;   // larger than the built-in scratch
   void* scratch = nullptr;
-  if (scratch_address(&scratch) != cudaSuccess) return PKVD_CUDA_ERROR;
+  if (scratch_address(static_cast<cudaStream_t>(stream), &scratch) != cudaSuccess) return PKVD_CUDA_ERROR;
   return pkvd_paged_decode_attention(out, q, cache, block_tables, max_blocks_per_seq, context_lens,
                                      max_context_len, num_seqs, num_q_heads, scale, scratch, need, stream,
                                      err_flag);

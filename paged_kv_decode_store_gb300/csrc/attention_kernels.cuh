@@ -643,9 +643,12 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(T* __restrict__ out, con
   __shared__ long long s_part[2][8];
   const int i = blockIdx.x;
   // Row i's chunk range [P, P + n) and the total C from the context lengths.
-  // They are inputs of the call, complete before the partition kernel (which
-  // waited for its own predecessor first) let this grid start, so this part
-  // overlaps the partition kernel; records are read after pdl_wait().
+  // They are read before pdl_wait(), so this part overlaps the partition
+  // kernel -- and possibly the kernel before it, since the partition kernel
+  // lets this grid start before its own dependency wait.  That is safe by the
+  // input contract of the attention call: context_lens is written by no
+  // kernel that lets its dependents start early (the library's own kernels
+  // never write it).  The partial records are read after pdl_wait().
   long long before = 0, all = 0;
   for (int r = threadIdx.x; r < num_seqs; r += blockDim.x) {
     const int c = chunks_of(ctx, r, ctx_cap, window);
@@ -748,15 +751,14 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(T* __restrict__ out, con
 // -------------------------------------------------------- launch helper
 inline size_t smem_header_bytes() { return ((sizeof(SmemHdr) + 127) / 128) * 128; }
 
+// The dynamic shared-memory limit is a per-device property of the kernel, so
+// it is set on every launch (a host-side call, no stream work): a process that
+// drives several GPUs, or several threads, needs no shared bookkeeping.
 template <typename T, int D, typename Consumer>
 cudaError_t launch_partition(const PartParams& pp, int grid, size_t smem, cudaStream_t stream) {
   auto kern = paged_decode_partition_kernel<T, D, Consumer>;
-  static size_t configured = 0;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(kAttnThreads), smem, stream, pp);
 }
 

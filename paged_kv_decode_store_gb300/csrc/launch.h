@@ -47,6 +47,14 @@ size_t attention_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, in
 bool attention_path_supported(int path, int dtype, int head_dim, int num_kv_heads, int group);
 int attention_default_path(int dtype, int head_dim, int num_kv_heads, int group);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
+// Host-side checks of a decode attention call (api.cu), shared by every
+// attention entry point: resolves PKVD_PATH_AUTO in *path and, for a call
+// with rows, gives the partition grid and the workspace bytes it needs.
+// Checks nothing about the workspace itself.
+pkvd_status attention_validate(void* out, const void* q, const pkvd_cache* cache, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t max_context_len,
+                               int32_t num_seqs, int32_t num_q_heads, float scale, int32_t window, int32_t* path,
+                               int* grid, size_t* need);
 
 cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* tables, int max_blocks,
                                 const int32_t* ctx, int num_seqs, int block_size,

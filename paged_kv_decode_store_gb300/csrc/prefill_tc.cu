@@ -42,6 +42,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <climits>
 #include <cmath>
 
@@ -748,17 +749,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
 
 using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
 
+// The driver's tensor-map encoder (one entry point for every device and
+// context).  Threads racing on the first lookup all store the same pointer.
+std::atomic<EncodeTiled> g_encode_fn{nullptr};
+
 EncodeTiled encode_fn() {
-  static EncodeTiled fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(f);
-    tried = true;
+  EncodeTiled fn = g_encode_fn.load(std::memory_order_acquire);
+  if (fn) return fn;
+  void* f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess) {
+    fn = reinterpret_cast<EncodeTiled>(f);
+    g_encode_fn.store(fn, std::memory_order_release);
   }
   return fn;
 }

@@ -38,6 +38,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "device_cache.h"
 #include "launch.h"
 
 namespace pkvd {
@@ -1765,17 +1766,24 @@ __global__ void __launch_bounds__(kExThreads) sample_extras_kernel(const ExtrasA
   (void)NP;
 }
 
-// Clusters of `cs` CTAs with `smem` bytes each that the GPU runs at once
-// (cached per size; a failed query falls back to an SM-count estimate).
+// Clusters of `cs` CTAs with `smem` bytes each that the GPU runs at once,
+// memoised per device and cluster size as one word (smem << 24 | count), so
+// concurrent first calls never pair one call's count with another's size.
+// A failed query falls back to an SM-count estimate.
+template <typename T>
+struct ClusterMemo {
+  static PerDeviceMemo<uint64_t> by_size[4];
+};
+template <typename T>
+PerDeviceMemo<uint64_t> ClusterMemo<T>::by_size[4];
+
 template <typename T>
 static int max_active_clusters(int cs, size_t smem, int sms) {
-  static int cache[4][64];
-  static size_t cache_smem[4][64];
-  int li = cs == 1 ? 0 : cs == 2 ? 1 : cs == 4 ? 2 : 3;
+  const int li = cs == 1 ? 0 : cs == 2 ? 1 : cs == 4 ? 2 : 3;
   int dev = 0;
-  cudaGetDevice(&dev);
-  dev &= 63;
-  if (cache[li][dev] > 0 && cache_smem[li][dev] == smem) return cache[li][dev];
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  const uint64_t known = ClusterMemo<T>::by_size[li].get(dev);
+  if (known != 0 && (known >> 24) == (uint64_t)smem) return (int)(known & 0xffffff);
   int n = 0;
   if (cudaFuncSetAttribute(sample_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
@@ -1793,8 +1801,8 @@ static int max_active_clusters(int cs, size_t smem, int sms) {
   }
   (void)cudaGetLastError();
   if (n <= 0) n = sms / cs > 0 ? sms / cs : 1;
-  cache[li][dev] = n;
-  cache_smem[li][dev] = smem;
+  if (n > 0xffffff) n = 0xffffff;
+  ClusterMemo<T>::by_size[li].put(dev, ((uint64_t)smem << 24) | (uint64_t)n);
   return n;
 }
 

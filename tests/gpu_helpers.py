@@ -15,6 +15,18 @@ ATOL_F32 = 1e-4
 RTOL_16 = 2e-2
 
 
+def sampling_exempt(info, p):
+    """True where float rounding may decide the draw: the oracle's two best
+    perturbed scores closer than 1e-5 * max(1, |s1|), or the nucleus cut mass
+    within 1e-6 of p (the readings of the "< 1e-5" rule and of the boundary)."""
+    if info["top2_gap"] < 1e-5 * max(1.0, abs(info["top1_score"])):
+        return True
+    n = info["nucleus"]
+    if n is not None and (abs(n["mass_before"] - p) < 1e-6 or abs(n["mass_after"] - p) < 1e-6):
+        return True
+    return False
+
+
 def require_gpu():
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
@@ -96,3 +108,53 @@ def oracle_sampled(w, gathered, rows, heads_per_row, window=0):
     q = w.q[rows].cpu().double().numpy()
     pairs = [(r, h) for r in range(len(rows)) for h in heads_per_row]
     return oracle.attention.decode_attention(q, kf, vf, tables, ctx, w.scale, pairs=pairs, window=window), pairs
+
+
+def oracle_rows_by_kv_head(w, rows, kv_heads_of_row):
+    """Oracle attention of whole rows of a (device) workload, for the listed KV
+    heads of each row and all their query heads.
+
+    Each row's blocks, restricted to those KV heads, are copied off the device
+    into a small cache of their own (call this before any kernel stores into
+    the cache); the oracle's store then writes the row's new token there and
+    the oracle's attention runs on it.  Returns {row: (query heads, output
+    [len(query heads), D] float64)}."""
+    lay, cfg = w.layout, w.cfg
+    bs, G, dt = cfg.block_size, cfg.group, w.cache.dtype
+    kc, vc = w.cache[0, lay.layer], w.cache[1, lay.layer]
+    res = {}
+    for i in rows:
+        c = int(lay.context_lens[i])
+        n = -(-c // bs)
+        hks = list(kv_heads_of_row[i])
+        heads = [hk * G + g for hk in hks for g in range(G)]
+        if n == 0:
+            res[i] = (heads, np.zeros((len(heads), cfg.head_dim)))
+            continue
+        idx = torch.from_numpy(lay.block_tables[i, :n].astype(np.int64)).to(kc.device)
+        hsel = torch.tensor(hks, dtype=torch.long, device=kc.device)
+        k = raw_numpy(kc.index_select(0, idx).index_select(2, hsel).cpu())
+        v = raw_numpy(vc.index_select(0, idx).index_select(2, hsel).cpu())
+        table = np.arange(n, dtype=np.int64)[None, :]
+        ctx = np.array([c], dtype=np.int64)
+        slot = oracle.paging.decode_slot_mapping(table, ctx, bs)
+        hsel_cpu = torch.tensor(hks, dtype=torch.long)
+        oracle.store.kv_store(raw_numpy(w.k_new[i:i + 1].cpu().index_select(1, hsel_cpu)),
+                              raw_numpy(w.v_new[i:i + 1].cpu().index_select(1, hsel_cpu)), slot, k, v)
+        kf = from_raw(k, dt).double().numpy()
+        vf = from_raw(v, dt).double().numpy()
+        q = w.q[i:i + 1, heads].double().cpu().numpy()
+        res[i] = (heads, oracle.attention.decode_attention(q, kf, vf, table, ctx, w.scale)[0])
+    return res
+
+
+def partition_ctas_per_row(context_lens, grid, chunk=16):
+    """How many partition CTAs share each row: the work is the flat list of
+    (row, 16-token chunk) pairs cut into `grid` equal contiguous slices."""
+    n = -(-np.maximum(np.asarray(context_lens, dtype=np.int64), 0) // chunk)
+    P = np.concatenate([[0], np.cumsum(n)[:-1]])
+    C = int(n.sum())
+    starts = np.array([(C * c) // grid for c in range(grid + 1)], dtype=np.int64)
+    first = np.searchsorted(starts, P, side="right") - 1
+    last = np.searchsorted(starts, P + np.maximum(n, 1) - 1, side="right") - 1
+    return np.where(n > 0, last - first + 1, 0)

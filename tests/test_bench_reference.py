@@ -25,14 +25,15 @@ def test_single_process_does_one_pass_over_every_row():
     cfg, w = _tiny()
     smp = bench.OracleSample(cfg, w)
     try:
-        done, secs, nbytes = smp.run(30.0, procs=1)
+        r = smp.run(30.0, procs=1)
     finally:
         smp.close()
     assert not os.path.exists(smp.path)
-    assert done == w.layout.num_seqs                     # every row once, well inside the budget
-    assert secs > 0
-    # the bytes of one pass over all rows are the workload's step bytes
-    assert nbytes == bench.algorithmic_bytes(cfg, w.layout)["step"]
+    assert r["rows"] == w.layout.num_seqs                # every row once, well inside the budget
+    assert r["seconds"] >= r["attention_seconds"] > 0
+    # the bytes of one pass over all rows are the workload's step and attention bytes
+    b = bench.algorithmic_bytes(cfg, w.layout)
+    assert r["bytes"] == b["step"] and r["attention_bytes"] == b["attention"]
 
 
 def test_processes_share_the_rows_and_cycle_for_the_budget():
@@ -40,9 +41,11 @@ def test_processes_share_the_rows_and_cycle_for_the_budget():
     cfg, w = _tiny()
     smp = bench.OracleSample(cfg, w)
     try:
-        done, secs, nbytes = smp.run(0.3, procs=3)
+        r = smp.run(0.3, procs=3)
     finally:
         smp.close()
+    done, secs, nbytes = r["rows"], r["seconds"], r["bytes"]
+    assert r["procs"] == 3
     per_row = [bench.algorithmic_bytes(cfg, type(w.layout)(w.layout.context_lens[i:i + 1],
                                                            w.layout.block_tables[i:i + 1], w.layout.num_blocks,
                                                            w.layout.layer, w.layout.max_context_len))["step"]
@@ -63,6 +66,27 @@ def test_reference_arm_prints_the_contract_line():
     for key in ("metric", "value", "unit", "n_gpus", "ms_per_step", "higher_is_better", "config", "cpu_baseline",
                 "e2e"):
         assert key in line, key
-    assert line["cpu_baseline"]["cores"] == max(1, os.cpu_count() or 1)
+    # one single-threaded process per host core, at most one per row (tiny has 4 rows)
+    assert line["cpu_baseline"]["cores"] == min(max(1, os.cpu_count() or 1), 4)
     assert line["cpu_baseline"]["value"] == line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and np.isfinite(line["e2e"]["value"])
+
+
+def test_oracle_sample_keeps_mid_length_rows_within_its_byte_bound():
+    """A long-context workload is sampled by whole mid-length rows under the
+    float64 byte bound (the full workload would be tens of GB of float64)."""
+    import bench
+    import workloads
+    from workloads import configs
+    cfg = configs.LONGCTX.scaled(num_seqs=40, vocab=1000)
+    w = workloads.make_workload(cfg, device="cpu")
+    per_token = 2 * cfg.num_kv_heads * cfg.head_dim * 8
+    smp = bench.OracleSample(cfg, w, max_bytes=200e6)
+    try:
+        ctx = w.layout.context_lens[smp.sel].astype(np.int64)
+        assert 1 <= smp.num_rows < 40
+        assert ctx.sum() * per_token <= 200e6 or smp.num_rows == 1
+        med = np.median(w.layout.context_lens)
+        assert ctx.max() <= np.max(w.layout.context_lens) and abs(np.median(ctx) - med) < med
+    finally:
+        smp.close()

@@ -14,7 +14,7 @@ import oracle
 import workloads
 from workloads import configs
 from gpu_helpers import (require_gpu, oracle_store_f64, check_attention, gather_rows_for_oracle,
-                         oracle_sampled)
+                         oracle_sampled, oracle_rows_by_kv_head, partition_ctas_per_row)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -138,6 +138,37 @@ def test_full_size_sampled_rows(name):
         a, b = outs[pk.PATH_FMA], outs[pk.PATH_MMA]
         rel = (a - b).abs().amax(dim=-1) / a.abs().amax(dim=-1).clamp_min(1e-6)
         assert float(rel.max()) <= 2 * 2e-2
+
+
+@pytest.mark.parametrize("name", ["grok1", "qwen3", "longctx"])
+def test_full_size_every_row_against_oracle(name):
+    """The benchmark's shapes and launch configuration, every row against the
+    oracle: grok1 and qwen3 with every head, longctx with one KV head per row
+    (rotating over the heads) and its whole query group.  The stream-K slices
+    cut many rows across three or more CTAs (the merge of several partial
+    records); the test asserts that such rows exist and are among those
+    checked."""
+    pk = require_gpu()
+    cfg = configs.CONFIGS[name]
+    w = workloads.make_workload(cfg, device=DEV)
+    lay = w.layout
+    B, Hkv = lay.num_seqs, cfg.num_kv_heads
+    if name == "longctx":
+        kv_heads = {i: [i % Hkv] for i in range(B)}
+    else:
+        kv_heads = {i: list(range(Hkv)) for i in range(B)}
+    ref = oracle_rows_by_kv_head(w, range(B), kv_heads)      # before any kernel touches the cache
+    ws = pk.decode_workspace_bytes(B, cfg.num_q_heads, cfg.head_dim, lay.max_context_len)
+    grid = ws // (2 * cfg.num_q_heads * (cfg.head_dim + 4) * 4)
+    spans = partition_ctas_per_row(lay.context_lens, grid)
+    assert spans.max() >= 3, spans.max()
+    for path in paths_for(cfg, pk):
+        out, err = run_attention(pk, w, path, cache=w.cache)
+        assert err == 0
+        o = out.double().cpu().numpy()
+        for i in range(B):
+            heads, r = ref[i]
+            check_attention(o[i:i + 1, heads], r[None], w.q.dtype)
 
 
 def test_workspace_is_reusable_without_clearing():

@@ -14,7 +14,7 @@ from scipy import stats
 import oracle
 import workloads
 from workloads import configs
-from gpu_helpers import require_gpu
+from gpu_helpers import require_gpu, sampling_exempt
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -27,13 +27,7 @@ def _dev_params(si, B=None):
             torch.from_numpy(si.offsets.view(np.int64)).to(DEV))
 
 
-def _exempt(info, p):
-    if info["top2_gap"] < 1e-5 * max(1.0, abs(info["top1_score"])):
-        return True
-    n = info["nucleus"]
-    if n is not None and (abs(n["mass_before"] - p) < 1e-6 or abs(n["mass_after"] - p) < 1e-6):
-        return True
-    return False
+_exempt = sampling_exempt
 
 
 @pytest.mark.parametrize("name", list(configs.CONFIGS))

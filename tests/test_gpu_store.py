@@ -93,15 +93,36 @@ def test_kv_store_skips_negative_and_flags_out_of_range():
     assert err.item() == pk.ERR_SLOT
 
 
-@pytest.mark.parametrize("name", list(_small_variants()) + ["qwen3_full"])
+FULL = {"qwen3_full": configs.QWEN3, "grok1_full": configs.GROK1, "longctx_full": configs.LONGCTX}
+
+
+def _touched_blocks(lay, bs):
+    """Rows with a token to store, the block each one's slot falls in, and the
+    row offset inside that block."""
+    ctx = lay.context_lens.astype(np.int64)
+    rows = np.nonzero(ctx > 0)[0]
+    blocks = np.array([lay.block_tables[i, (ctx[i] - 1) // bs] for i in rows], dtype=np.int64)
+    return rows, blocks, (ctx[rows] - 1) % bs
+
+
+@pytest.mark.parametrize("name", list(_small_variants()) + list(FULL))
 def test_kv_store_paged_matches_the_two_step_store(name):
     """The fused slot-mapping + store kernel writes the same cache bits and
-    slots as pkvd_slot_mapping followed by pkvd_kv_store (and the oracle)."""
+    slots as pkvd_slot_mapping followed by pkvd_kv_store, and the blocks it
+    touches hold what the oracle's store writes into a copy of them."""
     pk = require_gpu()
-    cfg = configs.QWEN3 if name == "qwen3_full" else _small_variants()[name]
-    w = workloads.make_workload(cfg, device=DEV if name == "qwen3_full" else "cpu")
+    cfg = FULL[name] if name in FULL else _small_variants()[name]
+    w = workloads.make_workload(cfg, device=DEV if name in FULL else "cpu")
     lay = w.layout
     base = w.cache.to(DEV)
+    # the oracle's store on a host copy of every block the step writes into
+    rows, blocks, offs = _touched_blocks(lay, cfg.block_size)
+    bidx = torch.from_numpy(blocks).to(DEV)
+    k_ref = raw_numpy(base[0, lay.layer].index_select(0, bidx).cpu())
+    v_ref = raw_numpy(base[1, lay.layer].index_select(0, bidx).cpu())
+    sub_slots = np.arange(len(rows), dtype=np.int64) * cfg.block_size + offs
+    ridx = torch.from_numpy(rows)
+    oracle.store.kv_store(raw_numpy(w.k_new.cpu()[ridx]), raw_numpy(w.v_new.cpu()[ridx]), sub_slots, k_ref, v_ref)
     tables = torch.from_numpy(lay.block_tables).to(DEV)
     ctx = torch.from_numpy(lay.context_lens).to(DEV)
     k_new, v_new = w.k_new.to(DEV), w.v_new.to(DEV)
@@ -120,6 +141,8 @@ def test_kv_store_paged_matches_the_two_step_store(name):
     assert err1.item() == 0 and err2.item() == 0
     ref = oracle.paging.decode_slot_mapping(lay.block_tables, lay.context_lens, cfg.block_size)
     assert np.array_equal(slots1.cpu().numpy(), ref)
+    assert np.array_equal(raw_numpy(one[0, lay.layer].index_select(0, bidx).cpu()), k_ref)
+    assert np.array_equal(raw_numpy(one[1, lay.layer].index_select(0, bidx).cpu()), v_ref)
 
 
 def test_kv_store_paged_flags_and_skips_like_slot_mapping():

@@ -64,12 +64,42 @@ def test_noalloc_matches_workspace_entry_point_twice(cfg):
         check_attention(out.double().cpu().numpy(), ref.double().cpu().numpy(), q.dtype)
 
 
+def _big_call(pk, entry, kc, vc, num_heads, scale, ws=None):
+    """A call with 4096 rows of `num_heads` query heads on buffers sized for it
+    (so even a call that went through would stay in bounds)."""
+    from paged_kv_decode_store_gb300 import _capi
+    B, D = 4096, kc.shape[-1]
+    q = torch.zeros(B, num_heads, D, dtype=kc.dtype, device=DEV)
+    out = torch.empty_like(q)
+    tables = torch.zeros(B, 4, dtype=torch.int32, device=DEV)
+    ctx = torch.full((B,), 64, dtype=torch.int32, device=DEV)
+    c = _capi.cache_desc(kc, vc)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    args = [out.data_ptr(), q.data_ptr(), ctypes.byref(c), tables.data_ptr(), 4, ctx.data_ptr(), 64, B,
+            num_heads, ctypes.c_float(scale)]
+    if entry == "noalloc":
+        st = pk.lib().pkvd_paged_decode_attention_noalloc(*args, stream, err.data_ptr())
+    else:
+        st = pk.lib().pkvd_paged_decode_attention(*args, ws.data_ptr(), ws.numel(), stream, err.data_ptr())
+    torch.cuda.synchronize()
+    return st, err.item()
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     pk, w, lay, kc, vc, tables, ctx = _inputs(configs.GROK1.scaled(num_seqs=2, ctx_args=(64,), vocab=2048))
-    big_seqs, big_heads = 4096, 128                # 128 query heads: records beyond the scratch
-    from paged_kv_decode_store_gb300 import _capi
-    c = _capi.cache_desc(kc, vc)
-    assert pk.decode_workspace_bytes(big_seqs, big_heads, 128, 64) > 16 << 20
-    st = pk.lib().pkvd_paged_decode_attention_noalloc(
-        0, 0, ctypes.byref(c), 0, 1, 0, 64, big_seqs, big_heads, ctypes.c_float(0.1), None, None)
-    assert st == 4                                 # PKVD_WORKSPACE_TOO_SMALL, nothing enqueued
+    assert pk.decode_workspace_bytes(4096, 128, 128, 64) > 16 << 20    # 128 query heads: beyond the scratch
+    st, err = _big_call(pk, "noalloc", kc, vc, 128, 0.1)
+    assert st == 4 and err == 0                    # PKVD_WORKSPACE_TOO_SMALL, nothing enqueued
+
+
+@pytest.mark.parametrize("heads,scale,status", [(132, 0.1, 3), (128, float("inf"), 1)],
+                         ids=["group_not_dividing", "scale_not_finite"])
+def test_noalloc_reports_invalid_calls_like_the_workspace_entry_point(heads, scale, status):
+    """An invalid call that is also too big for the scratch gets the workspace
+    entry point's status (the shape or argument error), not the size error."""
+    pk, w, lay, kc, vc, tables, ctx = _inputs(configs.GROK1.scaled(num_seqs=2, ctx_args=(64,), vocab=2048))
+    ws = torch.zeros(32 << 20, dtype=torch.uint8, device=DEV)
+    st_ws, _ = _big_call(pk, "workspace", kc, vc, heads, scale, ws)
+    st_na, err = _big_call(pk, "noalloc", kc, vc, heads, scale)
+    assert st_ws == status and st_na == status and err == 0

@@ -1126,7 +1126,8 @@ def run_profile_attention(args):
         raise RuntimeError(f"device error flag {int(step.err.item())}")
     nbytes = algorithmic_bytes(cfg, w.layout)
     print(json.dumps({"profile_attention": args.profile_attention, "attention_bytes": nbytes["attention"],
-                      "calls": args.steps, "workload": cfg.description,
+                      "calls": args.steps, "workload": cfg.description, "num_seqs": cfg.num_seqs,
+                      "num_layers": cfg.num_layers,
                       "device_gb": torch.cuda.max_memory_allocated() / 1e9}))
 
 

@@ -254,6 +254,57 @@ def time_attention(step, flush, steps, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
+def time_attention_loop(step, calls, stream):
+    """Mean per-call time (ms) of `calls` attention-graph replays back to back,
+    between two CUDA events: the steady state of a layer loop, each call
+    streaming its K/V from DRAM (only used where the K/V is larger than L2)."""
+    time_attention(step, L2FlushNone(), 1, stream)          # makes sure the graph exists
+    g = step._attn_graph
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(calls):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / calls
+
+
+class L2FlushNone:
+    def add_(self, _):
+        pass
+
+
+def time_sampler(step, flush, steps, stream):
+    """Per-call CUDA-event durations (ms) of the sampler alone, replayed from
+    its own CUDA graph right behind the L2 flush (the logits come from DRAM)."""
+    import paged_kv_decode_store_gb300 as pk
+
+    def call():
+        step._enqueue_sample(pk.lib(), pk.stream_handle(None, step.q))
+
+    g = getattr(step, "_samp_graph", None)
+    if g is None:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            call()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call()
+        step._samp_graph = g
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.add_(1)
+        starts[i].record(stream)
+        g.replay()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
 def time_e2e(step, host_inputs, flush, steps, stream):
     """Public-API step with host buffers: one graph holds the H2D copy of the
     step's inputs (pinned arena), the logits' H2D copy on a second stream
@@ -500,6 +551,10 @@ def config_block(cfg, lay, window=0, extras=False):
             "kv_heads": cfg.num_kv_heads, "head_dim": cfg.head_dim, "block_size": cfg.block_size,
             "vocab": cfg.vocab,
             "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MB write, then {FLUSH_BYTES >> 20} MB read)"}
+
+
+def device_l2_bytes():
+    return torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
 
 
 def peak_hbm():
@@ -995,6 +1050,9 @@ def main():
     step_med = max_over_ranks(statistics.median(step_ms), ws, dev)
     attn_med = max_over_ranks(statistics.median(attn_ms), ws, dev)
     clocks = clk.summary()
+    time_sampler(step, flush, 3, stream)
+    samp_ms = time_sampler(step, flush, n_attn, stream)
+    loop_ms = time_attention_loop(step, n_attn, stream) if nbytes["attention"] > device_l2_bytes() else None
 
     pinned = {k: v.cpu() for k, v in host.items()}
     for _ in range(2):
@@ -1026,6 +1084,15 @@ def main():
                  "frac": step_gbs / peak, "tokens_per_s_median": ws * lay.num_seqs / (step_med * 1e-3)},
         "attention_bytes": nbytes["attention"], "attention_ms_median": attn_med,
         "attention_ms_mean": statistics.mean(attn_ms), "attention_path": args.path,
+        "attention_back_to_back": loop_ms and {
+            "ms_per_call": loop_ms, "gbs": nbytes["attention"] / (loop_ms * 1e-3) / 1e9,
+            "frac": nbytes["attention"] / (loop_ms * 1e-3) / 1e9 / peak,
+            "is": f"{n_attn} attention calls back to back between two events (K/V larger than L2, so each "
+                  "call streams from DRAM): the steady state of a loop over layers"},
+        "sampler": {"ms_median": statistics.median(samp_ms), "bytes": nbytes["sampler"],
+                    "gbs": nbytes["sampler"] / (statistics.median(samp_ms) * 1e-3) / 1e9,
+                    "frac": nbytes["sampler"] / (statistics.median(samp_ms) * 1e-3) / 1e9 / peak,
+                    "is": f"the sampler call alone, median of {n_attn} graph replays, L2 flushed before each"},
         "roofline": {"kernel": "paged_decode_attention (partition + LSE merge kernels)", "bound": "hbm",
                      "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
                      "peak_source": f"{peak_src} (copy peak, burst)", "traffic": traffic and traffic["bytes"],
@@ -1036,6 +1103,7 @@ def main():
                 "is": "the attention bytes over the whole host-staged step (inputs copied in from pinned memory, "
                       "the step, outputs copied back)"},
         # the step graph's kernels, plus partition + merge of the attention-only replays
+        # (the sampler-alone and back-to-back timings run after the timed region)
         "gpu_launches": step.kernels_per_step * args.steps + 2 * n_attn,
         "clocks": clocks, "device_err_flag": err,
     }
@@ -1086,12 +1154,17 @@ def measure_config(cfg, dev, path, args, flush, stream, local, peak):
         step.replay()
     time_attention(step, flush, 3, stream)
     torch.cuda.synchronize()
+    time_sampler(step, flush, 3, stream)
     with ClockSampler(local) as clk:
         step_ms = time_steps(step, flush, n, stream)
         attn_ms = time_attention(step, flush, n, stream)
+        samp_ms = time_sampler(step, flush, n, stream)
     torch.cuda.synchronize()
     err = int(step.err.item())
     a_med, s_med = statistics.median(attn_ms), statistics.median(step_ms)
+    sp_med = statistics.median(samp_ms)
+    l2 = device_l2_bytes()
+    loop_ms = time_attention_loop(step, n, stream) if nbytes["attention"] > l2 else None
     a_gbs = nbytes["attention"] / (a_med * 1e-3) / 1e9
     s_gbs = nbytes["step"] / (s_med * 1e-3) / 1e9
     traffic = recorded_traffic(cfg.name, nbytes["attention"])
@@ -1100,6 +1173,11 @@ def measure_config(cfg, dev, path, args, flush, stream, local, peak):
            "attention_frac": a_gbs / peak,
            "traffic": traffic and traffic["bytes"], "traffic_source": traffic and traffic["source"],
            "traffic_over_algorithmic": traffic and traffic["bytes"] / nbytes["attention"],
+           "attention_us_back_to_back": loop_ms and 1e3 * loop_ms,
+           "attention_frac_back_to_back": loop_ms and nbytes["attention"] / (loop_ms * 1e-3) / 1e9 / peak,
+           "sampler_us": 1e3 * sp_med, "sampler_bytes": nbytes["sampler"],
+           "sampler_gbs": nbytes["sampler"] / (sp_med * 1e-3) / 1e9,
+           "sampler_frac": nbytes["sampler"] / (sp_med * 1e-3) / 1e9 / peak,
            "step_us": 1e3 * s_med, "step_bytes": nbytes["step"], "step_gbs": s_gbs, "step_frac": s_gbs / peak,
            "tokens_per_s": lay.num_seqs / (s_med * 1e-3), "clocks": clk.summary(), "device_err_flag": err}
     del w, step, host

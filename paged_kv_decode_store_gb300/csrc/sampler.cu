@@ -113,6 +113,15 @@ __device__ __forceinline__ uint32_t cluster_size() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Split cluster barrier: every thread arrives once at kernel start and waits
+// before its CTA's first access to a peer's shared memory, which is how a
+// CTA knows that every CTA of its cluster has started.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
 __device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
   uint32_t a;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
@@ -604,6 +613,7 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
 
   pdl_wait();                       // logits and parameters may come from the previous kernel
   pdl_trigger();
+  cluster_arrive_relaxed();         // matched by cluster_wait() before the first peer access
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   Ctx c{&h, (int)cluster_size(), 0};
   const uint32_t crank = cluster_rank();
@@ -696,6 +706,7 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
         for (int j = rest + tid; j < n; j += kSampThreads) mx = max(mx, K::key(bits_at(j)));
         kmr = (uint32_t)block_max_u64(mx, h.red);
       }
+      cluster_wait();                                   // every peer has started
       const float Tr = a.temperature[row_id];
       if (!(Tr > 0.f)) {
         // greedy: this slice's lowest index holding its max key, then one
@@ -1274,6 +1285,7 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_kernel(const SampArgs 
     best = pk > best ? pk : best;
   });
   best = block_max_u64(best, h.red);
+  cluster_wait();                                   // every peer has started
   best = cluster_scalar<true>(c, best);
   const uint32_t kmax = (uint32_t)(best >> 32);
   const int imax = (int)(0xffffffffu - (uint32_t)(best & 0xffffffffu));
@@ -1556,6 +1568,7 @@ __global__ void __launch_bounds__(kExThreads) sample_extras_kernel(const ExtrasA
   __shared__ long long s_n[kExWarps];
   pdl_wait();                       // the sampler's token and row_info
   pdl_trigger();
+  cluster_arrive_relaxed();         // matched by cluster_wait() before the push to rank 0
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t crank = cluster_rank();
   const int r = blockIdx.x / kExCluster;
@@ -1593,6 +1606,7 @@ __global__ void __launch_bounds__(kExThreads) sample_extras_kernel(const ExtrasA
         ++next;
       }
     }
+    cluster_wait();
     return;
   }
   const float Tr = e.temperature[r];
@@ -1705,6 +1719,7 @@ __global__ void __launch_bounds__(kExThreads) sample_extras_kernel(const ExtrasA
     for (int i = 0; i < kTop; ++i) s_top[warp][i] = wl[i];
   }
   __syncthreads();
+  cluster_wait();                   // every rank has started: rank 0's table may be written
   if (warp == 0) {
     double zb = lane < kExWarps ? s_z[lane] : 0.0;
     long long nb = lane < kExWarps ? s_n[lane] : 0;

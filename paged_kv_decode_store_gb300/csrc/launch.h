@@ -105,6 +105,35 @@ cudaError_t launch_kv_store_prefill(const void* k, const void* v, const int32_t*
 constexpr int kRowInfo = 8;
 constexpr int kRowGreedy = 1, kRowUniform = 2, kRowTopK = 4;
 
+// One sampler call's arguments, for the two builds of the sampler kernel
+// (sampler.cu: 1024-thread CTAs; sampler512.cu: 512-thread CTAs).
+struct SampleCall {
+  int32_t* token_ids;
+  const void* logits;
+  int dtype;
+  int num_rows;
+  int vocab;
+  int64_t row_stride;
+  const float* temperature;
+  const int32_t* top_k;
+  const float* top_p;
+  const uint64_t* seeds;
+  const uint64_t* offsets;
+  const uint32_t* mask;
+  int64_t mask_stride;
+  int32_t* row_info;
+};
+// Each build: launch (or, with waves_only, only report how many waves of
+// clusters it would need), and whether a masked row fits on chip.
+namespace s1024 {
+cudaError_t sample_launch(const SampleCall& c, cudaStream_t stream, int* waves_only);
+bool sample_mask_fits(int dtype, int vocab, int64_t row_stride, const void* logits);
+}  // namespace s1024
+namespace s512 {
+cudaError_t sample_launch(const SampleCall& c, cudaStream_t stream, int* waves_only);
+bool sample_mask_fits(int dtype, int vocab, int64_t row_stride, const void* logits);
+}  // namespace s512
+
 cudaError_t launch_sample(int32_t* token_ids, const void* logits, int dtype, int num_rows,
                           int vocab, int64_t row_stride, const float* temperature,
                           const int32_t* top_k, const float* top_p, const uint64_t* seeds,

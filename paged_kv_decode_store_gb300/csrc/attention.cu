@@ -98,16 +98,20 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   // the merge kernel as a programmatic dependent of the partition kernel
   const long long cap_all = (long long)a.max_blocks_per_seq * a.block_size;
   const int ctx_cap = (int)(cap_all < a.max_context_len ? cap_all : a.max_context_len);
-  const int groups = (a.num_q_heads * (a.head_dim / 4) + 255) / 256;
+  // lanes per output slice: enough that a row's records load in one round of
+  // eight per lane (rows are cut into about grid / num_seqs + 1 pieces)
+  const int pieces = a.grid / a.num_seqs + 1;
+  const int parts = pieces > 16 ? 4 : pieces > 8 ? 2 : 1;
+  const int groups = (a.num_q_heads * (a.head_dim / 4) * parts + 255) / 256;
   const dim3 mg((unsigned)a.num_seqs, (unsigned)groups), mb(256);
   if (a.dtype == PKVD_F32)
     return launch_pdl(lse_merge_kernel<float>, mg, mb, 0, stream, static_cast<float*>(a.out), (const float*)rec,
-                      a.context_lens, ctx_cap, a.window, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
+                      a.context_lens, ctx_cap, a.window, a.num_seqs, a.num_q_heads, a.head_dim, a.grid, parts);
   if (a.dtype == PKVD_F16)
     return launch_pdl(lse_merge_kernel<__half>, mg, mb, 0, stream, static_cast<__half*>(a.out), (const float*)rec,
-                      a.context_lens, ctx_cap, a.window, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
+                      a.context_lens, ctx_cap, a.window, a.num_seqs, a.num_q_heads, a.head_dim, a.grid, parts);
   return launch_pdl(lse_merge_kernel<__nv_bfloat16>, mg, mb, 0, stream, static_cast<__nv_bfloat16*>(a.out),
-                    (const float*)rec, a.context_lens, ctx_cap, a.window, a.num_seqs, a.num_q_heads, a.head_dim, a.grid);
+                    (const float*)rec, a.context_lens, ctx_cap, a.window, a.num_seqs, a.num_q_heads, a.head_dim, a.grid, parts);
 }
 
 }  // namespace pkvd

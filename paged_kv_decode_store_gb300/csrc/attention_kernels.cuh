@@ -637,7 +637,7 @@ constexpr int kMaxMergeRecords = 1024;     // >= any partition grid (one CTA per
 template <typename T>
 __global__ void __launch_bounds__(256) lse_merge_kernel(T* __restrict__ out, const float* __restrict__ rec,
                                                         const int32_t* __restrict__ ctx, int ctx_cap, int window,
-                                                        int num_seqs, int hq, int D, int grid) {
+                                                        int num_seqs, int hq, int D, int grid, int parts) {
   __shared__ int s_rec[kMaxMergeRecords];
   __shared__ int s_n;
   __shared__ long long s_part[2][8];
@@ -703,22 +703,31 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(T* __restrict__ out, con
   const int nrec = s_n;
   pdl_wait();                       // the partition kernel's records
   pdl_trigger();
+  // `parts` adjacent lanes (1, 2 or 4) share one float4 output slice: part
+  // p takes records p, p + parts, ..., so a row cut into many pieces needs
+  // fewer rounds of record loads; the parts' states are then combined with
+  // shuffles (the same identity).
   const int Q = D / 4;
   constexpr int R = 8;
-  for (int idx = blockIdx.y * blockDim.x + threadIdx.x; idx < hq * Q; idx += gridDim.y * blockDim.x) {
-    const int h = idx / Q, d4 = (idx % Q) * 4;
+  const int nslots = hq * Q * parts;
+  for (int base = blockIdx.y * blockDim.x; base < nslots; base += gridDim.y * blockDim.x) {
+    const int t = base + threadIdx.x;                 // whole warps iterate together
+    const int sl = t / parts, part = t % parts;
+    const bool live = t < nslots;
+    const int h = live ? sl / Q : 0, d4 = live ? (sl % Q) * 4 : 0;
     float M = -INFINITY, L = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k0 = 0; k0 < nrec; k0 += R) {
+    for (int k0 = part; live && k0 < nrec; k0 += R * parts) {
       float mk[R], lk[R];
       float4 ak[R];
 #pragma unroll
       for (int e = 0; e < R; ++e) {
+        const int k = k0 + e * parts;
         mk[e] = -INFINITY;
         lk[e] = 0.f;
         ak[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (k0 + e < nrec) {
-          const float* r = rec + ((int64_t)s_rec[k0 + e] * hq + h) * (D + 4);
+        if (k < nrec) {
+          const float* r = rec + ((int64_t)s_rec[k] * hq + h) * (D + 4);
           mk[e] = r[D];
           lk[e] = r[D + 1];
           ak[e] = *reinterpret_cast<const float4*>(r + d4);
@@ -739,12 +748,29 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(T* __restrict__ out, con
         M = Mn;
       }
     }
-    const float inv = 1.f / L;
-    T* dst = orow + h * D + d4;
-    dst[0] = DT<T>::from_f(o.x * inv);
-    dst[1] = DT<T>::from_f(o.y * inv);
-    dst[2] = DT<T>::from_f(o.z * inv);
-    dst[3] = DT<T>::from_f(o.w * inv);
+    for (int off = 1; off < parts; off <<= 1) {      // lanes of one slice are adjacent
+      const float Mo = __shfl_xor_sync(FULL_MASK, M, off);
+      const float Lo = __shfl_xor_sync(FULL_MASK, L, off);
+      const float ox = __shfl_xor_sync(FULL_MASK, o.x, off), oy = __shfl_xor_sync(FULL_MASK, o.y, off);
+      const float oz = __shfl_xor_sync(FULL_MASK, o.z, off), ow = __shfl_xor_sync(FULL_MASK, o.w, off);
+      const float Mn = fmaxf(M, Mo);
+      const float ca = M == -INFINITY ? 0.f : exp2f(M - Mn);
+      const float cb = Mo == -INFINITY ? 0.f : exp2f(Mo - Mn);
+      L = L * ca + Lo * cb;
+      o.x = o.x * ca + ox * cb;
+      o.y = o.y * ca + oy * cb;
+      o.z = o.z * ca + oz * cb;
+      o.w = o.w * ca + ow * cb;
+      M = Mn;
+    }
+    if (live && part == 0) {
+      const float inv = 1.f / L;
+      T* dst = orow + h * D + d4;
+      dst[0] = DT<T>::from_f(o.x * inv);
+      dst[1] = DT<T>::from_f(o.y * inv);
+      dst[2] = DT<T>::from_f(o.z * inv);
+      dst[3] = DT<T>::from_f(o.w * inv);
+    }
   }
 }
 

@@ -180,13 +180,21 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- setup
-def build_step(cfg, device, path, window=0, extras=False):
+def shared_prefix_of(cfg):
+    """Tokens every row of a workload shares (nanochat's cloned prefill), else 0."""
+    return int(cfg.ctx_args[0]) if cfg.table_kind == "shared_prefix" else 0
+
+
+def build_step(cfg, device, path, window=0, extras=False, shared_prefix=None):
     import paged_kv_decode_store_gb300 as pk
     w = workloads.make_workload(cfg, device=device)
     lay = w.layout
     kc, vc = w.cache[0, lay.layer], w.cache[1, lay.layer]
+    if shared_prefix is None:
+        shared_prefix = 0 if window else shared_prefix_of(cfg)
     step = pk.DecodeStep(kc, vc, lay.num_seqs, cfg.num_q_heads, lay.max_blocks_per_seq, lay.max_context_len,
-                         cfg.vocab, w.logits.dtype, w.scale, path=path, window=window, extras=extras)
+                         cfg.vocab, w.logits.dtype, w.scale, path=path, window=window, extras=extras,
+                         shared_prefix_len=shared_prefix)
     host = {
         "q": w.q, "k_new": w.k_new, "v_new": w.v_new,
         "block_tables": torch.from_numpy(lay.block_tables).to(device),
@@ -227,9 +235,7 @@ def time_attention(step, flush, steps, stream):
     import paged_kv_decode_store_gb300 as pk
 
     def call():
-        pk.paged_decode_attention(step.q, step.k_cache, step.v_cache, step.block_tables, step.context_lens,
-                                  step.max_context_len, step.scale, out=step.out, workspace=step.workspace,
-                                  err=step.err, path=step.path, window=step.window)
+        step.enqueue_attention()
 
     g = getattr(step, "_attn_graph", None)
     if g is None:
@@ -1168,7 +1174,19 @@ def measure_config(cfg, dev, path, args, flush, stream, local, peak):
     a_gbs = nbytes["attention"] / (a_med * 1e-3) / 1e9
     s_gbs = nbytes["step"] / (s_med * 1e-3) / 1e9
     traffic = recorded_traffic(cfg.name, nbytes["attention"])
+    plain_us = None
+    if step.shared_prefix_len:
+        # the same call through the plain kernel, which reads the prefix once per row
+        w2, step2, _ = build_step(cfg, dev, path, shared_prefix=0)
+        step2.enqueue()
+        time_attention(step2, flush, 3, stream)
+        plain_us = 1e3 * statistics.median(time_attention(step2, flush, n, stream))
+        del w2, step2
     res = {"workload": cfg.description, "timings": n,
+           "attention_call": ("pkvd_paged_decode_attention_prefix (shared prefix of "
+                              f"{step.shared_prefix_len} tokens)") if step.shared_prefix_len
+                             else "pkvd_paged_decode_attention",
+           "attention_plain_kernel_us": plain_us,
            "attention_us": 1e3 * a_med, "attention_bytes": nbytes["attention"], "attention_gbs": a_gbs,
            "attention_frac": a_gbs / peak,
            "traffic": traffic and traffic["bytes"], "traffic_source": traffic and traffic["source"],

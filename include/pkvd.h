@@ -244,6 +244,44 @@ pkvd_status pkvd_paged_decode_attention_window(void* out, const void* q, const p
                                                void* stream, int32_t* err_flag, int32_t path);
 
 /*
+ * pkvd_decode_prefix_workspace_bytes -- workspace bytes of
+ * pkvd_paged_decode_attention_prefix for these sizes (never less than
+ * pkvd_decode_workspace_bytes for the same call; sm_count <= 0: the current
+ * device's).  Host only.
+ */
+pkvd_status pkvd_decode_prefix_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                               int32_t head_dim, int32_t max_context_len, int32_t prefix_len,
+                                               int32_t sm_count, size_t* bytes);
+
+/*
+ * pkvd_paged_decode_attention_prefix -- the same attention as
+ * pkvd_paged_decode_attention for a batch whose rows share their first
+ * prefix_len cached tokens: nanochat "04 · Engine 推理与工具调用", sections
+ * 2-3, prefills a prompt once and clones its cache N ways, so every row's
+ * first prefix_len / block_size block-table entries name the same physical
+ * blocks.  Those blocks are read once per group of up to 16 / G rows (G
+ * query heads per KV head), every query of the group applied to each staged
+ * tile, instead of once per row.
+ * Requirements: prefix_len a multiple of block_size (0: no sharing); every
+ *         row's context longer than prefix_len (the token decoded now is the
+ *         row's own; a row that is not longer sets PKVD_ERR_CONTEXT and its
+ *         output is undefined); the shared entries equal in every row's
+ *         table (the prefix is read through row 0's table; this is not
+ *         checked).
+ * The shared-prefix kernel runs for 16-bit caches with 8 KV heads of 64 or
+ * 128 (the tensor-core consumer), at least two rows and no more row groups
+ * than partition CTAs; any other call gives the same result through the
+ * plain kernel.  Workspace: pkvd_decode_prefix_workspace_bytes.  Same input
+ * contract, status codes and device errors as pkvd_paged_decode_attention.
+ */
+pkvd_status pkvd_paged_decode_attention_prefix(void* out, const void* q, const pkvd_cache* cache,
+                                               const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                               const int32_t* context_lens, int32_t max_context_len,
+                                               int32_t num_seqs, int32_t num_q_heads, float scale,
+                                               int32_t prefix_len, void* workspace, size_t workspace_bytes,
+                                               void* stream, int32_t* err_flag);
+
+/*
  * pkvd_paged_decode_attention_noalloc -- the same attention as
  * pkvd_paged_decode_attention (same arguments without the workspace pair,
  * same results and errors), for callers that cannot allocate device memory

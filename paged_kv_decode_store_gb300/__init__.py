@@ -26,6 +26,7 @@ from .block_manager import BlockManager  # noqa: F401
 
 __all__ = ["BlockManager", "copy_blocks", "slot_mapping", "kv_store", "kv_store_paged", "kv_store_prefill",
            "prefill_attention", "sample_ex", "pack_mask", "paged_decode_attention", "decode_workspace_bytes",
+           "paged_decode_attention_prefix", "decode_prefix_workspace_bytes",
            "sample", "DecodeStep", "PkvdError", "lib"]
 
 
@@ -143,6 +144,35 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         ptr(out), ptr(q), ctypes.byref(c), ptr(block_tables), block_tables.shape[1],
         ptr(context_lens), max_context_len, B, Hq, ctypes.c_float(scale), ptr(workspace),
         workspace.numel() * workspace.element_size(), stream_handle(stream, q), _err_ptr(err), path))
+    return out
+
+
+def decode_prefix_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                                  max_context_len: int, prefix_len: int, sm_count: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    check(lib().pkvd_decode_prefix_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                                                   prefix_len, sm_count, ctypes.byref(n)))
+    return int(n.value)
+
+
+def paged_decode_attention_prefix(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                  block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                  max_context_len: int, scale: float, prefix_len: int,
+                                  out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                                  err: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """paged_decode_attention for rows whose first prefix_len cached tokens are
+    the same blocks in every row's table (read once per group of rows)."""
+    B, Hq, D = q.shape
+    c = cache_desc(k_cache, v_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = decode_prefix_workspace_bytes(B, Hq, k_cache.shape[2], D, max_context_len, prefix_len)
+        workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    check(lib().pkvd_paged_decode_attention_prefix(
+        ptr(out), ptr(q), ctypes.byref(c), ptr(block_tables), block_tables.shape[1], ptr(context_lens),
+        max_context_len, B, Hq, ctypes.c_float(scale), prefix_len, ptr(workspace),
+        workspace.numel() * workspace.element_size(), stream_handle(stream, q), _err_ptr(err)))
     return out
 
 

@@ -18,7 +18,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpkvd.so")
 
 SOURCES = ["api.cu", "api_noalloc.cu", "store.cu", "attention.cu", "attention_f32.cu", "attention_f16.cu",
-           "attention_bf16.cu", "sampler.cu", "sampler512.cu", "prefill.cu", "prefill_tc.cu", "prefill_fma.cu", "block_manager.cpp"]
+           "attention_bf16.cu", "attention_prefix.cu", "sampler.cu", "sampler512.cu", "prefill.cu", "prefill_tc.cu", "prefill_fma.cu", "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                 "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

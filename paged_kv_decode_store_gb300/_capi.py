@@ -71,6 +71,11 @@ SIGNATURES = {
     "pkvd_paged_decode_attention_window": (c_int32, [c_void_p, c_void_p, ctypes.POINTER(PkvdCache), c_void_p,
                                                      c_int32, c_void_p, c_int32, c_int32, c_int32, c_float,
                                                      c_int32, c_void_p, c_size_t, c_void_p, c_void_p, c_int32]),
+    "pkvd_decode_prefix_workspace_bytes": (c_int32, [c_int32, c_int32, c_int32, c_int32, c_int32, c_int32, c_int32,
+                                                     ctypes.POINTER(c_size_t)]),
+    "pkvd_paged_decode_attention_prefix": (c_int32, [c_void_p, c_void_p, ctypes.POINTER(PkvdCache), c_void_p, c_int32,
+                                                     c_void_p, c_int32, c_int32, c_int32, c_float, c_int32, c_void_p,
+                                                     c_size_t, c_void_p, c_void_p]),
     "pkvd_paged_decode_attention_noalloc": (c_int32, [c_void_p, c_void_p, ctypes.POINTER(PkvdCache), c_void_p,
                                                       c_int32, c_void_p, c_int32, c_int32, c_int32, c_float,
                                                       c_void_p, c_void_p]),

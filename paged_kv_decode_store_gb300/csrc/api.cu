@@ -263,18 +263,10 @@ pkvd_status attention_validate(void* out, const void* q, const pkvd_cache* cache
 extern "C" {
 
 namespace {
-pkvd_status attention_call(void* out, const void* q, const pkvd_cache* cache, const int32_t* block_tables,
-                           int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t max_context_len,
-                           int32_t num_seqs, int32_t num_q_heads, float scale, int32_t window, void* workspace,
-                           size_t workspace_bytes, void* stream, int32_t* err_flag, int32_t path) {
-  int grid = 0;
-  size_t need = 0;
-  const pkvd_status vs = attention_validate(out, q, cache, block_tables, max_blocks_per_seq, context_lens,
-                                            max_context_len, num_seqs, num_q_heads, scale, window, &path, &grid,
-                                            &need);
-  if (vs != PKVD_OK || num_seqs == 0) return vs;
-  if (!workspace || workspace_bytes < need) return PKVD_WORKSPACE_TOO_SMALL;
-  if (!aligned16(workspace)) return PKVD_UNSUPPORTED_SHAPE;
+AttnArgs attn_args(void* out, const void* q, const pkvd_cache* cache, const int32_t* block_tables,
+                   int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t max_context_len, int32_t num_seqs,
+                   int32_t num_q_heads, float scale, int32_t window, void* workspace, int32_t* err_flag, int grid,
+                   int32_t path) {
   AttnArgs a;
   a.out = out;
   a.q = q;
@@ -300,6 +292,23 @@ pkvd_status attention_call(void* out, const void* q, const pkvd_cache* cache, co
   a.grid = grid;
   a.path = path;
   a.window = window > 0 ? window : 0;
+  return a;
+}
+
+pkvd_status attention_call(void* out, const void* q, const pkvd_cache* cache, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t max_context_len,
+                           int32_t num_seqs, int32_t num_q_heads, float scale, int32_t window, void* workspace,
+                           size_t workspace_bytes, void* stream, int32_t* err_flag, int32_t path) {
+  int grid = 0;
+  size_t need = 0;
+  const pkvd_status vs = attention_validate(out, q, cache, block_tables, max_blocks_per_seq, context_lens,
+                                            max_context_len, num_seqs, num_q_heads, scale, window, &path, &grid,
+                                            &need);
+  if (vs != PKVD_OK || num_seqs == 0) return vs;
+  if (!workspace || workspace_bytes < need) return PKVD_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return PKVD_UNSUPPORTED_SHAPE;
+  const AttnArgs a = attn_args(out, q, cache, block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                               num_seqs, num_q_heads, scale, window, workspace, err_flag, grid, path);
   return from_cuda(launch_attention(a, static_cast<cudaStream_t>(stream)));
 }
 }  // namespace
@@ -323,6 +332,51 @@ pkvd_status pkvd_paged_decode_attention_window(void* out, const void* q, const p
   if (window < 0) return PKVD_INVALID_ARG;
   return attention_call(out, q, cache, block_tables, max_blocks_per_seq, context_lens, max_context_len, num_seqs,
                         num_q_heads, scale, window, workspace, workspace_bytes, stream, err_flag, path);
+}
+
+pkvd_status pkvd_decode_prefix_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                               int32_t head_dim, int32_t max_context_len, int32_t prefix_len,
+                                               int32_t sm_count, size_t* bytes) {
+  if (!bytes || num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||
+      prefix_len < 0)
+    return PKVD_INVALID_ARG;
+  if (sm_count <= 0) sm_count = device_sm_count();
+  if (sm_count <= 0) return PKVD_CUDA_ERROR;
+  const int grid = attention_grid(num_seqs, max_context_len, sm_count);
+  const size_t plain = attention_workspace_bytes(num_seqs, num_q_heads, head_dim, grid);
+  const size_t pre = prefix_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, grid, prefix_len);
+  *bytes = plain > pre ? plain : pre;
+  return PKVD_OK;
+}
+
+pkvd_status pkvd_paged_decode_attention_prefix(void* out, const void* q, const pkvd_cache* cache,
+                                               const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                               const int32_t* context_lens, int32_t max_context_len,
+                                               int32_t num_seqs, int32_t num_q_heads, float scale,
+                                               int32_t prefix_len, void* workspace, size_t workspace_bytes,
+                                               void* stream, int32_t* err_flag) {
+  if (prefix_len < 0) return PKVD_INVALID_ARG;
+  int32_t path = PKVD_PATH_AUTO;
+  int grid = 0;
+  size_t need = 0;
+  const pkvd_status vs = attention_validate(out, q, cache, block_tables, max_blocks_per_seq, context_lens,
+                                            max_context_len, num_seqs, num_q_heads, scale, 0, &path, &grid, &need);
+  if (vs != PKVD_OK) return vs;
+  if (prefix_len % cache->block_size) return PKVD_INVALID_ARG;      // whole blocks are shared
+  if (num_seqs == 0) return PKVD_OK;
+  const bool usable = path == PKVD_PATH_MMA && grid > 0 &&
+                      prefix_path_usable(cache->dtype, cache->head_dim, cache->num_kv_heads, num_q_heads, num_seqs,
+                                         grid, prefix_len, 0);
+  if (!usable)   // the same result from the plain kernel
+    return attention_call(out, q, cache, block_tables, max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                          num_q_heads, scale, 0, workspace, workspace_bytes, stream, err_flag, path);
+  const size_t need_p = prefix_workspace_bytes(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim, grid,
+                                               prefix_len);
+  if (!workspace || workspace_bytes < need_p) return PKVD_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return PKVD_UNSUPPORTED_SHAPE;
+  const AttnArgs a = attn_args(out, q, cache, block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                               num_seqs, num_q_heads, scale, 0, workspace, err_flag, grid, path);
+  return from_cuda(launch_attention_prefix(a, prefix_len, static_cast<cudaStream_t>(stream)));
 }
 
 pkvd_status pkvd_paged_decode_attention(void* out, const void* q, const pkvd_cache* cache,

@@ -48,39 +48,45 @@ int attention_default_path(int dtype, int head_dim, int num_kv_heads, int group)
   return 0;
 }
 
+PartParams part_params(const AttnArgs& a, float* rec) {
+  const int esz = elem_bytes(a.dtype);
+  PartParams pp;
+  pp.out = a.out;
+  pp.q = a.q;
+  pp.k_base = static_cast<const uint8_t*>(a.k_base);
+  pp.v_base = static_cast<const uint8_t*>(a.v_base);
+  pp.block_stride = a.block_stride;
+  pp.token_stride = a.token_stride;
+  pp.head_stride = a.head_stride;
+  pp.num_blocks = a.num_blocks;
+  pp.block_size = a.block_size;
+  pp.hkv = a.num_kv_heads;
+  pp.hq = a.num_q_heads;
+  pp.G = a.num_q_heads / a.num_kv_heads;
+  pp.tables = a.block_tables;
+  pp.max_blocks = a.max_blocks_per_seq;
+  pp.ctx = a.context_lens;
+  const long long cap = (long long)a.max_blocks_per_seq * a.block_size;
+  pp.ctx_cap = (int)(cap < a.max_context_len ? cap : a.max_context_len);
+  pp.window = a.window;
+  pp.num_seqs = a.num_seqs;
+  pp.scale_log2 = a.scale * 1.4426950408889634f;
+  pp.rec = rec;
+  pp.err = a.err;
+  pp.stages = stage_count(a.dtype, a.head_dim, a.num_kv_heads);
+  pp.row_bytes = a.num_kv_heads * a.head_dim * esz;
+  pp.rowb = pp.row_bytes + 16;
+  pp.rows_contig = a.head_stride == a.head_dim ? 1 : 0;
+  pp.active_warps = a.num_kv_heads == 16 ? kConsumerWarps : a.num_kv_heads;
+  return pp;
+}
+
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   const int esz = elem_bytes(a.dtype);
   const int G = a.num_q_heads / a.num_kv_heads;
   float* rec = static_cast<float*>(a.workspace);
   if (a.grid > 0) {
-    PartParams pp;
-    pp.out = a.out;
-    pp.q = a.q;
-    pp.k_base = static_cast<const uint8_t*>(a.k_base);
-    pp.v_base = static_cast<const uint8_t*>(a.v_base);
-    pp.block_stride = a.block_stride;
-    pp.token_stride = a.token_stride;
-    pp.head_stride = a.head_stride;
-    pp.num_blocks = a.num_blocks;
-    pp.block_size = a.block_size;
-    pp.hkv = a.num_kv_heads;
-    pp.hq = a.num_q_heads;
-    pp.G = G;
-    pp.tables = a.block_tables;
-    pp.max_blocks = a.max_blocks_per_seq;
-    pp.ctx = a.context_lens;
-    const long long cap = (long long)a.max_blocks_per_seq * a.block_size;
-    pp.ctx_cap = (int)(cap < a.max_context_len ? cap : a.max_context_len);
-    pp.window = a.window;
-    pp.num_seqs = a.num_seqs;
-    pp.scale_log2 = a.scale * 1.4426950408889634f;
-    pp.rec = rec;
-    pp.err = a.err;
-    pp.stages = stage_count(a.dtype, a.head_dim, a.num_kv_heads);
-    pp.row_bytes = a.num_kv_heads * a.head_dim * esz;
-    pp.rowb = pp.row_bytes + 16;
-    pp.rows_contig = a.head_stride == a.head_dim ? 1 : 0;
-    const int hpw = a.num_kv_heads == 16 ? 2 : 1;
+    PartParams pp = part_params(a, rec);    const int hpw = a.num_kv_heads == 16 ? 2 : 1;
     pp.active_warps = hpw == 2 ? kConsumerWarps : a.num_kv_heads;
     const size_t smem = smem_header_bytes() + (size_t)pp.stages * 2 * kChunk * pp.rowb;
     const int gmax = group_bound(G);

@@ -69,6 +69,10 @@ struct PartParams {
   int active_warps;    // consumer warps that own heads
 };
 
+// The partition kernel's parameters for a call (attention.cu); `rec` is the
+// record area of the workspace.
+PartParams part_params(const AttnArgs& a, float* rec);
+
 // First attended position of a context of c tokens: the newest `window`
 // positions with a sliding window (window > 0), else 0.
 __device__ __forceinline__ int window_start(int c, int window) { return (window > 0 && c > window) ? c - window : 0; }

@@ -47,6 +47,14 @@ size_t attention_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, in
 bool attention_path_supported(int path, int dtype, int head_dim, int num_kv_heads, int group);
 int attention_default_path(int dtype, int head_dim, int num_kv_heads, int group);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
+// Rows sharing their first prefix_len cached tokens (attention_prefix.cu):
+// whether the shared-prefix kernel takes such a call, its workspace, and the
+// launch (partition + merge).
+bool prefix_path_usable(int dtype, int head_dim, int num_kv_heads, int num_q_heads, int num_seqs, int grid,
+                        int prefix_len, int window);
+size_t prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int grid,
+                              int prefix_len);
+cudaError_t launch_attention_prefix(const AttnArgs& a, int prefix_len, cudaStream_t stream);
 // Host-side checks of a decode attention call (api.cu), shared by every
 // attention entry point: resolves PKVD_PATH_AUTO in *path and, for a call
 // with rows, gives the partition grid and the workspace bytes it needs.

@@ -10,6 +10,8 @@ buffers, replay.
 
 Step order (all library kernels):
     kv_store_paged (slot mapping + store) -> paged_decode_attention (partition + merge) -> sample
+(paged_decode_attention_prefix instead when the rows share a cached prefix,
+nanochat's one prefill cloned N ways).
 """
 from __future__ import annotations
 
@@ -24,7 +26,8 @@ class DecodeStep:
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, num_seqs: int,
                  num_q_heads: int, max_blocks_per_seq: int, max_context_len: int,
                  vocab: int, logits_dtype: torch.dtype, scale: float,
-                 path: int = _capi.PATH_AUTO, window: int = 0, extras: bool = False):
+                 path: int = _capi.PATH_AUTO, window: int = 0, extras: bool = False,
+                 shared_prefix_len: int = 0):
         dev = k_cache.device
         nb, bs, Hkv, D = k_cache.shape
         B, Hq = num_seqs, num_q_heads
@@ -34,6 +37,11 @@ class DecodeStep:
         self.scale = float(scale)
         self.path = path
         self.window = int(window)        # > 0: sliding-window attention over the newest positions
+        # > 0: every row's first shared_prefix_len cached tokens are the same
+        # blocks (one prefill cloned N ways); attention reads them once per row group
+        self.shared_prefix_len = int(shared_prefix_len)
+        if self.shared_prefix_len and self.window:
+            raise ValueError("a shared prefix and a sliding window do not combine")
         dt = k_cache.dtype
         # Per-step inputs and outputs live in two byte arenas (256-byte aligned
         # views), so a host-staged step moves each side with one copy.
@@ -68,8 +76,13 @@ class DecodeStep:
         self.logits = torch.zeros(B, vocab, dtype=logits_dtype, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         nbytes = ctypes.c_size_t(0)
-        _capi.check(_capi.lib().pkvd_decode_workspace_bytes(B, Hq, D, max_context_len, 0,
-                                                            ctypes.byref(nbytes)))
+        if self.shared_prefix_len:
+            _capi.check(_capi.lib().pkvd_decode_prefix_workspace_bytes(B, Hq, Hkv, D, max_context_len,
+                                                                       self.shared_prefix_len, 0,
+                                                                       ctypes.byref(nbytes)))
+        else:
+            _capi.check(_capi.lib().pkvd_decode_workspace_bytes(B, Hq, D, max_context_len, 0,
+                                                                ctypes.byref(nbytes)))
         self.workspace = torch.zeros(max(int(nbytes.value), 16), dtype=torch.uint8, device=dev)
         self.cache = _capi.cache_desc(k_cache, v_cache)
         self.graph = None
@@ -88,6 +101,20 @@ class DecodeStep:
         _capi.check(L.pkvd_kv_store_paged(p(self.k_new), p(self.v_new), p(self.block_tables),
                                           self.block_tables.shape[1], p(self.context_lens), self.B,
                                           p(self.slots), ctypes.byref(self.cache), s, p(self.err)))
+        self.enqueue_attention(L, s)
+
+    def enqueue_attention(self, L=None, s=None) -> None:
+        """The attention call of the step alone (on the current stream by default)."""
+        L = L or _capi.lib()
+        s = s if s is not None else _capi.stream_handle(None, self.q)
+        p = _capi.ptr
+        if self.shared_prefix_len:
+            _capi.check(L.pkvd_paged_decode_attention_prefix(
+                p(self.out), p(self.q), ctypes.byref(self.cache), p(self.block_tables),
+                self.block_tables.shape[1], p(self.context_lens), self.max_context_len, self.B, self.Hq,
+                ctypes.c_float(self.scale), self.shared_prefix_len, p(self.workspace), self.workspace.numel(), s,
+                p(self.err)))
+            return
         _capi.check(L.pkvd_paged_decode_attention_window(
             p(self.out), p(self.q), ctypes.byref(self.cache), p(self.block_tables),
             self.block_tables.shape[1], p(self.context_lens), self.max_context_len, self.B, self.Hq,

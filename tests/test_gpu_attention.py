@@ -253,3 +253,87 @@ def test_sliding_window_full_size_sampled_rows(name):
         assert err == 0
         o = out[torch.tensor(rows, device=DEV)].double().cpu().numpy()
         check_attention(o, ref, w.q.dtype, pairs=pairs)
+
+
+# ---------------------------------------------------------------- shared prefix
+def prefix_variants():
+    """Batches whose rows share their first `prefix` cached tokens (the same
+    physical blocks at the start of every table), with the prefix length."""
+    nano = configs.NANOCHAT
+    return {
+        "nanochat": (nano, 1024),
+        "g6_head128": (nano.scaled(num_q_heads=48, num_kv_heads=8, ctx_args=(512, 200)), 512),
+        "g8_rows12": (nano.scaled(num_seqs=12, num_q_heads=64, num_kv_heads=8, ctx_args=(256, 300)), 256),
+        "g2_head64_f16": (nano.scaled(num_q_heads=16, num_kv_heads=8, head_dim=64, dtype="f16",
+                                      ctx_args=(160, 40)), 160),
+        "one_block_prefix": (nano.scaled(num_seqs=5, ctx_args=(16, 70)), 16),
+        "block32": (nano.scaled(num_seqs=7, block_size=32, ctx_args=(320, 90)), 320),
+        "many_rows": (nano.scaled(num_seqs=64, ctx_args=(128, 20)), 128),
+    }
+
+
+def run_prefix_attention(pk, w, prefix, workspace_fill=None):
+    lay = w.layout
+    cache = w.cache.to(DEV)
+    kc, vc = cache[0, lay.layer], cache[1, lay.layer]
+    tables = torch.from_numpy(lay.block_tables).to(DEV)
+    ctx = torch.from_numpy(lay.context_lens).to(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    slots = pk.slot_mapping(tables, ctx, w.cfg.block_size, lay.num_blocks, err=err)
+    pk.kv_store(w.k_new.to(DEV), w.v_new.to(DEV), slots, kc, vc, err=err)
+    ws = None
+    if workspace_fill is not None:
+        n = pk.decode_prefix_workspace_bytes(lay.num_seqs, w.cfg.num_q_heads, w.cfg.num_kv_heads, w.cfg.head_dim,
+                                             lay.max_context_len, prefix)
+        ws = torch.full((n,), workspace_fill, dtype=torch.uint8, device=DEV)
+    out = pk.paged_decode_attention_prefix(w.q.to(DEV), kc, vc, tables, ctx, lay.max_context_len, w.scale, prefix,
+                                           workspace=ws, err=err)
+    torch.cuda.synchronize()
+    return out, err.item()
+
+
+@pytest.mark.parametrize("name", list(prefix_variants()))
+def test_shared_prefix_attention_matches_oracle(name):
+    """Every row against the oracle's plain attention over its own table (the
+    prefix blocks are shared in the tables, so both read the same rows)."""
+    pk = require_gpu()
+    cfg, prefix = prefix_variants()[name]
+    w = workloads.make_workload(cfg)
+    lay = w.layout
+    nb = prefix // cfg.block_size
+    assert (lay.block_tables[:, :nb] == lay.block_tables[0, :nb]).all()
+    assert (lay.context_lens > prefix).all()
+    kf, vf, _ = oracle_store_f64(w)
+    ref = oracle.attention.decode_attention(w.q.double().numpy(), kf, vf, lay.block_tables, lay.context_lens, w.scale)
+    out, err = run_prefix_attention(pk, w, prefix, workspace_fill=0x7F)      # the workspace needs no clearing
+    assert err == 0
+    check_attention(out.double().cpu().numpy(), ref, w.q.dtype)
+    again, _ = run_prefix_attention(pk, w, prefix)
+    assert torch.equal(out, again)
+
+
+@pytest.mark.parametrize("name,prefix", [("tiny", 16), ("qwen3_small", 256), ("nanochat", 0)])
+def test_shared_prefix_call_falls_back_to_the_plain_kernel(name, prefix):
+    """fp32 caches, 16 KV heads, or no prefix: the same result as the plain call."""
+    pk = require_gpu()
+    cfg = small_variants()[name]
+    w = workloads.make_workload(cfg)
+    lay = w.layout
+    plain, err = run_attention(pk, w, pk.PATH_AUTO)
+    assert err == 0
+    pre, err = run_prefix_attention(pk, w, prefix)
+    assert err == 0
+    assert torch.equal(plain, pre)
+
+
+def test_shared_prefix_rejects_partial_blocks_and_flags_short_rows():
+    pk = require_gpu()
+    cfg, prefix = prefix_variants()["one_block_prefix"]
+    w = workloads.make_workload(cfg)
+    with pytest.raises(pk.PkvdError):
+        run_prefix_attention(pk, w, 8)                       # not a whole block
+    # a row whose context does not reach past the prefix is flagged
+    lay = w.layout
+    lay.context_lens[2] = prefix
+    _, err = run_prefix_attention(pk, w, prefix)
+    assert err & pk.ERR_CONTEXT

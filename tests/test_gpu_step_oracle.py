@@ -91,14 +91,15 @@ def _oracle_steps(w, steps):
     return res
 
 
-def _run_steps(w, steps, host_staged):
+def _run_steps(w, steps, host_staged, shared_prefix=0):
     """Replay the captured step twice on a fresh device copy of the cache."""
     pk = require_gpu()
     lay, cfg = w.layout, w.cfg
     cache = w.cache.to(DEV)
     kc, vc = cache[0, lay.layer], cache[1, lay.layer]
     step = pk.DecodeStep(kc, vc, lay.num_seqs, cfg.num_q_heads, lay.max_blocks_per_seq,
-                         lay.max_blocks_per_seq * cfg.block_size, cfg.vocab, w.logits.dtype, w.scale)
+                         lay.max_blocks_per_seq * cfg.block_size, cfg.vocab, w.logits.dtype, w.scale,
+                         shared_prefix_len=shared_prefix)
     got = []
     if host_staged:
         h = step.host_buffers()
@@ -167,4 +168,15 @@ def test_replayed_step_matches_oracle(name, host_staged):
     if name != "grok1":                                   # grok1 rows fill their tables: nothing can move
         assert moved > 0
     got = _run_steps(w, steps, host_staged)
+    _compare(w, got, ref, steps)
+
+
+@pytest.mark.parametrize("host_staged", [False, True], ids=["device_graph", "host_staged_graph"])
+def test_replayed_step_with_shared_prefix_matches_oracle(host_staged):
+    """nanochat's rows share a 1,024-token prefill: the step's attention runs
+    the shared-prefix kernel, with the same results as the oracle's plain
+    attention (both steps; the second moves rows one token on)."""
+    require_gpu()
+    w, steps, moved, ref = _case("nanochat")
+    got = _run_steps(w, steps, host_staged, shared_prefix=w.cfg.ctx_args[0])
     _compare(w, got, ref, steps)

@@ -1214,9 +1214,7 @@ def run_profile_attention(args):
     w, step, _ = build_step(cfg, dev, pk.PATH_AUTO)
     step.enqueue()
     for _ in range(args.steps):
-        pk.paged_decode_attention(step.q, step.k_cache, step.v_cache, step.block_tables, step.context_lens,
-                                  step.max_context_len, step.scale, out=step.out, workspace=step.workspace,
-                                  err=step.err)
+        step.enqueue_attention()          # the step's own attention call (shared-prefix where the rows share one)
     torch.cuda.synchronize()
     if int(step.err.item()):
         raise RuntimeError(f"device error flag {int(step.err.item())}")

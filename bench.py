@@ -4,22 +4,33 @@ A step is the whole hot path for one layer of one decode batch:
 slot mapping -> KV store -> paged decode attention (partition + LSE merge)
 -> fused sampler, replayed as one CUDA graph.  Inputs are seeded synthetic
 tensors with the named workload's shapes, resident in HBM when timing
-starts; L2 is flushed before every timed step, outside the timed events (a
-512 MB write, then a 512 MB read so the timed kernels find clean lines).
+starts; L2 is flushed before every timed step or call, outside the timed
+events (a 512 MB write, then a 512 MB read so the timed kernels find clean
+lines).  The headline workload is the long-context batch (256 rows, 8.3 GB
+of K/V per step); grok1, qwen3 and nanochat are timed in the same run under
+`per_config`.
 
 Reported (one JSON line on rank 0):
-  value        algorithmic HBM GB/s of the step (bytes the method must move
-               / step time), unit GB/s; tokens_per_s = batch / step time
-  roofline     the attention call timed alone with CUDA events, against the
-               measured HBM copy peak
-  e2e          the same metric through the public API with host buffers:
-               pinned host -> device copy of the step's inputs, the step, and
-               device -> host copy of its outputs, all inside the timing
-  cpu_baseline the float64 oracle on a bounded sample, on every host core
-               (single-threaded processes), with the one-thread figure beside it
+  value        decode-attention HBM GB/s: the attention's algorithmic bytes
+               over the median of 100 timings of the attention call alone
+               (partition + merge); ms_per_step and tokens_per_s are the whole
+               step over the --steps timed steps, `step` its median and its
+               fraction of the roofline
+  roofline     the attention call against the measured HBM copy peak, with
+               the DRAM traffic recorded by ncu for the current kernel sources
+  attention_back_to_back, sampler
+               the attention calls back to back (K/V larger than L2), and the
+               sampler call alone
+  e2e          the attention bytes over the step through the public API with
+               host buffers: pinned host -> device copy of the step's inputs,
+               the step, device -> host copy of its outputs, all timed
+  cpu_baseline the float64 oracle on whole mid-length rows, on every host
+               core (single-threaded processes), with the one-thread figure
+  per_config   the same figures for the other workloads
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config qwen3]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--per-config LIST|none]
     python bench.py --impl reference ...   (the oracle as the reference arm)
+    python bench.py --profile-attention NAME --steps 3   (the command the DRAM captures profile)
 """
 from __future__ import annotations
 

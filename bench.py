@@ -191,9 +191,11 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- setup
-def shared_prefix_of(cfg):
-    """Tokens every row of a workload shares (nanochat's cloned prefill), else 0."""
-    return int(cfg.ctx_args[0]) if cfg.table_kind == "shared_prefix" else 0
+def shared_prefix_of(lay, block_size):
+    """Tokens every row of a batch shares (nanochat's cloned prefill), found
+    from the host block tables as a scheduler would; 0 when none."""
+    from paged_kv_decode_store_gb300 import shared_prefix_len
+    return shared_prefix_len(lay.block_tables, lay.context_lens, block_size)
 
 
 def build_step(cfg, device, path, window=0, extras=False, shared_prefix=None):
@@ -202,7 +204,7 @@ def build_step(cfg, device, path, window=0, extras=False, shared_prefix=None):
     lay = w.layout
     kc, vc = w.cache[0, lay.layer], w.cache[1, lay.layer]
     if shared_prefix is None:
-        shared_prefix = 0 if window else shared_prefix_of(cfg)
+        shared_prefix = 0 if window else shared_prefix_of(lay, cfg.block_size)
     step = pk.DecodeStep(kc, vc, lay.num_seqs, cfg.num_q_heads, lay.max_blocks_per_seq, lay.max_context_len,
                          cfg.vocab, w.logits.dtype, w.scale, path=path, window=window, extras=extras,
                          shared_prefix_len=shared_prefix)

@@ -510,6 +510,16 @@ pkvd_status pkvd_bm_fork(pkvd_block_manager* bm, const int32_t* block_table, int
 /* A sequence ends: every block of its table loses a reference (last first). */
 pkvd_status pkvd_bm_release(pkvd_block_manager* bm, const int32_t* block_table, int32_t num_blocks);
 
+/* The prefix a decode batch shares, for pkvd_paged_decode_attention_prefix:
+ * the longest run of leading table entries that name the same physical
+ * block in every row, counting only blocks that every row holds in full
+ * before its newest token (so every context passes the prefix), in tokens
+ * (a multiple of block_size; 0 for fewer than two rows).  block_tables and
+ * context_lens are HOST arrays ([num_seqs][table_stride], [num_seqs]), as the
+ * scheduler keeps them; nothing is read on the device. */
+pkvd_status pkvd_bm_shared_prefix(const int32_t* block_tables, int32_t num_seqs, int32_t table_stride,
+                                  const int32_t* context_lens, int32_t block_size, int32_t* prefix_tokens);
+
 /*
  * pkvd_copy_blocks -- the device side of copy-on-write: for each i < count,
  * the first rows[i] token rows of block src[i] (K and V, every head) are

@@ -22,11 +22,11 @@ from ._capi import (LIB_PATH, PATH_AUTO, PATH_FMA, PATH_MMA, PATH_TC, ERR_BLOCK_
                     ERR_CONTEXT, ERR_TIMEOUT, PkvdCache, PkvdError, lib, check, dtype_code,
                     stream_handle, cache_desc, ptr)
 from .step import DecodeStep  # noqa: F401
-from .block_manager import BlockManager  # noqa: F401
+from .block_manager import BlockManager, shared_prefix_len  # noqa: F401
 
 __all__ = ["BlockManager", "copy_blocks", "slot_mapping", "kv_store", "kv_store_paged", "kv_store_prefill",
            "prefill_attention", "sample_ex", "pack_mask", "paged_decode_attention", "decode_workspace_bytes",
-           "paged_decode_attention_prefix", "decode_prefix_workspace_bytes",
+           "paged_decode_attention_prefix", "decode_prefix_workspace_bytes", "shared_prefix_len",
            "sample", "DecodeStep", "PkvdError", "lib"]
 
 

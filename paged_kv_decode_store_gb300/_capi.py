@@ -57,6 +57,7 @@ SIGNATURES = {
     "pkvd_bm_append": (c_int32, [c_void_p, c_void_p, c_int32, c_void_p, ctypes.POINTER(c_int32), c_int32,
                                  ctypes.POINTER(c_int32), ctypes.POINTER(c_int32), ctypes.POINTER(c_int32)]),
     "pkvd_bm_fork": (c_int32, [c_void_p, c_void_p, c_int32]),
+    "pkvd_bm_shared_prefix": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_int32, ctypes.POINTER(c_int32)]),
     "pkvd_bm_release": (c_int32, [c_void_p, c_void_p, c_int32]),
     "pkvd_copy_blocks": (c_int32, [ctypes.POINTER(PkvdCache), c_void_p, c_void_p, c_void_p, c_int32, c_void_p,
                                    c_void_p]),

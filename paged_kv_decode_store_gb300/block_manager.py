@@ -87,3 +87,15 @@ class BlockManager:
     def release(self, table) -> None:
         t, tp = _arr(table)
         _capi.check(self._lib.pkvd_bm_release(self._h, tp, len(table)))
+
+
+def shared_prefix_len(block_tables, context_lens, block_size: int) -> int:
+    """Tokens a decode batch shares at the start of every row (whole blocks
+    that are the same physical block in every table and full before each
+    row's newest token), for the shared-prefix attention call.  Host arrays."""
+    t = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32))
+    c = np.ascontiguousarray(np.asarray(context_lens, dtype=np.int32))
+    out = ctypes.c_int32(0)
+    _capi.check(_capi.lib().pkvd_bm_shared_prefix(t.ctypes.data_as(ctypes.c_void_p), t.shape[0], t.shape[1],
+                                                  c.ctypes.data_as(ctypes.c_void_p), block_size, ctypes.byref(out)))
+    return int(out.value)

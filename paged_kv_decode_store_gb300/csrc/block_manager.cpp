@@ -188,6 +188,32 @@ pkvd_status pkvd_bm_fork(pkvd_block_manager* bm, const int32_t* block_table, int
   return PKVD_OK;
 }
 
+pkvd_status pkvd_bm_shared_prefix(const int32_t* block_tables, int32_t num_seqs, int32_t table_stride,
+                                  const int32_t* context_lens, int32_t block_size, int32_t* prefix_tokens) {
+  if (!prefix_tokens || num_seqs < 0 || block_size <= 0 || table_stride < 0) return PKVD_INVALID_ARG;
+  *prefix_tokens = 0;
+  if (num_seqs < 2) return PKVD_OK;
+  if (!block_tables || !context_lens) return PKVD_INVALID_ARG;
+  // whole blocks that every row holds before its newest token, and that are
+  // the same physical block in every row
+  int64_t limit = table_stride;
+  for (int32_t i = 0; i < num_seqs; ++i) {
+    if (context_lens[i] <= 0) return PKVD_OK;
+    const int64_t full = (int64_t)(context_lens[i] - 1) / block_size;
+    if (full < limit) limit = full;
+  }
+  int64_t shared = 0;
+  for (; shared < limit; ++shared) {
+    const int32_t b = block_tables[shared];
+    if (b < 0) break;
+    bool same = true;
+    for (int32_t i = 1; i < num_seqs && same; ++i) same = block_tables[(int64_t)i * table_stride + shared] == b;
+    if (!same) break;
+  }
+  *prefix_tokens = (int32_t)(shared * block_size);
+  return PKVD_OK;
+}
+
 pkvd_status pkvd_bm_release(pkvd_block_manager* bm, const int32_t* block_table, int32_t num_blocks) {
   if (!bm || num_blocks < 0 || (num_blocks > 0 && !block_table)) return PKVD_INVALID_ARG;
   for (int32_t i = 0; i < num_blocks; ++i)

@@ -174,3 +174,44 @@ def test_native_block_manager_rejects_bad_tables():
     with pytest.raises(_capi.PkvdError):
         bm.fork([3])                               # an unreferenced block cannot be cloned
     assert bm.allocate([1] * 20) is None and bm.num_free() == 2
+
+
+def _shared_prefix_brute(tables, ctx, bs):
+    """Longest run of leading blocks equal in every row and full before each
+    row's newest token, by brute force, in tokens."""
+    B = len(tables)
+    if B < 2:
+        return 0
+    best = 0
+    for nb in range(0, min(len(t) for t in tables) + 1):
+        ok = all(int(c) - 1 >= nb * bs for c in ctx) and \
+            all(all(tables[i][j] == tables[0][j] and tables[0][j] >= 0 for i in range(B)) for j in range(nb))
+        if ok:
+            best = nb * bs
+    return best
+
+
+def test_shared_prefix_of_a_batch():
+    """pkvd_bm_shared_prefix against brute force: forked rows share their
+    prompt's blocks, private blocks differ, short rows cap the prefix."""
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_decode_store_gb300 import shared_prefix_len
+    rng = np.random.default_rng(3)
+    for trial in range(200):
+        bs = int(rng.choice([16, 32]))
+        B = int(rng.integers(1, 6))
+        width = int(rng.integers(1, 12))
+        shared = int(rng.integers(0, width + 1))
+        base = rng.permutation(1000)[:width]
+        tables = []
+        for i in range(B):
+            t = base.copy()
+            t[shared:] = rng.permutation(1000)[:width - shared] + 1000 * (i + 1)   # private blocks
+            if rng.random() < 0.2 and width:
+                t[int(rng.integers(0, width))] = -1
+            tables.append(t)
+        ctx = rng.integers(0, width * bs + 1, size=B)
+        got = shared_prefix_len(np.array(tables, dtype=np.int32), ctx.astype(np.int32), bs)
+        want = _shared_prefix_brute([list(t) for t in tables], ctx, bs)
+        assert got == want, (trial, got, want)

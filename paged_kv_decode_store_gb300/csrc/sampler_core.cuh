@@ -180,13 +180,19 @@ __device__ __forceinline__ float ex2_ftz(float x) {
 // E_j = -ln u_j for id j's uniform: word (j mod 4) of Philox4x32-10 at
 // counter (j / 4, offset), u = ((w >> 9) + 1/2) 2^-23, exact in f32 and
 // strictly inside (0, 1), so E_j > 0 (accurate near u = 1, where it is tiny)
-__device__ __forceinline__ float exp_noise(uint64_t seed, uint64_t offset, uint32_t j) {
-  const uint4 ctr = make_uint4(j >> 2, (uint32_t)offset, (uint32_t)(offset >> 32), 0u);
-  const uint4 w4 = philox4x32_10(ctr, make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
-  const uint32_t sel = j & 3u;
-  const uint32_t w = sel == 0 ? w4.x : (sel == 1 ? w4.y : (sel == 2 ? w4.z : w4.w));
+__device__ __forceinline__ float noise_of_word(uint32_t w) {
   const float u = (__uint2float_rn(w >> 9) + 0.5f) * 1.1920928955078125e-07f;   // * 2^-23, exact
   return -logf(u);
+}
+// The four Philox words of ids 4c .. 4c + 3 (one call serves the four).
+__device__ __forceinline__ uint4 noise_words(uint64_t seed, uint64_t offset, uint32_t c) {
+  const uint4 ctr = make_uint4(c, (uint32_t)offset, (uint32_t)(offset >> 32), 0u);
+  return philox4x32_10(ctr, make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+}
+__device__ __forceinline__ float exp_noise(uint64_t seed, uint64_t offset, uint32_t j) {
+  const uint4 w4 = noise_words(seed, offset, j >> 2);
+  const uint32_t sel = j & 3u;
+  return noise_of_word(sel == 0 ? w4.x : (sel == 1 ? w4.y : (sel == 2 ? w4.z : w4.w)));
 }
 
 // Gumbel-max as an exponential race: argmax_j x_j / T - ln(-ln u_j) is
@@ -194,9 +200,12 @@ __device__ __forceinline__ float exp_noise(uint64_t seed, uint64_t offset, uint3
 // above every x_j of the slice) the factor lies in [1, 2^31) for every id
 // that can win.  The packed key makes the smallest race time the largest
 // key, and the lowest id the winner among equal times.  d2 = (m - x) / (T ln 2).
-__device__ __forceinline__ unsigned long long race_key(uint64_t seed, uint64_t offset, uint32_t j, float d2) {
-  const float t = exp_noise(seed, offset, j) * ex2_ftz(d2);
+__device__ __forceinline__ unsigned long long race_key_of(float e, uint32_t j, float d2) {
+  const float t = e * ex2_ftz(d2);
   return ((unsigned long long)(uint32_t)~f32_order_key(t) << 32) | (0xffffffffu - j);
+}
+__device__ __forceinline__ unsigned long long race_key(uint64_t seed, uint64_t offset, uint32_t j, float d2) {
+  return race_key_of(exp_noise(seed, offset, j), j, d2);
 }
 
 // ------------------------------------------------------------ shared state
@@ -1185,7 +1194,45 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sample_kernel(co
         unsigned long long total_u;
         const int first = (int)block_excl_scan_u64((unsigned long long)mine, h.red, total_u);
         const int total = (int)total_u;
-        for (int r0 = 0; r0 < total; r0 += cap) {          // block-uniform
+        // Dense candidates (sampling close to the plain softmax): more than a
+        // quarter of the slice, and more than four per thread (below that one
+        // candidate per thread in parallel is quicker): walk the words instead
+        // of compacting, one Philox call per group of four ids that holds a
+        // candidate (the slice starts on a multiple of 8 ids, so groups never
+        // straddle words), the same uniforms per id.
+        const bool dense = (long long)total * 4 > (long long)n && total > 4 * kSampThreads;
+        if (dense) {
+          for (int v = tid; v < nvec; v += kSampThreads) {
+            const uint32_t cb = pass_bits<T>(sv[v], thr_v2);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const uint32_t hb = (cb >> (4 * half)) & 0xfu;
+              if (!hb) continue;
+              const int j0 = v * 8 + half * 4;
+              const uint4 w4 = noise_words(seed, off, (uint32_t)(lo + j0) >> 2);
+              const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                if (!((hb >> e) & 1u)) continue;
+                const int j = j0 + e;
+                const uint32_t b = bits_at(j);
+                if (keep(j, b)) {
+                  const unsigned long long pk =
+                      race_key_of(noise_of_word(ws[e]), (uint32_t)(lo + j), (mrow - K::value(b)) * l2t);
+                  bestg = pk > bestg ? pk : bestg;
+                }
+              }
+            }
+          }
+          for (int j = rest + tid; j < n; j += kSampThreads) {
+            const uint32_t b = bits_at(j);
+            if (K::key(b) >= thr && keep(j, b)) {
+              const unsigned long long pk = score_of(lo + j, b);
+              bestg = pk > bestg ? pk : bestg;
+            }
+          }
+        }
+        for (int r0 = 0; !dense && r0 < total; r0 += cap) {   // block-uniform
           const int r1 = min(total, r0 + cap);
           if (mine > 0 && first < r1 && first + mine > r0) {
             int kk = first;                                 // list rank of this thread's next candidate

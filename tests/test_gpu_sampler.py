@@ -378,3 +378,51 @@ def test_single_and_multi_wave_launches_match_oracle():
                 if t != ref[i][0] and not sampling_exempt(ref[i][1], float(si.top_p[i])):
                     bad += 1
             assert bad == 0, (copies, c)
+
+
+@pytest.mark.parametrize("dtype,T", [(torch.bfloat16, 1.0), (torch.float16, 2.0), (torch.bfloat16, 0.5)])
+def test_untruncated_draws_match_oracle(dtype, T):
+    """No top-k and no nucleus (the plain temperature softmax): most ids are
+    candidates, so the kernel draws word by word with one Philox call per
+    four ids; the ids still follow the Philox stream id by id."""
+    pk = require_gpu()
+    rng = np.random.default_rng(21)
+    R, V = 96, 6000
+    logits = torch.from_numpy((rng.standard_normal((R, V)) * 2).astype(np.float32)).to(dtype)
+    seeds = rng.integers(0, 2**62, size=R, dtype=np.int64)
+    offs = rng.integers(0, 2**40, size=R, dtype=np.int64)
+    T32 = float(np.float32(T))
+    tok = pk.sample(logits.to(DEV), torch.full((R,), T, device=DEV), torch.zeros(R, dtype=torch.int32, device=DEV),
+                    torch.ones(R, device=DEV), torch.from_numpy(seeds).to(DEV),
+                    torch.from_numpy(offs).to(DEV)).cpu().numpy()
+    x = logits.double().numpy()
+    bad = exempt = 0
+    for i in range(R):
+        ref, info = oracle.sampler.sample_row(x[i], T32, 0, 1.0, int(seeds[i]), int(offs[i]), return_info=True)
+        if int(tok[i]) != ref:
+            if sampling_exempt(info, 1.0):
+                exempt += 1
+            else:
+                bad += 1
+    assert bad == 0 and exempt <= 2
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_chi_square_untruncated_16bit(dtype):
+    pk = require_gpu()
+    rng = np.random.default_rng(8)
+    V, R = 48, 100_000
+    row = torch.from_numpy((rng.standard_normal(V) * 1.2).astype(np.float32)).to(dtype)
+    logits = row.unsqueeze(0).repeat(R, 1).to(DEV)
+    tok = pk.sample(logits, torch.ones(R, device=DEV), torch.zeros(R, dtype=torch.int32, device=DEV),
+                    torch.ones(R, device=DEV), torch.full((R,), 77, dtype=torch.int64, device=DEV),
+                    torch.arange(R, dtype=torch.int64, device=DEV)).cpu().numpy()
+    probs = oracle.sampler.truncated_probs(row.double().numpy(), 1.0, 0, 1.0)
+    counts = np.bincount(tok, minlength=V)
+    expected = probs * R
+    keep = expected >= 5
+    obs = np.append(counts[keep], counts[~keep].sum())
+    exp = np.append(expected[keep], expected[~keep].sum())
+    if exp[-1] == 0:
+        obs, exp = obs[:-1], exp[:-1]
+    assert stats.chisquare(obs, exp).pvalue > 1e-3

@@ -647,6 +647,10 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sample_kernel(co
   const int copy = warp & (kHistCopies - 1);
   const uint32_t* mask_row = a.mask ? a.mask + (int64_t)row_id * a.mask_stride : nullptr;
   const uint64_t seed = a.seeds[row_id], off = a.offsets[row_id];
+  // the row's sampling parameters, read before the slice lands so their
+  // latency hides under the logit copies
+  const float row_T = a.temperature[row_id], row_p = a.top_p[row_id];
+  const int row_k = a.top_k[row_id];
   // the row's cut parameters for the extras kernel (rank 0 writes them)
   auto put_row_info = [&](int flags, uint32_t tau_k, uint32_t kth_k, uint32_t tie_enc, float row_max) {
     if (a.row_info && crank == 0 && tid == 0) {
@@ -730,7 +734,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sample_kernel(co
         kmr = (uint32_t)block_max_u64(mx, h.red);
       }
       cluster_wait();                                   // every peer has started
-      const float Tr = a.temperature[row_id];
+      const float Tr = row_T;
       if (!(Tr > 0.f)) {
         // greedy: this slice's lowest index holding its max key, then one
         // exchange; the packed (key, ~index) max is the row's answer
@@ -763,9 +767,9 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sample_kernel(co
         return;
       }
       const float l2t = 1.4426950408889634f / Tr;
-      const int k = a.top_k[row_id];
+      const int k = row_k;
       const bool topk_on = k > 0 && k < a.V;
-      const float p = a.top_p[row_id];
+      const float p = row_p;
       const bool nucleus_on = p < 1.f;
       const bool need_win = topk_on || nucleus_on;
       const bool need_z = nucleus_on && !topk_on;
@@ -1350,7 +1354,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sample_kernel(co
   best = cluster_scalar<true>(c, best);
   const uint32_t kmax = (uint32_t)(best >> 32);
   const int imax = (int)(0xffffffffu - (uint32_t)(best & 0xffffffffu));
-  const float Tr = a.temperature[row_id];
+  const float Tr = row_T;
   if (!(Tr > 0.f)) {
     if (crank == 0 && tid == 0) a.token_ids[row_id] = imax;
     put_row_info(kRowGreedy, 0u, 0u, 0u, 0.f);
@@ -1361,9 +1365,9 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sample_kernel(co
   const float l2t = 1.4426950408889634f / Tr;
   auto wfix = [&](float x) -> unsigned long long { return fixed_weight(exp2f((x - m) * l2t)); };
 
-  const int k = a.top_k[row_id];
+  const int k = row_k;
   const bool topk_on = k > 0 && k < a.V;
-  const float p = a.top_p[row_id];
+  const float p = row_p;
   const bool nucleus_on = p < 1.f;
   uint32_t kth = 0;          // key of the k-th largest
   long long need_eq = 0, cnt_eq = 0;

@@ -221,6 +221,9 @@ struct SampHdr {
   int sel_aux;
   unsigned long long sel_val;
   unsigned long long zsum;
+  unsigned long long fin_best;           // the row's winning race key (warp 0's combine of the ranks)
+  float fin_mm;                          // the largest rank bound
+  uint32_t fin_tie;                      // the last kept tie over the ranks
 };
 
 struct Ctx {
@@ -695,12 +698,13 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sample_kernel(co
       {
         const int bulk = nvec * 16;
         const int nch = (bulk + kChunkBytes - 1) / kChunkBytes;
+        // thread 0 sets up the barriers and issues every copy before the
+        // CTA-wide barrier, so the requests leave while the other warps of
+        // the CTA are still arriving; the barrier then publishes the
+        // initialised mbarriers to the waiting threads
         if (tid == 0) {
           for (int i = 0; i < nch; ++i) mbar_init(&h.bar[i], 1);
           fence_mbar_init();
-        }
-        __syncthreads();
-        if (tid == 0) {
           for (int i = 0; i < nch; ++i) {
             const int off = i * kChunkBytes;
             const int sz = min(kChunkBytes, bulk - off);
@@ -709,6 +713,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sample_kernel(co
                      (uint32_t)sz, &h.bar[i]);
           }
         }
+        __syncthreads();
         for (int j = rest + tid; j < n; j += kSampThreads)
           slice_smem[j] = (mask_row && !allowed_bit(mask_row, lo + j)) ? neg_inf_value<T>() : row[lo + j];
         const uint8_t* mbytes = mask_row ? reinterpret_cast<const uint8_t*>(mask_row) + (lo >> 3) : nullptr;
@@ -1274,32 +1279,54 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sample_kernel(co
       // log2 units: log2 t + (max - mrow) / (T ln 2).
       const ulonglong2* px = cluster_push(c, crank, bestg,
                                           ((unsigned long long)tie_code(tie_cand) << 32) | __float_as_uint(mrow));
-      // every thread combines the ranks (the result is cluster-uniform)
-      unsigned long long best = 0;
-      uint32_t tie_enc = 0;
-      float mm = __uint_as_float((uint32_t)px[0].y);
-      {
-        bool same = true;
-        for (int r = 0; r < c.cs; ++r) {
-          same = same && (uint32_t)px[r].y == (uint32_t)px[0].y;
-          mm = fmaxf(mm, __uint_as_float((uint32_t)px[r].y));
-          tie_enc = max(tie_enc, (uint32_t)(px[r].y >> 32));
+      // warp 0 combines the ranks, lane r taking rank r, and hands the
+      // result to the CTA through shared memory (every CTA computes the same
+      // answer from the same table, so it is cluster-uniform)
+      if (warp == 0) {
+        const bool has = lane < c.cs;
+        const ulonglong2 pr = has ? px[lane] : make_ulonglong2(0ull, 0ull);
+        const float mr_l = __uint_as_float((uint32_t)pr.y);
+        float mm_w = has ? mr_l : -INFINITY;
+        uint32_t te = has ? (uint32_t)(pr.y >> 32) : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          mm_w = fmaxf(mm_w, __shfl_xor_sync(FULL_MASK, mm_w, o));
+          te = max(te, __shfl_xor_sync(FULL_MASK, te, o));
         }
+        const bool same = __all_sync(FULL_MASK, !has || (uint32_t)pr.y == (uint32_t)px[0].y);
+        unsigned long long bw = has ? pr.x : 0ull;
         if (same) {
-          for (int r = 0; r < c.cs; ++r) best = px[r].x > best ? px[r].x : best;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long t = __shfl_xor_sync(FULL_MASK, bw, o);
+            bw = t > bw ? t : bw;
+          }
         } else {
-          float bl = 0.f;
-          for (int r = 0; r < c.cs; ++r) {
-            if (px[r].x == 0) continue;
-            const float t = Keys<float>::value_of_key(~(uint32_t)(px[r].x >> 32));
-            const float lr = log2f(t) + (mm - __uint_as_float((uint32_t)px[r].y)) * l2t;
-            if (best == 0 || lr < bl || (lr == bl && (uint32_t)px[r].x > (uint32_t)best)) {
-              bl = lr;
-              best = px[r].x;
+          // the smallest log2 race time wins, then the lowest id (the
+          // largest low word); ranks without a candidate carry +inf
+          float lr = INFINITY;
+          if (bw != 0) lr = log2f(Keys<float>::value_of_key(~(uint32_t)(bw >> 32))) + (mm_w - mr_l) * l2t;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const float lo2 = __shfl_xor_sync(FULL_MASK, lr, o);
+            const unsigned long long bo = __shfl_xor_sync(FULL_MASK, bw, o);
+            const bool take = bo != 0 && (bw == 0 || lo2 < lr || (lo2 == lr && (uint32_t)bo > (uint32_t)bw));
+            if (take) {
+              lr = lo2;
+              bw = bo;
             }
           }
         }
+        if (lane == 0) {
+          h.fin_best = bw;
+          h.fin_mm = mm_w;
+          h.fin_tie = te;
+        }
       }
+      __syncthreads();
+      unsigned long long best = h.fin_best;
+      const uint32_t tie_enc = h.fin_tie;
+      const float mm = h.fin_mm;
       // the max allowed id passes every filter, so best is 0 only when no id
       // is allowed (or none is finite)
       const bool uniform = best == 0;
@@ -1317,12 +1344,9 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sample_kernel(co
     const int bytes = n * (int)sizeof(T);
     const int bulk = bytes & ~15;
     const int nch = (bulk + kChunkBytes - 1) / kChunkBytes;
-    if (tid == 0) {
+    if (tid == 0) {                 // copies issued before the barrier, as in the fast path
       for (int i = 0; i < nch; ++i) mbar_init(&h.bar[i], 1);
       fence_mbar_init();
-    }
-    __syncthreads();
-    if (tid == 0) {
       for (int i = 0; i < nch; ++i) {
         const int off = i * kChunkBytes;
         const int sz = min(kChunkBytes, bulk - off);
@@ -1331,6 +1355,7 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sample_kernel(co
                  (uint32_t)sz, &h.bar[i]);
       }
     }
+    __syncthreads();
     for (int j = bulk / (int)sizeof(T) + tid; j < n; j += kSampThreads) slice_smem[j] = src[j];
     for (int i = 0; i < nch; ++i) mbar_wait_bounded(&h.bar[i], 0);
     __syncthreads();

@@ -221,6 +221,8 @@ struct SampHdr {
   int sel_aux;
   unsigned long long sel_val;
   unsigned long long zsum;
+  unsigned int tie_mine;                 // this CTA's count of the k-th key
+  long long tie_before;                  // that count over the lower ranks
   unsigned long long fin_best;           // the row's winning race key (warp 0's combine of the ranks)
   float fin_mm;                          // the largest rank bound
   uint32_t fin_tie;                      // the last kept tie over the ranks
@@ -1051,9 +1053,8 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sample_kernel(co
       }
 
       // ---- F3. this CTA's share of the lowest-index ties at the k-th key
-      // (slices are ordered by index, so lower ranks take theirs first).
-      // The exchange of the tie counts is also the barrier after which no
-      // peer reads this CTA's window any more.
+      // (slices are ordered by index, so lower ranks take theirs first), and
+      // the index of the last tie it keeps.
       int tie_lim = 0x7fffffff;
       int tie_cand = 0x7fffffff;   // index of this CTA's last kept tie, for the extras (INT_MAX: all kept)
       if (topk_on && need_eq < cnt_eq) {
@@ -1062,77 +1063,78 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sample_kernel(co
         auto tie_bits = [&](const uint4 u) -> uint32_t {
           return pass_bits<T>(u, ge_k) & (hi_ok ? ~pass_bits<T>(u, ge_k1) : 0xffu);
         };
-        int tn = 0;
-        for (int v = tid; v < nvec; v += kSampThreads) tn += __popc(tie_bits(sv[v]));
-        for (int j = rest + tid; j < n; j += kSampThreads) tn += K::key(bits_at(j)) == kth;
-        const unsigned long long mine = block_sum_u64((unsigned long long)tn, h.red);
+        unsigned long long mine;
         long long before = 0;
-        {
+        if (!windows_free) {
+          // The k-th key came from the window walk, so every rank's window
+          // bins still hold its exact count of that key (rank r's bin for
+          // row distance d is d - gap[r]): this CTA's ties and those of the
+          // lower ranks are read there, with no pass over the slice and no
+          // exchange.  Nothing below writes the window, so peers may go on
+          // reading it.
+          if (warp == 0) {                    // lane r reads rank r's bin (r <= this rank)
+            const int d = (int)(kmax - kth);
+            const int dr = lane <= (int)crank ? d - h.gap[lane] : -1;
+            unsigned int cnt_r = 0u;
+            if (dr >= 0) cnt_r = lane == (int)crank ? win[dr] : dsmem_ld_u32(dsmem_addr(&win[dr], (uint32_t)lane));
+            unsigned long long b = lane < (int)crank ? cnt_r : 0u;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) b += __shfl_xor_sync(FULL_MASK, b, o);
+            const unsigned int own = __shfl_sync(FULL_MASK, cnt_r, (int)crank);
+            if (lane == 0) {
+              h.tie_mine = own;
+              h.tie_before = (long long)b;
+            }
+          }
+          __syncthreads();
+          mine = h.tie_mine;
+          before = h.tie_before;
+        } else {
+          // the k-th key came from the radix selection (the window is gone):
+          // count the ties and exchange the counts
+          int tn = 0;
+          for (int v = tid; v < nvec; v += kSampThreads) tn += __popc(tie_bits(sv[v]));
+          for (int j = rest + tid; j < n; j += kSampThreads) tn += K::key(bits_at(j)) == kth;
+          mine = block_sum_u64((unsigned long long)tn, h.red);
           const ulonglong2* px = cluster_push(c, crank, mine, 0ull);
           for (int r = 0; r < (int)crank; ++r) before += (long long)px[r].x;
         }
-        windows_free = true;
         const long long want = min(max(need_eq - before, 0ll), (long long)mine);
-        // the tie list goes after the candidate list (or anywhere in the
-        // region once that list is gone)
-        uint32_t* tl = list_ok ? list + list_n : win;
-        const long long tcap = list_ok ? (long long)a.list_cap - list_n : (long long)a.list_cap + kWin1;
         if (want == 0) {
           tie_lim = -1;
-        } else if (want < (long long)mine && (long long)mine <= tcap) {
-          // ties in index order: each thread takes a contiguous run of
-          // words (the few ids past the last word go to the last thread),
-          // a block scan places the runs, and the want-th tie is the limit
+        } else if (want < (long long)mine) {
+          // The want-th tie in index order: each thread counts the ties in a
+          // contiguous run of words (the ids past the last word go to the
+          // last thread), a block scan places the runs, and the one thread
+          // whose run holds the want-th tie walks it to that id.
           const int per = (nvec + kSampThreads - 1) / kSampThreads;
           const int v0 = min(nvec, tid * per), v1 = min(nvec, v0 + per);
           int cnt = 0;
           for (int v = v0; v < v1; ++v) cnt += __popc(tie_bits(sv[v]));
           if (tid == kSampThreads - 1)
             for (int j = rest; j < n; ++j) cnt += K::key(bits_at(j)) == kth;
+          if (tid == 0) h.sel_aux = -1;       // ordered before the finder's write by the scan's barriers
           unsigned long long tot_t;
-          int pos = (int)block_excl_scan_u64((unsigned long long)cnt, h.red, tot_t);
-          for (int v = v0; v < v1; ++v) {
-            uint32_t tb = tie_bits(sv[v]);
-            while (tb) {
-              const int e = __ffs(tb) - 1;
-              tb &= tb - 1;
-              tl[pos++] = (uint32_t)(v * 8 + e);
+          const long long pos = (long long)block_excl_scan_u64((unsigned long long)cnt, h.red, tot_t);
+          if (pos < want && want <= pos + cnt) {
+            int r = (int)(want - pos);                    // 1-based rank inside this run
+            int at = -1;
+            for (int v = v0; v < v1 && at < 0; ++v) {
+              uint32_t tb = tie_bits(sv[v]);
+              const int c1 = __popc(tb);
+              if (r > c1) {
+                r -= c1;
+                continue;
+              }
+              for (int q = 1; q < r; ++q) tb &= tb - 1;
+              at = v * 8 + __ffs(tb) - 1;
             }
+            for (int j = rest; at < 0 && j < n; ++j)       // the last thread's tail ids
+              if (K::key(bits_at(j)) == kth && --r == 0) at = j;
+            h.sel_aux = at;
           }
-          if (tid == kSampThreads - 1)
-            for (int j = rest; j < n; ++j)
-              if (K::key(bits_at(j)) == kth) tl[pos++] = (uint32_t)j;
           __syncthreads();
-          tie_lim = (int)tl[want - 1];
-        } else if (want < (long long)mine) {
-          // too many ties for the free space: local radix select over the
-          // tie indices, in bins that overlay the region
-          list_ok = false;
-          uint32_t prefix = 0;
-          unsigned long long remaining = (unsigned long long)want;
-          for (int shift = 16; shift >= 0; shift -= 8) {       // 24-bit slice-local indices
-            for (int i = tid; i < kHistCopies * 256; i += kSampThreads) (&hist[0][0])[i] = 0ull;
-            __syncthreads();
-            const uint32_t hi_mask = (shift + 8 >= 24) ? 0u : ((~0u << (shift + 8)) & 0xffffffu);
-            visit<T>(slice_smem, n, true, [&](int j, uint32_t b) {
-              if (K::key(b) != kth) return;
-              const uint32_t ik = 0xffffffu - (uint32_t)j;
-              if ((ik & hi_mask) == (prefix & hi_mask))
-                atomicAdd(reinterpret_cast<unsigned int*>(&hist[copy][(ik >> shift) & 255u]), 1u);
-            });
-            __syncthreads();
-            if (tid < 256) {
-              unsigned long long s2 = 0;
-              for (int cp = 0; cp < kHistCopies; ++cp) s2 += (unsigned int)(hist[cp][tid] & 0xffffffffull);
-              h.tot[tid] = s2;
-            }
-            __syncthreads();
-            select_bin<true>(h, remaining, false);
-            remaining -= h.sel_before;
-            prefix |= (uint32_t)h.sel_bin << shift;
-            __syncthreads();
-          }
-          tie_lim = (int)(0xffffffu - prefix);
+          tie_lim = h.sel_aux;
         }
         tie_cand = want == 0 ? -1 : (want == (long long)mine ? lo + n - 1 : lo + tie_lim);
       }

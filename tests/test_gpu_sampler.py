@@ -180,6 +180,35 @@ def test_window_fallback_when_top_k_lies_below_the_window():
     assert set(tok.tolist()) == ref
 
 
+def test_radix_top_k_ties_straddle_ranks():
+    """A k-th value too far below the max for the window (radix selection),
+    held by a tie group that starts inside one rank's slice and runs on into
+    the next: the lowest-index ties are kept across the rank boundary."""
+    pk = require_gpu()
+    V, R = 151936, 64
+    x = torch.full((V,), -60000.0)
+    x[70000:] = -30000.0
+    top = [7, 100000, 151000]
+    x[top] = 65000.0
+    t = 8000
+    k = len(top) + t
+    logits = x.to(torch.float16).unsqueeze(0).repeat(R, 1).to(DEV)
+    seeds = torch.arange(R, dtype=torch.int64) * 31 + 5
+    offs = torch.arange(R, dtype=torch.int64)
+    T = 1e6
+    tok = pk.sample(logits, torch.full((R,), T, device=DEV), torch.full((R,), k, dtype=torch.int32, device=DEV),
+                    torch.ones(R, device=DEV), seeds.to(DEV), offs.to(DEV)).cpu().numpy()
+    xd = x.to(torch.float16).double().numpy()
+    allowed = set(oracle.sampler.topk_set(xd, k).tolist())
+    assert sorted(a for a in allowed if a not in top) == list(range(70000, 70000 + t))
+    assert set(tok.tolist()) <= allowed
+    assert max(int(a) for a in tok if a not in top) > 76000     # past a two-way split of the row
+    for i in range(8):
+        ref, info = oracle.sampler.sample_row(xd, float(np.float32(T)), k, 1.0, int(seeds[i]), int(offs[i]),
+                                              return_info=True)
+        assert int(tok[i]) == ref or _exempt(info, 1.0)
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 def test_unaligned_rows_stochastic_match_oracle(dtype):
     """Rows that cannot be bulk-copied take the generic radix path."""

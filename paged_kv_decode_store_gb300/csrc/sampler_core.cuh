@@ -35,8 +35,10 @@
 //   and scored evenly by all threads; the generic path queues them per warp.
 //   Either way Philox and the logarithms run on full warps.
 // * Ties at the k-th key straddling the cut: slices are ordered by index, so
-//   each CTA takes its share of the lowest-index ties and resolves it with a
-//   local radix select over its tie indices.
+//   each CTA takes its share of the lowest-index ties.  For 16-bit logits the
+//   shares come from the window bins and the one CTA whose share ends inside
+//   its ties finds that tie by a block scan of per-thread runs; the generic
+//   path resolves its share with a local radix select over its tie indices.
 #pragma once
 
 #include <type_traits>

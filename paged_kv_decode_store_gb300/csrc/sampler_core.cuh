@@ -31,8 +31,9 @@
 //   select with cluster-summed histograms instead.
 // * Gumbel pass: only ids that can win are considered (x'_j >= max x' - 21,
 //   since u lies in [2^-24, 1 - 2^-24] and g in [-2.81, 16.64]).  For 16-bit
-//   logits the candidates are compacted in index order into one list per CTA
-//   and scored evenly by all threads; the generic path queues them per warp.
+//   logits the candidates are compacted into one list per CTA (in no
+//   particular order: the race is a max of keys that carry the id) and
+//   scored evenly by all threads; the generic path queues them per warp.
 //   Either way Philox and the logarithms run on full warps.
 // * Ties at the k-th key straddling the cut: slices are ordered by index, so
 //   each CTA takes its share of the lowest-index ties.  For 16-bit logits the

@@ -818,10 +818,17 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sample_kernel(co
           zc = (t - zs) - y;
           zs = t;
         };
+        // each word's pass mask is kept (one byte per word, at the far end
+        // of the list's space) so that the write pass reads it instead of
+        // comparing the word again; the list may use the space before it
+        const int list_room = a.list_cap - (nvec + 3) / 4;
+        uint8_t* wmask = reinterpret_cast<uint8_t*>(list + list_room);
         int hits = 0;
         for (int v = tid; v < nvec; v += kSampThreads) {
           const uint4 u = sv[v];
-          hits += __popc(pass_bits<T>(u, t1v2));
+          const uint32_t cb = pass_bits<T>(u, t1v2);
+          wmask[v] = (uint8_t)cb;
+          hits += __popc(cb);
           if (need_z) {
             const uint32_t w[4] = {u.x, u.y, u.z, u.w};
             float vs = 0.f;
@@ -841,12 +848,12 @@ __global__ void __launch_bounds__(kSampThreads, kSampCtasPerSm) sample_kernel(co
         unsigned long long tot_u;
         const int first = (int)block_excl_scan_u64((unsigned long long)hits, h.red, tot_u);
         list_n = (int)tot_u;
-        list_ok = list_n <= a.list_cap;
+        list_ok = list_n <= list_room;
         if (list_ok) {
           if (hits > 0) {
             int kk = first;
             for (int v = tid; v < nvec; v += kSampThreads) {
-              uint32_t cb = pass_bits<T>(sv[v], t1v2);
+              uint32_t cb = wmask[v];
               while (cb) {
                 const int e = __ffs(cb) - 1;
                 cb &= cb - 1;

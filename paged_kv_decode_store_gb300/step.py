@@ -182,14 +182,34 @@ class DecodeStep:
         L = _capi.lib()
         s = _capi.stream_handle(None, self.q)
         self._enqueue_kv_attention(L, s)
+        # the attention output goes back to the host on a third stream,
+        # beside the sampler (which does not touch it); the sampler's
+        # outputs follow on this stream, which then joins the third
+        out_side = self._side2
+        out_side.wait_stream(cur)
+        n_out = self._out_bytes("out")
+        with torch.cuda.stream(out_side):
+            h["_out"][:n_out].copy_(self.outputs[:n_out], non_blocking=True)
         cur.wait_stream(side)
         self._enqueue_sample(L, s)
-        h["_out"].copy_(self.outputs, non_blocking=True)
+        h["_out"][n_out:].copy_(self.outputs[n_out:], non_blocking=True)
+        cur.wait_stream(out_side)
+
+    def _out_bytes(self, name: str) -> int:
+        """End offset of output `name` in the output arena (the first field
+        starts at 0, so this is where the fields after it begin)."""
+        for n, _shape, _dtype, off, nbytes in self._out_layout:
+            if n == name:
+                return off + (nbytes + 255) // 256 * 256
+        raise KeyError(name)
 
     def capture_host(self) -> None:
         """Record a host-staged step (one input copy, the logits copy on a
-        second stream, the kernels, one output copy) into a CUDA graph."""
+        second stream, the kernels, the attention output's copy on a third
+        stream beside the sampler, then the sampler's outputs) into a CUDA
+        graph."""
         self._side = torch.cuda.Stream(device=self.q.device)
+        self._side2 = torch.cuda.Stream(device=self.q.device)
         warm = torch.cuda.Stream(device=self.q.device)
         warm.wait_stream(torch.cuda.current_stream(self.q.device))
         with torch.cuda.stream(warm):

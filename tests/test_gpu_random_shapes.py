@@ -138,3 +138,42 @@ def test_random_sampler_rows_match_oracle(seed):
                 assert sampling_exempt(info, float(P[r])), (V, str(dt), float(T[r]), int(K[r]), float(P[r]))
                 exempt += 1
     assert exempt <= max(2, rows // 100)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_random_prefill_batches_match_oracle(seed):
+    """Varlen prefill (store bit-exact, attention on every (token, head)) over
+    random head counts, groups up to 16, head_dim, block sizes 8-256, query
+    lengths, cached prefixes (private or shared) and windows, on the
+    tensor-core paths for 16-bit caches and the CUDA-core path for fp32."""
+    from workloads import prefill as wp
+    from test_gpu_prefill import oracle_cache, to_f64, run_prefill, check_rows
+    from gpu_helpers import raw_numpy
+    pk = require_gpu()
+    rng = np.random.default_rng(8000 + seed)
+    for i in range(8):
+        dtype = str(rng.choice(["bf16", "f16", "f32"], p=[0.45, 0.45, 0.1]))
+        hkv = int(rng.choice([1, 2, 4, 8]))
+        B = int(rng.integers(1, 5))
+        cfg = wp.PrefillConfig(name="random", index=600 + seed * 100 + i, num_seqs=B,
+                               num_q_heads=hkv * int(rng.choice([1, 2, 3, 4, 6, 8, 16])), num_kv_heads=hkv,
+                               head_dim=int(rng.choice([64, 128])), block_size=int(rng.choice([8, 16, 32, 64, 128, 256])),
+                               dtype=dtype, q_kind="fixed",
+                               q_args=tuple(int(x) for x in rng.integers(1, int(rng.choice([2, 40, 300])), B)),
+                               hit_kind="fixed", hit_args=tuple(int(x) for x in rng.integers(0, 4, B)),
+                               prefix_kind=str(rng.choice(["private", "shared"])))
+        b = wp.make_prefill_batch(cfg)
+        window = int(rng.choice([0, 0, 1, 33, 200]))
+        k_ref, v_ref, slots_ref = oracle_cache(b)
+        dt = b.cache.dtype
+        ref = oracle.prefill.prefill_attention(b.q.double().numpy(), to_f64(k_ref, dt), to_f64(v_ref, dt),
+                                               b.block_tables, b.cu_seqlens_q, b.cu_seqlens_k, b.scale, window=window)
+        T, Hq, _ = ref.shape
+        for path in (["fma"] if dtype == "f32" else ["tc", "mma"]):
+            cache, slots, out, err = run_prefill(pk, b, window=window,
+                                                 path={"tc": pk.PATH_TC, "mma": pk.PATH_MMA, "fma": pk.PATH_FMA}[path])
+            assert err == 0, (cfg, window, path)
+            np.testing.assert_array_equal(slots, slots_ref)
+            np.testing.assert_array_equal(raw_numpy(cache[0]), k_ref)
+            np.testing.assert_array_equal(raw_numpy(cache[1]), v_ref)
+            check_rows(out.double().numpy(), ref, [(t, h) for t in range(T) for h in range(Hq)], f32=dtype == "f32")

@@ -177,3 +177,46 @@ def test_random_prefill_batches_match_oracle(seed):
             np.testing.assert_array_equal(raw_numpy(cache[0]), k_ref)
             np.testing.assert_array_equal(raw_numpy(cache[1]), v_ref)
             check_rows(out.double().numpy(), ref, [(t, h) for t in range(T) for h in range(Hq)], f32=dtype == "f32")
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_random_sample_ex_rows_match_oracle(seed):
+    """The sampler extras over random vocabularies (16-byte rows, which a
+    mask needs), dtypes, masks from all-allowed to nearly-all-masked, and cut
+    parameters: ids, token_prob and the top-8 against the oracle."""
+    pk = require_gpu()
+    rng = np.random.default_rng(9000 + seed)
+    for _ in range(10):
+        V = int(rng.choice([8, 96, 1000, 5000, 32000, 65536, 151936]))
+        R = int(rng.integers(1, 32 if V <= 5000 else 8))
+        dt = [torch.float32, torch.float16, torch.bfloat16][int(rng.integers(3))]
+        x = (rng.standard_normal((R, V)) * float(rng.choice([0.5, 2.0, 3.0, 8.0]))).astype(np.float32)
+        if rng.random() < 0.3:
+            x = np.round(x * 4) / 4
+        logits = torch.from_numpy(x).to(dt)
+        T = rng.choice([0.0, 0.6, 1.0, 1.4], R).astype(np.float32)
+        K = rng.choice([0, 1, 5, 50, 300], R).astype(np.int32)
+        P = rng.choice([1.0, 0.95, 0.9, 0.5], R).astype(np.float32)
+        allowed = rng.random((R, V)) > rng.choice([0.0, 0.0, 0.3, 0.9, 0.999], R)[:, None]
+        S = rng.integers(0, 2**62, R, dtype=np.int64)
+        O = rng.integers(0, 2**30, R, dtype=np.int64)
+        tok, tp, p8, i8 = pk.sample_ex(logits.to(DEV), torch.from_numpy(T).to(DEV), torch.from_numpy(K).to(DEV),
+                                       torch.from_numpy(P).to(DEV), torch.from_numpy(S).to(DEV),
+                                       torch.from_numpy(O).to(DEV), mask_words=pk.pack_mask(torch.from_numpy(allowed)).to(DEV))
+        tok, tp, p8, i8 = tok.cpu().numpy(), tp.cpu().numpy(), p8.cpu().numpy(), i8.cpu().numpy()
+        xd = logits.double().numpy()
+        for r in range(R):
+            if not allowed[r].any():
+                assert 0 <= tok[r] < V
+                continue
+            (rt, rp, r8p, r8i), info = oracle.sampler.sample_outputs(xd[r], float(T[r]), int(K[r]), float(P[r]),
+                                                                      int(S[r]), int(O[r]), mask=allowed[r],
+                                                                      return_info=True)
+            if int(tok[r]) != rt:
+                assert sampling_exempt(info, float(P[r]))
+                continue
+            assert allowed[r, tok[r]]
+            np.testing.assert_allclose(tp[r], rp, rtol=1e-5, atol=1e-30)
+            nv = min(8, V)
+            assert i8[r][:nv].tolist() == r8i[:nv].tolist()
+            np.testing.assert_allclose(p8[r][:nv], r8p[:nv], rtol=1e-5, atol=1e-30)
